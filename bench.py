@@ -1,0 +1,509 @@
+#!/usr/bin/env python
+"""Benchmark of the routed multi-tenant LoRA delta on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one ``lora_delta_fused`` call (the whole hot path: routing, shrink,
+expand + fold) on one decode batch of the "decode BGMV qkv" workload: 64 rows,
+k_in 4096, output slices (4096, 1024, 1024), 16 adapter slots of rank 16, 10%
+unrouted rows.  Inputs are seeded synthetic data already resident in HBM; each
+step uses the next of C rotating copies of (pool, x, out, seq_slot) whose total
+is more than twice the L2, so the adapter bytes come from HBM.  The K timed
+steps are one CUDA graph, timed with CUDA events on the launching stream.
+
+Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs its own
+batch with the pool replicated (rows are independent: no collective on the
+data path), and the slowest rank's time is used.
+
+``--impl reference`` times the CPU oracle (the plain C reference) on the same
+workload, on this machine's host cores, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-delta rows/s; BGMV HBM GB/s and SGMV TFLOP/s as % of GB300 roofline"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        rows = []
+        for ts, line in self.lines:
+            if t0 is not None and (ts < t0 or ts > t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------- the workloads --
+
+def algorithmic_bytes(case, rows_mask=None):
+    """HBM bytes the delta must move for one call: each routed slot's A and B
+    once (at the padded rank), x of the routed rows, out read + write of the
+    routed rows' columns."""
+    import numpy as np
+    seq = case.seq_slot if rows_mask is None else case.seq_slot[rows_mask]
+    routed = (seq >= 0) & (seq < case.max_loras)
+    slots = np.unique(seq[routed])
+    n_routed = int(routed.sum())
+    per_slot = 0
+    for s in slots:
+        ad = case.adapters[s]
+        for j, w in enumerate(case.widths):
+            if ad is not None and ad.adapted[j]:
+                per_slot += case.max_rank * case.k_in * 2 + w * case.max_rank * 2
+    cols = sum(case.widths)
+    return per_slot + n_routed * case.k_in * 2 + n_routed * cols * 2 * 2
+
+
+def algorithmic_flops(case):
+    seq = case.seq_slot
+    routed = int(((seq >= 0) & (seq < case.max_loras)).sum())
+    S = len(case.widths)
+    return routed * 2 * case.max_rank * (S * case.k_in + sum(case.widths))
+
+
+def l2_bytes():
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 126 * 1024 * 1024
+
+
+def make_copies(ld, di, case, copies, device):
+    """``copies`` independent device copies of (pool, x, out, seq_slot)."""
+    import torch
+    base = di.linear_to_device(case, device)
+    out = []
+    for c in range(copies):
+        if c == 0:
+            pool = base.pool
+        else:
+            pool = ld.LoraPool(case.k_in, case.widths, case.max_loras, case.max_rank,
+                               device=device)
+            for j in range(pool.S):
+                pool.A[j].copy_(base.pool.A[j])
+                pool.B[j].copy_(base.pool.B[j])
+            pool.scale_table.copy_(base.pool.scale_table)
+            L = case.max_loras
+            a_host = [0] * (pool.S * L)
+            b_host = [0] * (pool.S * L)
+            at = base.pool.a_table.cpu().tolist()
+            for j in range(pool.S):
+                for s in range(L):
+                    if at[j * L + s]:
+                        a_host[j * L + s] = pool.A[j][s].data_ptr()
+                        b_host[j * L + s] = pool.B[j][s].data_ptr()
+            pool.a_table.copy_(torch.tensor(a_host, dtype=torch.int64))
+            pool.b_table.copy_(torch.tensor(b_host, dtype=torch.int64))
+        out.append(dict(pool=pool, x=base.x.clone(), out=base.out0.clone(),
+                        seq=base.seq_slot.clone()))
+    torch.cuda.synchronize(device)
+    return out
+
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import lora_delta_gb300 as ld
+    from lora_delta_gb300 import device_inputs as di
+    from lora_delta_gb300 import dist as ldist
+    from lora_delta_gb300 import inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    ld.lib()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+
+    case = inputs.decode_qkv_case(seed=1235 + 1000 * rank)
+    n = case.n
+    per_copy = (case.max_loras * sum(case.max_rank * case.k_in * 2 + w * case.max_rank * 2
+                                      for w in case.widths)
+                + n * case.k_in * 2 + n * case.ld_out * 2 + n * 4)
+    copies = max(2, int(np.ceil(2.2 * l2_bytes() / per_copy)))
+    bufs = make_copies(ld, di, case, copies, device)
+    stream = torch.cuda.Stream(device)
+    K, W = args.steps, args.warmup
+
+    def step(k):
+        b = bufs[k % copies]
+        return lambda: ld.lora_delta_fused(b["out"], b["x"], b["seq"], b["pool"])
+
+    # warm-up: W eager steps (also the first use of every copy)
+    with torch.cuda.stream(stream):
+        for k in range(max(W, copies)):
+            step(k)()
+    torch.cuda.synchronize(device)
+
+    # the K timed steps as one CUDA graph
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(K):
+            step(k)()
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # untimed pre-roll so that clocks settle and the sampler sees the load
+    t_pre = time.time()
+    n_pre = 0
+    while time.time() - t_pre < 0.4 or n_pre < 1:
+        g.replay()
+        torch.cuda.synchronize(device)
+        n_pre += 1
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ldist.barrier()
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    ldist.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    sampler.stop()
+    clocks = sampler.summary(t_pre, t_wall1)
+    ms_total = ldist.max_over_ranks(ms_total, device)
+    ms_step = ms_total / K
+    total_rows = ldist.sum_over_ranks(n * K, device)
+    value = total_rows / (ms_total / 1e3)
+
+    # roofline of the dominant (only) kernel of the step
+    abytes = algorithmic_bytes(case)
+    achieved = abytes / (ms_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "traffic": None, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": abytes,
+                "kernel": "delta_cluster_kernel<16,fused,LinearTables>"}
+
+    # eager (no graph) timing of the same K steps, for context
+    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev2.record(stream)
+        for k in range(K):
+            step(k)()
+        ev3.record(stream)
+    torch.cuda.synchronize(device)
+    eager_ms = ev2.elapsed_time(ev3) / K
+
+    e2e = run_e2e(ld, di, case, bufs, copies, K, W, device)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init adapters)",
+        "config": {"workload": case.name, "rows_per_step": n, "k_in": case.k_in,
+                   "output_slices": list(case.widths), "max_loras": case.max_loras,
+                   "max_rank": case.max_rank, "unrouted_rows": int((case.seq_slot < 0).sum()),
+                   "l2": f"{copies} rotating copies of pool/x/out/seq_slot "
+                         f"({copies * per_copy / 2**20:.0f} MiB > 2x L2)",
+                   "timing": "one CUDA graph of K steps, CUDA events on the launching stream",
+                   "parallelism": f"dp{world} (rows sharded, pool replicated)"},
+        "roofline": roofline,
+        "eager_ms_per_step": round(eager_ms, 6),
+        "e2e": e2e,
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(case)
+        if not args.no_extra:
+            line["other_workloads"] = other_workloads(ld, di, inputs, device, hbm_peak,
+                                                      bf16_peak, peak_src)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(ld, di, case, bufs, copies, K, W, device):
+    """The same metric through the public API with host buffers: per step one
+    pinned host->device copy of (x, out, seq_slot), the call, and one
+    device->host copy of the updated out."""
+    import torch
+    n = case.n
+    x_b, o_b, s_b = n * case.k_in * 2, n * case.ld_out * 2, n * 4
+    align = lambda v: (v + 255) // 256 * 256
+    total = align(x_b) + align(o_b) + align(s_b)
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    host[:x_b].copy_(bufs[0]["x"].view(torch.uint8).view(-1).cpu())
+    host[align(x_b):align(x_b) + o_b].copy_(bufs[0]["out"].view(torch.uint8).view(-1).cpu())
+    host[align(x_b) + align(o_b):align(x_b) + align(o_b) + s_b].copy_(
+        bufs[0]["seq"].view(torch.uint8).view(-1).cpu())
+    host_out = torch.empty(o_b, dtype=torch.uint8).pin_memory()
+    dev = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(copies)]
+    views = []
+    for d in dev:
+        x = d[:x_b].view(torch.bfloat16).view(n, case.k_in)
+        o = d[align(x_b):align(x_b) + o_b].view(torch.bfloat16).view(n, case.ld_out)
+        s = d[align(x_b) + align(o_b):align(x_b) + align(o_b) + s_b].view(torch.int32)
+        views.append((d, x, o, s))
+    stream = torch.cuda.Stream(device)
+
+    def step(k):
+        d, x, o, s = views[k % copies]
+        d.copy_(host, non_blocking=True)
+        ld.lora_delta_fused(o, x, s, bufs[k % copies]["pool"])
+        host_out.copy_(d[align(x_b):align(x_b) + o_b], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(max(W, 3)):
+            step(k)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(K):
+            step(k)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / K
+    return {"value": round(n / (ms / 1e3), 1), "unit": "rows/s", "ms_per_step": round(ms, 6),
+            "h2d_bytes_per_step": total, "d2h_bytes_per_step": o_b,
+            "path": "pinned host -> device copy, lora_delta_fused, device -> pinned host"}
+
+
+def cpu_baseline(case, budget_s: float = 10.0):
+    """The CPU oracle as it stands, on this machine's host cores."""
+    import numpy as np
+
+    import oracle
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, case.max_loras,
+                             case.max_rank)
+    out = case.out0.copy()
+    oracle.delta(out, case.x, case.seq_slot, pool)  # untimed first call
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.delta(out, case.x, case.seq_slot, pool)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 2000:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(reps * case.n / dt, 1), "unit": "rows/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{reps} repetitions of the full {case.n}-row decode batch "
+                      f"({dt:.1f} s, OpenMP over rows, {cores} threads)"}
+
+
+def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src):
+    """The other workloads of the path, each timed on its own (not the headline)."""
+    import numpy as np
+    import torch
+    res = {}
+    stream = torch.cuda.Stream(device)
+
+    def timed(fn, reps=5, warm=2):
+        with torch.cuda.stream(stream):
+            for _ in range(warm):
+                fn()
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps
+
+    # prefill SGMV gate_up (8192 rows)
+    case = inputs.prefill_gate_up_case()
+    d = di.linear_to_device(case, device)
+    ws = torch.empty(ld.lora_workspace_size(case.n, case.max_loras), dtype=torch.uint8,
+                     device=device)
+    ms = timed(lambda: ld.lora_delta_fused(d.out0, d.x, d.seq_slot, d.pool, workspace=ws))
+    ab, fl = algorithmic_bytes(case), algorithmic_flops(case)
+    gbs, tfs = ab / (ms / 1e3) / 1e9, fl / (ms / 1e3) / 1e12
+    attain = min(bf16_peak, fl / ab * hbm_peak / 1e3)
+    res["prefill_gate_up"] = {"rows_per_s": round(case.n / (ms / 1e3), 1), "ms": round(ms, 4),
+                              "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+                              "TFLOP_per_s": round(tfs, 2),
+                              "tensor_frac": round(tfs / bf16_peak, 5),
+                              "attainable_TFLOP_per_s": round(attain, 1),
+                              "roofline_frac": round(tfs / attain, 4),
+                              "launches_per_call": 2}
+    del d, ws
+    torch.cuda.empty_cache()
+
+    # skewed many-adapter decode: both projections per step
+    c1, c2 = inputs.skewed_case(0), inputs.skewed_case(1)
+    d1, d2 = di.linear_to_device(c1, device), di.linear_to_device(c2, device)
+    ms = timed(lambda: (ld.lora_delta_fused(d1.out0, d1.x, d1.seq_slot, d1.pool),
+                        ld.lora_delta_fused(d2.out0, d2.x, d2.seq_slot, d2.pool)))
+    ab = algorithmic_bytes(c1) + algorithmic_bytes(c2)
+    res["skewed_decode"] = {"rows_per_s": round(c1.n / (ms / 1e3), 1), "ms": round(ms, 4),
+                            "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
+                            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                            "launches_per_call": 2}
+    del d1, d2
+    torch.cuda.empty_cache()
+
+    # MoE FC1 (regular and shared-A / fused-B)
+    for shared in (False, True):
+        mc = inputs.moe_case(shared_a=shared)
+        dm = di.moe_to_device(mc, device)
+        out = torch.empty(mc.T, mc.top_k, 2 * mc.I, dtype=torch.bfloat16, device=device)
+        ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L),
+                         dtype=torch.uint8, device=device)
+        ms = timed(lambda: ld.lora_moe_fc1_delta(out, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b,
+                                                 dm.stride_b, shared, dm.topk_ids, dm.lora_ids,
+                                                 mc.E, mc.I, mc.rank, mc.L, mc.scale,
+                                                 workspace=ws))
+        valid = mc.lora_ids >= 0
+        pairs = int(valid.sum()) * mc.top_k
+        keys = {(int(l), int(e)) for t in np.flatnonzero(valid) for l, e in
+                zip([mc.lora_ids[t]] * mc.top_k, mc.topk_ids[t])}
+        n_a = 1 if shared else 2
+        bank = len(keys) * (n_a * mc.rank * mc.H * 2 + 2 * mc.I * mc.rank * 2)
+        ab = bank + mc.T * mc.top_k * 2 * mc.I * 2 + int(valid.sum()) * mc.H * 2
+        res["moe_fc1_" + ("shared" if shared else "regular")] = {
+            "pairs_per_s": round(mc.T * mc.top_k / (ms / 1e3), 1), "ms": round(ms, 4),
+            "routed_pairs": pairs, "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
+            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 3}
+        del dm, out, ws
+        torch.cuda.empty_cache()
+    res["peak_source"] = peak_src
+    return res
+
+
+# ---------------------------------------------------------- reference arm --
+
+def run_reference(args, rank, world):
+    """The CPU oracle on the same workload (rank 0 only), bounded per step."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from lora_delta_gb300 import inputs
+    case = inputs.decode_qkv_case()
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, case.max_loras,
+                             case.max_rank)
+    out = case.out0.copy()
+    t0 = time.perf_counter()
+    oracle.delta(out, case.x, case.seq_slot, pool)
+    t_full = time.perf_counter() - t0
+    K, W = args.steps, args.warmup
+    budget = 60.0
+    rows = int(np.clip(case.n * budget / max(1e-9, (K + W) * t_full), 1, case.n))
+    x, seq, o = case.x[:rows].copy(), case.seq_slot[:rows].copy(), case.out0[:rows].copy()
+    for _ in range(W):
+        oracle.delta(o, x, seq, pool)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle.delta(o, x, seq, pool)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    value = rows * K / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "rows/s",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(dt / K * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; random-init adapters)",
+            "config": {"workload": case.name, "rows_per_step": rows},
+            "cpu_baseline": {"value": round(value, 1), "unit": "rows/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"first {rows} rows of the decode batch per step"},
+            "e2e": {"value": round(value, 1), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads (prefill, skewed, MoE)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from lora_delta_gb300 import dist as ldist
+    rank, world = ldist.init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

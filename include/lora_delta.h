@@ -1,0 +1,203 @@
+/*
+ * lora_delta.h -- C ABI of the GB300 (sm_103a) routed multi-tenant LoRA delta.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensors are caller-owned DEVICE memory unless an argument says
+ *    "host".  bf16 tensors are row-major with the stated leading dimension.
+ *  - Launchers only enqueue work on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream): they allocate nothing and never synchronize
+ *    ("Module lora_delta", module invariants).  The one exception is
+ *    lora_get_error, which waits on `stream` to read the error word back.
+ *  - Return value: LORA_OK (0) or a host-detected LORA_ERR_* status; an error
+ *    status means nothing was enqueued.  Nothing is ever thrown.
+ *  - Device-detected problems never trap: the offending row / pair is handled
+ *    as stated per call and a LORA_DEV_ERR_* bit is OR-ed into the caller's
+ *    `err_word` (a device uint32, may be NULL to ignore).  Read it with
+ *    lora_get_error.
+ *  - Alignment: k_in, every slice width, ld_out, offset_start and the pool
+ *    rank R must be multiples of 8 elements (16 bytes of bf16), and x / out /
+ *    h must be 16-byte aligned; otherwise LORA_ERR_ALIGN.  A pool address in a
+ *    device table that is not 16-byte aligned is found on the device: that
+ *    slice is skipped and LORA_DEV_ERR_ALIGN is set.
+ *  - Limits: 1 <= S <= 8 slices, 8 <= R <= 128, S*R <= 512, max_loras <= 3071
+ *    (LORA_ERR_UNSUPPORTED beyond).
+ *
+ * Pages the calls follow (cited per call below):
+ *  [punica]     "vllm/lora/punica_wrapper/punica_base.py": add_shrink,
+ *               add_expand, add_lora_linear "Semantics"; prefill_metadata.
+ *  [sharded]    "vllm.lora.fully_sharded_layers": the float32 shrink buffer
+ *               and the shrink-with-scale-1.0 then expand sequence.
+ *  [metrale]    "Module lora_delta": LoraPair / LoraRoute layouts, the
+ *               padded-rank invariant, apply_lora_bgmv, the scale rule.
+ *  [flashinfer] "flashinfer.fused_moe.bgmv_moe_gemm1_lora_delta".
+ */
+#ifndef LORA_DELTA_H
+#define LORA_DELTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
+
+/* host-detected status codes */
+#define LORA_OK 0
+#define LORA_ERR_ARG 1         /* NULL pointer, negative size, bad flag        */
+#define LORA_ERR_SHAPE 2       /* inconsistent sizes                           */
+#define LORA_ERR_ALIGN 3       /* a size or pointer breaks the 16-byte rule    */
+#define LORA_ERR_CUDA 4        /* a CUDA launch or copy failed                 */
+#define LORA_ERR_WORKSPACE 5   /* workspace missing or smaller than required   */
+#define LORA_ERR_UNSUPPORTED 6 /* outside the limits stated above              */
+
+/* device-detected bits, OR-ed into *err_word */
+#define LORA_DEV_ERR_SLOT 1u    /* seq_slot >= max_loras: the row gets no delta        */
+#define LORA_DEV_ERR_EXPERT 2u  /* MoE expert id outside [0, E): pair written as zeros */
+#define LORA_DEV_ERR_LORA 4u    /* MoE adapter id >= num_loras: pair written as zeros  */
+#define LORA_DEV_ERR_TIMEOUT 8u /* a bounded wait inside a kernel gave up              */
+#define LORA_DEV_ERR_ALIGN 16u  /* a table address is not 16-byte aligned: slice skipped */
+
+/* Human-readable name of a status code (static string). */
+const char *lora_status_string(int status);
+
+/* ABI version of this library (bumped on any signature change). */
+int lora_abi_version(void);
+
+/*
+ * lora_scale -- the adapter scale ([metrale] LoraPair): alpha / r, or
+ * alpha / sqrt(r) when use_rslora is nonzero.  Computed on the host; the
+ * caller stores it in its scale table.  Applied in the fold (after the
+ * expand's rank contraction), never folded into B.  r <= 0 gives 0.
+ */
+float lora_scale(float alpha, int r, int use_rslora);
+
+/*
+ * lora_pool_pack -- pack one PEFT adapter into one padded pool slot
+ * ([metrale] module invariants + LoraPair).
+ *   a_slot [R, k_in] bf16 (out): rows 0..r-1 = a_r, rows r..R-1 = 0.
+ *   b_slot [w, R]    bf16 (out): columns 0..r-1 of each row = b_r, r..R-1 = 0.
+ *   a_r    [r, k_in] bf16 (in) : PEFT lora_A, row-major.
+ *   b_r    [w, r]    bf16 (in) : PEFT lora_B, row-major.
+ * Every element of both slots is written (the zero padding is what lets both
+ * stages contract at R).  The caller then stores a_slot / b_slot in its
+ * a_table / b_table.  Errors: LORA_ERR_ARG (r < 0, r > R, NULL), ALIGN.
+ */
+int lora_pool_pack(void *a_slot, void *b_slot, const void *a_r, const void *b_r, int r, int R,
+                   int k_in, int w, lora_stream_t stream);
+
+/*
+ * Routing tables shared by the linear calls ([metrale] LoraRoute):
+ *   a_table, b_table [S * max_loras] uint64 (device): entry j*max_loras + s
+ *     is the device address of slot s's A_j [R, k_in] (resp. B_j [w_j, R])
+ *     pool region, 0 when slot s does not adapt slice j.
+ *   scale_table [max_loras] float (device), or NULL for scale 1.
+ *   seq_slot [n] int32 (device): the row's slot; negative = no delta
+ *     ([metrale] apply_lora_bgmv); >= max_loras = no delta + LORA_DEV_ERR_SLOT.
+ *   widths [S] int32 (HOST): the output slice widths; slice j's columns start
+ *     at offset_start + widths[0] + ... + widths[j-1] ([punica] add_expand).
+ *
+ * Workspace: when n > 1024 the rows are first clustered by slot on the
+ * device (a stable counting sort, [punica] prefill_metadata) into a
+ * caller-provided scratch buffer of lora_workspace_size(n, max_loras) bytes,
+ * 256-byte aligned.  For n <= 1024 each kernel clusters its own rows and the
+ * workspace may be NULL.
+ */
+size_t lora_workspace_size(int n, int max_loras);
+
+/*
+ * lora_route -- the routing step on its own ([punica] prefill_metadata):
+ * a stable clustering of the n rows by slot.
+ *   perm      [n] int32 (out): perm[0 .. seg_start[max_loras]) are the rows
+ *             with 0 <= slot < max_loras, by ascending slot, then ascending
+ *             row index; entries past that are unspecified.
+ *   seg_start [max_loras + 2] int32 (out): cluster s is
+ *             perm[seg_start[s] .. seg_start[s+1]); the rows with no valid
+ *             slot follow, up to seg_start[max_loras + 1] == n.
+ * Rows with slot >= max_loras set LORA_DEV_ERR_SLOT.
+ */
+int lora_route(int32_t *perm, int32_t *seg_start, const int32_t *seq_slot, int n,
+               int max_loras, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_shrink -- [punica] add_shrink: for every slice j and routed row i
+ *   h[j, i, q] += scale_s * sum_k x[i, k] * A_j,s[q, k],   q < R
+ * ("y[i] += (x @ lora_a_stacked[i]) * scale" with A in the [R, k_in] pool
+ * layout, so the product is x A^T).  h [S, n, R] float32 (in/out): the
+ * [sharded] layers zero it and pass scale 1.0 (scale_table NULL).  Rows with
+ * no slot and slices whose a_table entry is 0 are left untouched.
+ */
+int lora_shrink(float *h, const void *x, int n, int k_in, const int32_t *seq_slot,
+                const uint64_t *a_table, const float *scale_table, int S, int R, int max_loras,
+                void *workspace, size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_expand -- [punica] add_expand: for every slice j and routed row i
+ *   v = scale_s * sum_q h[j, i, q] * B_j,s[c, q]
+ *   out[i, off_j + c] = RN_bf16(out + v)   (add_inputs != 0)
+ *                     = RN_bf16(v)         (add_inputs == 0)
+ * out [n, ld_out] bf16 (in/out).  scale_table NULL means scale 1 (the
+ * [punica] expand carries no scale; pass the table to fold it here as
+ * [metrale] does).  Rows with no slot and slices whose b_table entry is 0
+ * are left untouched bit for bit.  Accumulation is fp32; one rounding to bf16.
+ */
+int lora_expand(void *out, int64_t ld_out, const float *h, const int32_t *seq_slot,
+                const uint64_t *b_table, const float *scale_table, const int32_t *widths, int S,
+                int R, int n, int max_loras, int offset_start, int add_inputs, void *workspace,
+                size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_delta_fused -- the routed delta in one pass ([punica] add_lora_linear,
+ * [metrale] apply_lora_bgmv): for every routed row i (s = seq_slot[i]) and
+ * slice j whose A and B table entries are both nonzero,
+ *   out[i, off_j : off_j + w_j] = RN_bf16(out + scale_s * (x[i] A_j,s^T) B_j,s^T)
+ * (RN_bf16(scale_s * ...) when add_inputs == 0).  Both contractions run at
+ * the padded rank R; the rank-R intermediate stays in fp32 on chip and
+ * never goes to global memory.  x [n, k_in] bf16, out [n, ld_out] bf16.
+ */
+int lora_delta_fused(void *out, int64_t ld_out, const void *x, int n, int k_in,
+                     const int32_t *seq_slot, const uint64_t *a_table, const uint64_t *b_table,
+                     const float *scale_table, const int32_t *widths, int S, int R,
+                     int max_loras, int offset_start, int add_inputs, void *workspace,
+                     size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_moe_fc1_delta -- [flashinfer] bgmv_moe_gemm1_lora_delta.  For every
+ * routed pair (token t, slot j): e = topk_ids[t, j], l = lora_ids[t];
+ *   regular (shared_a == 0): w_ptr_a / w_ptr_b are [2, E] int64 tables of
+ *     bank base addresses [A_gate, A_up] / [B_gate, B_up];
+ *     out[t, j, 0:I]  = RN_bf16(scale * B_gate[l,e] (A_gate[l,e] x[t]))
+ *     out[t, j, I:2I] = RN_bf16(scale * B_up[l,e]   (A_up[l,e]   x[t]))
+ *   shared  (shared_a != 0): [E] tables, one shared A and a fused
+ *     B [2I, rank] (gate rows 0:I, up rows I:2I);
+ *     out[t, j, :] = RN_bf16(scale * B_fused[l,e] (A_shared[l,e] x[t]))
+ * Adapter l of a bank starts l * stride elements after the bank base; A[l,e]
+ * is [rank, H] row-major, B[l,e] is [I, rank] (or [2I, rank]) row-major.
+ * out [T, top_k, 2I] bf16 is fully written: pairs with l < 0 are zeros (the
+ * page skips them), pairs with l >= num_loras or e outside [0, E) are zeros
+ * and set LORA_DEV_ERR_LORA / LORA_DEV_ERR_EXPERT.  The delta stays per
+ * (token, slot): no routing weights, no sum over experts.
+ * Requires H, I, rank multiples of 8, rank <= 128, E * num_loras <= 3071 and
+ * a workspace of lora_moe_workspace_size(T, top_k, E, num_loras) bytes.
+ */
+size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras);
+int lora_moe_fc1_delta(void *out, const void *x, const int64_t *w_ptr_a, int64_t stride_a,
+                       const int64_t *w_ptr_b, int64_t stride_b, int shared_a,
+                       const int32_t *topk_ids, const int32_t *lora_ids, int T, int top_k, int E,
+                       int H, int I, int rank, int num_loras, float scale, void *workspace,
+                       size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_get_error -- copy the device error word to *host_out after all work
+ * queued on `stream` so far has finished (this call synchronizes `stream`),
+ * then clear it on the device when `clear` is nonzero.
+ */
+int lora_get_error(uint32_t *err_word, uint32_t *host_out, int clear, lora_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_DELTA_H */

@@ -1,1 +1,251 @@
-"""GB300-native routed multi-tenant LoRA delta (placeholder during bring-up)."""
+"""GB300-native (sm_103a) routed multi-tenant LoRA delta.
+
+Thin Python binding over the C ABI in ``include/lora_delta.h``: every function
+here only marshals torch tensors into pointers and sizes, passes torch's
+current CUDA stream, and turns a nonzero status into an exception.  All of the
+arithmetic runs in the library's CUDA kernels; if the library is missing the
+calls raise (there is no CPU or PyTorch fallback).
+
+Pages the calls follow: "vllm/lora/punica_wrapper/punica_base.py" (add_shrink,
+add_expand, add_lora_linear, prefill_metadata), "Module lora_delta" (LoraPair,
+LoraRoute, apply_lora_bgmv, the scale rule) and
+"flashinfer.fused_moe.bgmv_moe_gemm1_lora_delta".
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import LibraryMissing, lib, status_string
+
+__all__ = [
+    "LoraError", "LibraryMissing", "LoraPool", "lora_scale", "lora_pool_pack",
+    "lora_workspace_size", "lora_route", "lora_shrink", "lora_expand", "lora_delta_fused",
+    "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_get_error", "new_error_word",
+]
+
+
+class LoraError(RuntimeError):
+    def __init__(self, what: str, code: int):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def _check(what: str, code: int):
+    if code != 0:
+        raise LoraError(what, code)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def new_error_word(device=None) -> torch.Tensor:
+    """A zeroed device error word (int32 view of the C uint32)."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def _widths_arg(widths):
+    arr = (ctypes.c_int32 * len(widths))(*[int(w) for w in widths])
+    return arr
+
+
+# ---------------------------------------------------------------- scalars --
+
+def lora_scale(alpha: float, r: int, use_rslora: bool = False) -> float:
+    return float(lib().lora_scale(float(alpha), int(r), int(bool(use_rslora))))
+
+
+def lora_workspace_size(n: int, max_loras: int) -> int:
+    return int(lib().lora_workspace_size(int(n), int(max_loras)))
+
+
+def lora_moe_workspace_size(T: int, top_k: int, E: int, num_loras: int) -> int:
+    return int(lib().lora_moe_workspace_size(int(T), int(top_k), int(E), int(num_loras)))
+
+
+def _workspace(nbytes: int, workspace, device):
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    if nbytes == 0:
+        return None, 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws, nbytes
+
+
+# -------------------------------------------------------------------- pack --
+
+def lora_pool_pack(a_slot: torch.Tensor, b_slot: torch.Tensor, a_r: torch.Tensor,
+                   b_r: torch.Tensor, stream=None):
+    """Pack PEFT ``a_r`` [r, k_in] / ``b_r`` [w, r] into padded ``a_slot`` [R, k_in] /
+    ``b_slot`` [w, R] (all bf16 device tensors)."""
+    for t, nm in ((a_slot, "a_slot"), (b_slot, "b_slot"), (a_r, "a_r"), (b_r, "b_r")):
+        _dev(t, nm, torch.bfloat16)
+    R, k_in = a_slot.shape
+    r = a_r.shape[0]
+    w = b_slot.shape[0]
+    if a_r.shape[1] != k_in or b_r.shape != (w, r) or b_slot.shape[1] != R:
+        raise ValueError("lora_pool_pack: inconsistent shapes")
+    _check("lora_pool_pack", lib().lora_pool_pack(_ptr(a_slot), _ptr(b_slot), _ptr(a_r),
+                                                  _ptr(b_r), r, R, k_in, w, _stream(stream)))
+
+
+class LoraPool:
+    """Device adapter pool of one projection plus its routing tables.
+
+    Per slice j: ``A[j]`` [max_loras, R, k_in] and ``B[j]`` [max_loras, w_j, R] bf16,
+    zeroed at creation ("Module lora_delta": the pool is zeroed before packing);
+    ``a_table`` / ``b_table`` [S * max_loras] int64 device addresses (0 = slot does
+    not adapt the slice); ``scale_table`` [max_loras] float32.
+    """
+
+    def __init__(self, k_in: int, widths, max_loras: int, R: int, device="cuda"):
+        self.k_in, self.widths, self.max_loras, self.R = int(k_in), tuple(widths), max_loras, R
+        self.device = torch.device(device)
+        S = len(self.widths)
+        self.A = [torch.zeros(max_loras, R, k_in, dtype=torch.bfloat16, device=device)
+                  for _ in range(S)]
+        self.B = [torch.zeros(max_loras, w, R, dtype=torch.bfloat16, device=device)
+                  for w in self.widths]
+        self._a_host = [0] * (S * max_loras)
+        self._b_host = [0] * (S * max_loras)
+        self.scale_table = torch.zeros(max_loras, dtype=torch.float32, device=device)
+        self.a_table = torch.zeros(S * max_loras, dtype=torch.int64, device=device)
+        self.b_table = torch.zeros(S * max_loras, dtype=torch.int64, device=device)
+
+    @property
+    def S(self):
+        return len(self.widths)
+
+    def pack(self, slot: int, a_r_list, b_r_list, alpha: float, rank: int,
+             use_rslora: bool = False, adapted=None):
+        """Pack one slot's PEFT tensors (device bf16: per slice [rank, k_in] / [w_j, rank])."""
+        adapted = [True] * self.S if adapted is None else list(adapted)
+        self.scale_table[slot] = lora_scale(alpha, rank, use_rslora)
+        for j in range(self.S):
+            if adapted[j]:
+                lora_pool_pack(self.A[j][slot], self.B[j][slot], a_r_list[j], b_r_list[j])
+                self._a_host[j * self.max_loras + slot] = self.A[j][slot].data_ptr()
+                self._b_host[j * self.max_loras + slot] = self.B[j][slot].data_ptr()
+            else:
+                self._a_host[j * self.max_loras + slot] = 0
+                self._b_host[j * self.max_loras + slot] = 0
+        self.a_table.copy_(torch.tensor(self._a_host, dtype=torch.int64))
+        self.b_table.copy_(torch.tensor(self._b_host, dtype=torch.int64))
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * 2 for t in self.A + self.B)
+
+
+# ----------------------------------------------------------------- routing --
+
+def lora_route(seq_slot: torch.Tensor, max_loras: int, perm=None, seg_start=None, err=None,
+               stream=None):
+    """Stable clustering of rows by slot: returns (perm [n], seg_start [max_loras+2])."""
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n = seq_slot.numel()
+    dev = seq_slot.device
+    perm = torch.empty(max(n, 1), dtype=torch.int32, device=dev) if perm is None else perm
+    seg_start = (torch.empty(max_loras + 2, dtype=torch.int32, device=dev)
+                 if seg_start is None else seg_start)
+    _check("lora_route", lib().lora_route(_ptr(perm), _ptr(seg_start), _ptr(seq_slot), n,
+                                          int(max_loras), _ptr(err), _stream(stream)))
+    return perm, seg_start
+
+
+# --------------------------------------------------------------- the delta --
+
+def lora_shrink(h, x, seq_slot, pool: LoraPool, scale_table=None, workspace=None, err=None,
+                stream=None):
+    """h[j, i, :] += scale_s * x[i] A_j,s^T (h [S, n, R] float32)."""
+    _dev(h, "h", torch.float32)
+    _dev(x, "x", torch.bfloat16)
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n, k_in = x.shape
+    ws, wsb = _workspace(lora_workspace_size(n, pool.max_loras) if n > 1024 else 0, workspace,
+                         x.device)
+    _check("lora_shrink", lib().lora_shrink(
+        _ptr(h), _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table), _ptr(scale_table),
+        pool.S, pool.R, pool.max_loras, _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_expand(out, h, seq_slot, pool: LoraPool, scale_table=None, offset_start: int = 0,
+                add_inputs: bool = True, workspace=None, err=None, stream=None):
+    """out[i, off_j + c] (+)= scale_s * h[j, i] . B_j,s[c] (out [n, ld_out] bf16)."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(h, "h", torch.float32)
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n, ld_out = out.shape
+    ws, wsb = _workspace(lora_workspace_size(n, pool.max_loras) if n > 1024 else 0, workspace,
+                         out.device)
+    w = _widths_arg(pool.widths)
+    _check("lora_expand", lib().lora_expand(
+        _ptr(out), ld_out, _ptr(h), _ptr(seq_slot), _ptr(pool.b_table), _ptr(scale_table), w,
+        pool.S, pool.R, n, pool.max_loras, int(offset_start), int(bool(add_inputs)), _ptr(ws),
+        wsb, _ptr(err), _stream(stream)))
+
+
+def lora_delta_fused(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,
+                     add_inputs: bool = True, scale_table=None, workspace=None, err=None,
+                     stream=None):
+    """out[i, slices] (+)= scale_s * (x[i] A_s^T) B_s^T over the pool's slices, in place."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n, k_in = x.shape
+    if out.shape[0] != n:
+        raise ValueError("out and x must have the same number of rows")
+    st = pool.scale_table if scale_table is None else scale_table
+    ws, wsb = _workspace(lora_workspace_size(n, pool.max_loras) if n > 1024 else 0, workspace,
+                         x.device)
+    w = _widths_arg(pool.widths)
+    _check("lora_delta_fused", lib().lora_delta_fused(
+        _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
+        _ptr(pool.b_table), _ptr(st), w, pool.S, pool.R, pool.max_loras, int(offset_start),
+        int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_moe_fc1_delta(out, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, shared_a: bool,
+                       topk_ids, lora_ids, E: int, I: int, rank: int, num_loras: int,
+                       scale: float, workspace=None, err=None, stream=None):
+    """MoE FC1 delta into ``out`` [T, top_k, 2I] bf16 (fully written)."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(topk_ids, "topk_ids", torch.int32)
+    _dev(lora_ids, "lora_ids", torch.int32)
+    _dev(w_ptr_a, "w_ptr_a", torch.int64)
+    _dev(w_ptr_b, "w_ptr_b", torch.int64)
+    T, H = x.shape
+    top_k = topk_ids.shape[1]
+    ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras), workspace, x.device)
+    _check("lora_moe_fc1_delta", lib().lora_moe_fc1_delta(
+        _ptr(out), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
+        int(bool(shared_a)), _ptr(topk_ids), _ptr(lora_ids), T, top_k, int(E), H, int(I),
+        int(rank), int(num_loras), float(scale), _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_get_error(err: torch.Tensor, clear: bool = True, stream=None) -> int:
+    """Synchronize the stream and return the device error word (clearing it)."""
+    host = ctypes.c_uint32(0)
+    _check("lora_get_error", lib().lora_get_error(_ptr(err), ctypes.byref(host), int(clear),
+                                                  _stream(stream)))
+    return int(host.value)

@@ -1,0 +1,401 @@
+// C ABI of the routed LoRA delta: host-side validation, launch planning and
+// dispatch onto the caller's stream.  Nothing here allocates or synchronizes
+// (lora_get_error excepted); every failure is a status code.
+#include <math.h>
+#include <string.h>
+
+#include "bgmv.cuh"
+#include "common.cuh"
+#include "lora_delta.h"
+#include "route.cuh"
+
+using namespace lora;
+
+namespace {
+
+constexpr int kClusterSize = 8;
+constexpr int kStageBudgetBytes = 96 * 1024;
+constexpr int kAbiVersion = 1;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Dynamic shared memory above 48 KB needs an opt-in per kernel (and device).
+template <class K>
+cudaError_t allow_smem(K kernel, int bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+// Plan of one delta-kernel launch.
+struct Plan {
+  DeltaArgs a;
+  int smem;
+  int n_keys;
+};
+
+int make_slices(const int32_t* widths, int S, int offset_start, Slices& sl, int* rel) {
+  if (!widths || S < 1 || S > kMaxSlices) return S > kMaxSlices ? LORA_ERR_UNSUPPORTED : LORA_ERR_ARG;
+  if (offset_start < 0) return LORA_ERR_ARG;
+  if (offset_start % 8) return LORA_ERR_ALIGN;
+  sl.S = S;
+  int o = 0;
+  for (int j = 0; j < kMaxSlices; ++j) {
+    sl.width[j] = 0;
+    sl.off[j] = 0;
+    rel[j] = 0;
+  }
+  for (int j = 0; j < S; ++j) {
+    if (widths[j] < 0) return LORA_ERR_ARG;
+    if (widths[j] % 8) return LORA_ERR_ALIGN;
+    sl.width[j] = widths[j];
+    sl.off[j] = offset_start + o;
+    rel[j] = o;
+    o += widths[j];
+  }
+  for (int j = S; j < kMaxSlices; ++j) rel[j] = o;
+  sl.n_cols = o;
+  return LORA_OK;
+}
+
+int check_rank(int S, int R) {
+  if (R < 1) return LORA_ERR_ARG;
+  if (R % 8) return LORA_ERR_ALIGN;
+  if (R > kMaxRank || S * R > kMaxSR) return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+// k-range per CTA, stage width and columns per CTA for a cluster of kClusterSize.
+void plan_tiles(DeltaArgs& a, int k_in, int n_cols, int sr_max, int mode) {
+  const int cs = kClusterSize;
+  a.kc = ((k_in + cs - 1) / cs + 7) / 8 * 8;
+  if (a.kc < 8) a.kc = 8;
+  int ks_max = kStageBudgetBytes / (2 * (sr_max + kRowsPerPass));
+  ks_max = ks_max / 8 * 8;
+  if (ks_max < 8) ks_max = 8;
+  a.ks = (mode == kModeExpand) ? 8 : (a.kc < ks_max ? a.kc : ks_max);
+  a.cpc = ((n_cols + cs - 1) / cs + 7) / 8 * 8;
+  if (a.cpc < 8) a.cpc = 8;
+}
+
+template <int RMAX, int MODE, class Tables>
+int launch_delta_r(const DeltaArgs& a, const Tables& tb, int n_keys, int smem,
+                   cudaStream_t stream) {
+  auto kernel = delta_cluster_kernel<RMAX, MODE, Tables>;
+  cudaError_t e = allow_smem(kernel, smem);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_keys * kClusterSize), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterSize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, a, tb);
+  return cuda_status(e);
+}
+
+template <int MODE, class Tables>
+int launch_delta(const DeltaArgs& a, const Tables& tb, int n_keys, int smem, cudaStream_t s) {
+  if (a.R <= 16) return launch_delta_r<16, MODE>(a, tb, n_keys, smem, s);
+  if (a.R <= 32) return launch_delta_r<32, MODE>(a, tb, n_keys, smem, s);
+  if (a.R <= 64) return launch_delta_r<64, MODE>(a, tb, n_keys, smem, s);
+  return launch_delta_r<128, MODE>(a, tb, n_keys, smem, s);
+}
+
+template <class KeyFn>
+int launch_route(const KeyFn& kf, int n, int n_keys, int32_t* perm, int32_t* seg_start,
+                 uint32_t* err, cudaStream_t stream) {
+  const int smem = (int)route_smem_bytes(n_keys);
+  auto kernel = route_kernel<KeyFn>;
+  cudaError_t e = allow_smem(kernel, smem);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  kernel<<<1, kRouteThreads, smem, stream>>>(kf, n, n_keys, perm, seg_start, err);
+  return cuda_status(cudaGetLastError());
+}
+
+// Workspace layout: perm [n] int32 | seg_start [n_keys + 2] int32.
+size_t ws_bytes_for(int n, int n_keys) {
+  return align256((size_t)(n > 0 ? n : 1) * 4) + align256((size_t)(n_keys + 2) * 4);
+}
+
+// Common front half of the linear calls: row clustering (own scan or routing
+// kernel into the workspace).
+int prepare_rows(DeltaArgs& a, const int32_t* seq_slot, int n, int max_loras, void* workspace,
+                 size_t ws_bytes, uint32_t* err, cudaStream_t stream) {
+  a.seq_slot = seq_slot;
+  a.n = n;
+  a.n_keys = max_loras;
+  a.err = err;
+  if (n <= kInlineRowsMax) {
+    a.perm = nullptr;
+    a.seg_start = nullptr;
+    a.row_cap = n;
+    return LORA_OK;
+  }
+  if (!workspace || ws_bytes < ws_bytes_for(n, max_loras)) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
+  int32_t* perm = reinterpret_cast<int32_t*>(workspace);
+  int32_t* seg = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
+                                            align256((size_t)n * 4));
+  const int rc = launch_route(SlotKey{seq_slot, max_loras}, n, max_loras, perm, seg, err, stream);
+  if (rc) return rc;
+  a.perm = perm;
+  a.seg_start = seg;
+  a.row_cap = 0;
+  return LORA_OK;
+}
+
+int check_max_loras(int max_loras) {
+  if (max_loras < 1) return LORA_ERR_ARG;
+  if (max_loras > kMaxKeys) return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ pack --
+__global__ void pool_pack_kernel(__nv_bfloat16* __restrict__ a_slot,
+                                 __nv_bfloat16* __restrict__ b_slot,
+                                 const __nv_bfloat16* __restrict__ a_r,
+                                 const __nv_bfloat16* __restrict__ b_r, int r, int R, int k_in,
+                                 int w) {
+  const int64_t na = (int64_t)R * k_in, nb = (int64_t)w * R;
+  const __nv_bfloat16 zero = __float2bfloat16_rn(0.0f);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < na + nb;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < na) {
+      const int q = (int)(i / k_in);
+      a_slot[i] = (q < r) ? a_r[i] : zero;  // row q < r of a_r sits at the same offset
+    } else {
+      const int64_t t = i - na;
+      const int c = (int)(t / R), q = (int)(t - (int64_t)c * R);
+      b_slot[t] = (q < r) ? b_r[(int64_t)c * r + q] : zero;
+    }
+  }
+}
+
+__global__ void clear_word_kernel(uint32_t* w) { *w = 0u; }
+
+extern "C" {
+
+const char* lora_status_string(int status) {
+  switch (status) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_ARG: return "LORA_ERR_ARG";
+    case LORA_ERR_SHAPE: return "LORA_ERR_SHAPE";
+    case LORA_ERR_ALIGN: return "LORA_ERR_ALIGN";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA";
+    case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE";
+    case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED";
+    default: return "LORA_ERR_UNKNOWN";
+  }
+}
+
+int lora_abi_version(void) { return kAbiVersion; }
+
+float lora_scale(float alpha, int r, int use_rslora) {
+  if (r <= 0) return 0.0f;
+  return use_rslora ? (float)((double)alpha / sqrt((double)r)) : (float)((double)alpha / r);
+}
+
+int lora_pool_pack(void* a_slot, void* b_slot, const void* a_r, const void* b_r, int r, int R,
+                   int k_in, int w, lora_stream_t stream) {
+  if (!a_slot || !b_slot || r < 0 || r > R || k_in < 0 || w < 0) return LORA_ERR_ARG;
+  if (r > 0 && (!a_r || !b_r)) return LORA_ERR_ARG;
+  const int64_t total = (int64_t)R * k_in + (int64_t)w * R;
+  if (total == 0) return LORA_OK;
+  const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  pool_pack_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
+      (__nv_bfloat16*)a_slot, (__nv_bfloat16*)b_slot, (const __nv_bfloat16*)a_r,
+      (const __nv_bfloat16*)b_r, r, R, k_in, w);
+  return cuda_status(cudaGetLastError());
+}
+
+size_t lora_workspace_size(int n, int max_loras) {
+  if (n < 0 || max_loras < 1) return 0;
+  return ws_bytes_for(n, max_loras);
+}
+
+int lora_route(int32_t* perm, int32_t* seg_start, const int32_t* seq_slot, int n, int max_loras,
+               uint32_t* err_word, lora_stream_t stream) {
+  if (n < 0 || !seg_start || (n > 0 && (!perm || !seq_slot))) return LORA_ERR_ARG;
+  int rc = check_max_loras(max_loras);
+  if (rc) return rc;
+  return launch_route(SlotKey{seq_slot, max_loras}, n, max_loras, perm, seg_start, err_word,
+                      (cudaStream_t)stream);
+}
+
+int lora_shrink(float* h, const void* x, int n, int k_in, const int32_t* seq_slot,
+                const uint64_t* a_table, const float* scale_table, int S, int R, int max_loras,
+                void* workspace, size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (n < 0 || k_in < 0) return LORA_ERR_ARG;
+  if (n == 0) return LORA_OK;
+  if (!h || !x || !seq_slot || !a_table) return LORA_ERR_ARG;
+  int rc = check_max_loras(max_loras);
+  if (rc) return rc;
+  if (S < 1 || S > kMaxSlices) return S > kMaxSlices ? LORA_ERR_UNSUPPORTED : LORA_ERR_ARG;
+  if ((rc = check_rank(S, R))) return rc;
+  if (k_in % 8 || !aligned16(x) || !aligned16(h)) return LORA_ERR_ALIGN;
+  if (k_in == 0) return LORA_OK;
+  DeltaArgs a = {};
+  a.x = (const __nv_bfloat16*)x;
+  a.ld_x = k_in;
+  a.k_in = k_in;
+  a.h = h;
+  a.R = R;
+  a.sl.S = S;
+  a.sr_max = S * R;
+  rc = prepare_rows(a, seq_slot, n, max_loras, workspace, ws_bytes, err_word,
+                    (cudaStream_t)stream);
+  if (rc) return rc;
+  plan_tiles(a, k_in, 8, a.sr_max, kModeShrink);
+  const int smem = smem_plan(a.row_cap, a.sr_max, a.ks, kModeShrink).total;
+  LinearTables tb{a_table, nullptr, scale_table, max_loras};
+  return launch_delta<kModeShrink>(a, tb, max_loras, smem, (cudaStream_t)stream);
+}
+
+int lora_expand(void* out, int64_t ld_out, const float* h, const int32_t* seq_slot,
+                const uint64_t* b_table, const float* scale_table, const int32_t* widths, int S,
+                int R, int n, int max_loras, int offset_start, int add_inputs, void* workspace,
+                size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (n < 0) return LORA_ERR_ARG;
+  if (n == 0) return LORA_OK;
+  if (!out || !h || !seq_slot || !b_table) return LORA_ERR_ARG;
+  int rc = check_max_loras(max_loras);
+  if (rc) return rc;
+  DeltaArgs a = {};
+  if ((rc = make_slices(widths, S, offset_start, a.sl, a.rel))) return rc;
+  if ((rc = check_rank(S, R))) return rc;
+  if (ld_out < (int64_t)offset_start + a.sl.n_cols) return LORA_ERR_SHAPE;
+  if (ld_out % 8 || !aligned16(out) || !aligned16(h)) return LORA_ERR_ALIGN;
+  if (a.sl.n_cols == 0) return LORA_OK;
+  a.out = (__nv_bfloat16*)out;
+  a.ld_out = ld_out;
+  a.h = (float*)h;
+  a.R = R;
+  a.add_inputs = add_inputs ? 1 : 0;
+  a.sr_max = S * R;
+  rc = prepare_rows(a, seq_slot, n, max_loras, workspace, ws_bytes, err_word,
+                    (cudaStream_t)stream);
+  if (rc) return rc;
+  plan_tiles(a, 8, a.sl.n_cols, a.sr_max, kModeExpand);
+  const int smem = smem_plan(a.row_cap, a.sr_max, a.ks, kModeExpand).total;
+  LinearTables tb{nullptr, b_table, scale_table, max_loras};
+  return launch_delta<kModeExpand>(a, tb, max_loras, smem, (cudaStream_t)stream);
+}
+
+int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
+                     const int32_t* seq_slot, const uint64_t* a_table, const uint64_t* b_table,
+                     const float* scale_table, const int32_t* widths, int S, int R,
+                     int max_loras, int offset_start, int add_inputs, void* workspace,
+                     size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (n < 0 || k_in < 0) return LORA_ERR_ARG;
+  if (n == 0) return LORA_OK;
+  if (!out || !x || !seq_slot || !a_table || !b_table) return LORA_ERR_ARG;
+  int rc = check_max_loras(max_loras);
+  if (rc) return rc;
+  DeltaArgs a = {};
+  if ((rc = make_slices(widths, S, offset_start, a.sl, a.rel))) return rc;
+  if ((rc = check_rank(S, R))) return rc;
+  if (ld_out < (int64_t)offset_start + a.sl.n_cols) return LORA_ERR_SHAPE;
+  if (k_in % 8 || ld_out % 8 || !aligned16(out) || !aligned16(x)) return LORA_ERR_ALIGN;
+  if (a.sl.n_cols == 0) return LORA_OK;
+  a.out = (__nv_bfloat16*)out;
+  a.ld_out = ld_out;
+  a.x = (const __nv_bfloat16*)x;
+  a.ld_x = k_in;
+  a.k_in = k_in;
+  a.R = R;
+  a.add_inputs = add_inputs ? 1 : 0;
+  a.sr_max = S * R;
+  rc = prepare_rows(a, seq_slot, n, max_loras, workspace, ws_bytes, err_word,
+                    (cudaStream_t)stream);
+  if (rc) return rc;
+  plan_tiles(a, k_in, a.sl.n_cols, a.sr_max, kModeFused);
+  const int smem = smem_plan(a.row_cap, a.sr_max, a.ks, kModeFused).total;
+  LinearTables tb{a_table, b_table, scale_table, max_loras};
+  return launch_delta<kModeFused>(a, tb, max_loras, smem, (cudaStream_t)stream);
+}
+
+size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras) {
+  if (T < 0 || top_k < 0 || E < 1 || num_loras < 1) return 0;
+  return ws_bytes_for(T * top_k, E * num_loras);
+}
+
+int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t stride_a,
+                       const int64_t* w_ptr_b, int64_t stride_b, int shared_a,
+                       const int32_t* topk_ids, const int32_t* lora_ids, int T, int top_k, int E,
+                       int H, int I, int rank, int num_loras, float scale, void* workspace,
+                       size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (T < 0 || top_k < 0 || E < 1 || H < 0 || I < 0 || num_loras < 1 || stride_a < 0 ||
+      stride_b < 0)
+    return LORA_ERR_ARG;
+  const int64_t n64 = (int64_t)T * top_k;
+  if (n64 == 0 || I == 0) return LORA_OK;
+  if (n64 > (1 << 30)) return LORA_ERR_UNSUPPORTED;
+  if (!out || !x || !w_ptr_a || !w_ptr_b || !topk_ids || !lora_ids) return LORA_ERR_ARG;
+  if ((int64_t)E * num_loras > kMaxKeys) return LORA_ERR_UNSUPPORTED;
+  const int n_slices = shared_a ? 1 : 2;
+  int rc = check_rank(n_slices, rank);
+  if (rc) return rc;
+  if (H % 8 || I % 8 || stride_a % 8 || stride_b % 8 || !aligned16(out) || !aligned16(x))
+    return LORA_ERR_ALIGN;
+  const int n = (int)n64, n_keys = E * num_loras;
+  if (!workspace || ws_bytes < ws_bytes_for(n, n_keys)) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* perm = reinterpret_cast<int32_t*>(workspace);
+  int32_t* seg =
+      reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) + align256((size_t)n * 4));
+  rc = launch_route(MoeKey{topk_ids, lora_ids, top_k, E, num_loras}, n, n_keys, perm, seg,
+                    err_word, s);
+  if (rc) return rc;
+
+  DeltaArgs a = {};
+  int32_t widths[2] = {shared_a ? 2 * I : I, I};
+  if ((rc = make_slices(widths, n_slices, 0, a.sl, a.rel))) return rc;
+  a.out = (__nv_bfloat16*)out;
+  a.ld_out = 2 * (int64_t)I;
+  a.x = (const __nv_bfloat16*)x;
+  a.ld_x = H;
+  a.k_in = H;
+  a.R = rank;
+  a.add_inputs = 0;
+  a.sr_max = n_slices * rank;
+  a.n = n;
+  a.n_keys = n_keys;
+  a.perm = perm;
+  a.seg_start = seg;
+  a.row_cap = 0;
+  a.err = err_word;
+  plan_tiles(a, H, a.sl.n_cols, a.sr_max, kModeFused);
+  const int smem = smem_plan(0, a.sr_max, a.ks, kModeFused).total;
+  MoeTables tb{w_ptr_a, w_ptr_b, stride_a, stride_b, E, top_k, n_slices, scale};
+  rc = launch_delta<kModeFused>(a, tb, n_keys, smem, s);
+  if (rc) return rc;
+  // the pairs with no adapter (the no-key bucket) are written as zeros
+  zero_rows_kernel<<<1024, 256, 0, s>>>(a.out, a.ld_out, 2 * I, perm, seg, n_keys);
+  return cuda_status(cudaGetLastError());
+}
+
+int lora_get_error(uint32_t* err_word, uint32_t* host_out, int clear, lora_stream_t stream) {
+  if (!err_word || !host_out) return LORA_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(host_out, err_word, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) {
+    clear_word_kernel<<<1, 1, 0, s>>>(err_word);
+    e = cudaGetLastError();
+  }
+  return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,310 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle on the same
+seeded inputs (marked gpu).
+
+Bar: bf16 outputs within max|err| <= 1e-2 + 1e-2*|ref|; rows that get no delta,
+routing (perm / segment starts) and packing bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from lora_delta_gb300 import inputs
+from tests.gpu_util import assert_close, oracle_delta
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ld():
+    import __graft_entry__
+    __graft_entry__.build()
+    import lora_delta_gb300
+    assert torch.cuda.is_available()
+    return lora_delta_gb300
+
+
+@pytest.fixture(scope="module")
+def di(ld):
+    from lora_delta_gb300 import device_inputs
+    return device_inputs
+
+
+def run_fused(ld, di, case, R=None, add_inputs=True, scale_table=None):
+    d = di.linear_to_device(case, R=R)
+    out = d.out0.clone()
+    err = ld.new_error_word()
+    ld.lora_delta_fused(out, d.x, d.seq_slot, d.pool, offset_start=case.offset_start,
+                        add_inputs=add_inputs, scale_table=scale_table, err=err)
+    e = ld.lora_get_error(err)
+    return di.bits(out), e, d
+
+
+def check_linear(oracle, case, got, err, rows=None, R=None, add_inputs=True):
+    ref, ref_err = oracle_delta(oracle, case, rows=rows, R=R, add_inputs=add_inputs)
+    sub = got if rows is None else got[np.asarray(rows)]
+    out0 = case.out0 if rows is None else case.out0[np.asarray(rows)]
+    seq = case.seq_slot if rows is None else case.seq_slot[np.asarray(rows)]
+    assert_close(sub, ref, case.name)
+    none = (seq < 0) | (seq >= case.max_loras)
+    assert np.array_equal(sub[none], out0[none]), "rows without a delta must be untouched"
+    assert err == ref_err
+
+
+# ------------------------------------------------------------------ pack --
+
+def test_pool_pack_bit_exact(ld, di, oracle):
+    rng = np.random.default_rng(0)
+    for r, R, k_in, w in [(5, 16, 40, 24), (16, 16, 256, 64), (1, 64, 8, 8), (0, 8, 16, 16)]:
+        a_r = inputs.to_bf16_bits(rng.standard_normal((r, k_in), dtype=np.float32))
+        b_r = inputs.to_bf16_bits(rng.standard_normal((w, r), dtype=np.float32))
+        a_slot = torch.full((R, k_in), 7.0, dtype=torch.bfloat16, device="cuda")
+        b_slot = torch.full((w, R), 7.0, dtype=torch.bfloat16, device="cuda")
+        ld.lora_pool_pack(a_slot, b_slot, di.bf16(a_r.reshape(r, k_in)),
+                          di.bf16(b_r.reshape(w, r)))
+        a_ref, b_ref = oracle.pool_pack(a_r.reshape(r, k_in), b_r.reshape(w, r), R)
+        assert np.array_equal(di.bits(a_slot), a_ref)
+        assert np.array_equal(di.bits(b_slot), b_ref)
+
+
+# --------------------------------------------------------------- routing --
+
+@pytest.mark.parametrize("n,L", [(0, 3), (1, 1), (37, 4), (1000, 16), (8192, 8), (20000, 128),
+                                 (5000, 3071)])
+def test_route_bit_exact(ld, oracle, n, L):
+    rng = np.random.default_rng(n + L)
+    seq = rng.integers(-2, L + 2, size=n).astype(np.int32)
+    err = ld.new_error_word()
+    perm, seg = ld.lora_route(torch.from_numpy(seq).cuda(), L, err=err)
+    e = ld.lora_get_error(err)
+    ref_perm, ref_seg, ref_err = oracle.segments(seq, L)
+    seg = seg.cpu().numpy()
+    assert np.array_equal(seg[: L + 1], ref_seg)
+    assert seg[L + 1] == n
+    assert np.array_equal(perm.cpu().numpy()[: ref_seg[-1]], ref_perm)
+    rest = np.sort(perm.cpu().numpy()[ref_seg[-1]:n])
+    assert np.array_equal(rest, np.flatnonzero((seq < 0) | (seq >= L)))
+    assert e == ref_err
+
+
+# ------------------------------------------------------- the fused delta --
+
+def test_tiny_workload(ld, di, oracle):
+    case = inputs.tiny_case()
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+def test_decode_qkv_workload(ld, di, oracle):
+    case = inputs.decode_qkv_case()
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+@pytest.mark.parametrize("proj", [0, 1])
+def test_skewed_workload(ld, di, oracle, proj):
+    case = inputs.skewed_case(proj)
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+def test_prefill_workload_sampled_rows(ld, di, oracle):
+    """Full prefill gate_up size (8192 rows, 28672 columns), the launch the
+    benchmark times; the oracle recomputes 192 sampled rows on their own."""
+    case = inputs.prefill_gate_up_case()
+    got, err, _ = run_fused(ld, di, case)
+    rows = np.sort(np.random.default_rng(1).choice(case.n, 192, replace=False))
+    check_linear(oracle, case, got, err, rows=rows)
+
+
+def test_prefill_shaped_small(ld, di, oracle):
+    """Routed path (n > 1024) at a size the oracle finishes whole: ragged
+    segments, several row passes per slot, unsorted rows."""
+    case = inputs.prefill_gate_up_case(seed=77, n_tokens=3000, n_segments=12, seg_lo=16,
+                                       seg_hi=700, k_in=512, widths=(1024, 776))
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+def test_x_scaled_reading(ld, di, oracle):
+    case = inputs.decode_qkv_case(x_scaled=True)
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+def test_out_zero_start(ld, di, oracle):
+    case = inputs.decode_qkv_case(out0="zero")
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+# ------------------------------------------------------------ edge cases --
+
+def test_all_rows_unrouted_is_a_bitwise_no_op(ld, di, oracle):
+    case = inputs.linear_case(5, n=50, k_in=64, widths=(32,), max_loras=3, max_rank=16,
+                              ranks=[16, 8, 4], alpha=16.0,
+                              seq_slot=np.full(50, -1, np.int32))
+    got, err, _ = run_fused(ld, di, case)
+    assert np.array_equal(got, case.out0) and err == 0
+
+
+def test_single_slot_many_rows_and_rank8(ld, di, oracle):
+    seq = np.zeros(900, dtype=np.int32)
+    case = inputs.linear_case(6, n=900, k_in=256, widths=(128, 64), max_loras=1, max_rank=8,
+                              ranks=[8], alpha=8.0, seq_slot=seq)
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+def test_table_zero_scale_zero_and_offsets(ld, di, oracle):
+    adapted = [[True, False, True], [False, False, False], [True, True, True],
+               [False, True, False]]
+    case = inputs.linear_case(7, n=77, k_in=320, widths=(64, 40, 24), max_loras=4,
+                              max_rank=16, ranks=[16, 8, 4, 12], alpha=16.0, p_none=0.2,
+                              adapted=adapted, offset_start=16, ld_out=160)
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+    zero = torch.zeros(4, dtype=torch.float32, device="cuda")
+    got0, _, _ = run_fused(ld, di, case, scale_table=zero)
+    assert np.array_equal(got0, case.out0)
+
+
+def test_add_inputs_false(ld, di, oracle):
+    case = inputs.linear_case(8, n=40, k_in=128, widths=(48, 16), max_loras=3, max_rank=16,
+                              ranks=[16, 16, 8], alpha=16.0, p_none=0.3)
+    got, err, _ = run_fused(ld, di, case, add_inputs=False)
+    check_linear(oracle, case, got, err, add_inputs=False)
+
+
+def test_bad_slot_sets_error_and_skips(ld, di, oracle):
+    seq = np.array([0, 9, -1, 1, 2, 7, 0, 1], dtype=np.int32)
+    case = inputs.linear_case(9, n=8, k_in=64, widths=(32,), max_loras=3, max_rank=8,
+                              ranks=[8, 8, 8], alpha=8.0, seq_slot=seq)
+    got, err, _ = run_fused(ld, di, case)
+    assert err & 1
+    check_linear(oracle, case, got, err)
+
+
+def test_misaligned_table_entry_is_skipped_and_flagged(ld, di, oracle):
+    case = inputs.linear_case(10, n=16, k_in=64, widths=(32,), max_loras=2, max_rank=8,
+                              ranks=[8, 8], alpha=8.0, seq_slot=np.array([0, 1] * 8, np.int32))
+    d = di.linear_to_device(case)
+    d.pool.a_table[1] += 2  # slot 1: not 16-byte aligned
+    out = d.out0.clone()
+    err = ld.new_error_word()
+    ld.lora_delta_fused(out, d.x, d.seq_slot, d.pool, err=err)
+    assert ld.lora_get_error(err) & 16
+    got = di.bits(out)
+    assert np.array_equal(got[1::2], case.out0[1::2])
+    ref, _ = oracle_delta(oracle, case)
+    assert_close(got[0::2], ref[0::2], "slot 0 still applies")
+
+
+def test_deterministic(ld, di):
+    case = inputs.skewed_case(0)
+    a, _, _ = run_fused(ld, di, case)
+    b, _, _ = run_fused(ld, di, case)
+    assert np.array_equal(a, b)
+
+
+def test_empty_batch_is_a_no_op(ld, di):
+    case = inputs.tiny_case()
+    d = di.linear_to_device(case)
+    out = d.out0[:0]
+    ld.lora_delta_fused(out, d.x[:0], d.seq_slot[:0], d.pool)
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------- shrink / expand alone --
+
+def test_shrink_matches_oracle(ld, di, oracle):
+    case = inputs.linear_case(11, n=1500, k_in=1024, widths=(64, 32), max_loras=5,
+                              max_rank=16, ranks=[16, 8, 0, 16, 4], alpha=16.0, p_none=0.1)
+    d = di.linear_to_device(case)
+    h = torch.full((2, case.n, 16), 0.5, dtype=torch.float32, device="cuda")
+    err = ld.new_error_word()
+    ld.lora_shrink(h, d.x, d.seq_slot, d.pool, scale_table=d.pool.scale_table, err=err)
+    assert ld.lora_get_error(err) == 0
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, 5, 16)
+    href, _ = oracle.shrink(case.x, case.seq_slot, pool, pool.scale_table,
+                            h=np.full((2, case.n, 16), 0.5, np.float32), acc64=True)
+    got = h.cpu().numpy()
+    xf = (case.x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # rigorous fp32 summation bound: k_in * 2^-24 * scale * sum |x||A| (+ the add)
+    for j in range(2):
+        Aabs = np.abs((pool.A[j].astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+        for i in range(case.n):
+            s = case.seq_slot[i]
+            if s < 0 or case.adapters[s] is None:
+                assert np.array_equal(got[j, i], np.full(16, 0.5, np.float32))
+                continue
+            sc = float(pool.scale_table[s])
+            bound = 2 * case.k_in * 2.0 ** -24 * sc * (np.abs(xf[i]) @ Aabs[s].T) + 1e-6
+            assert np.all(np.abs(got[j, i] - href[j, i]) <= bound)
+
+
+def test_expand_matches_oracle_and_composes(ld, di, oracle):
+    case = inputs.linear_case(12, n=1300, k_in=256, widths=(96, 32), max_loras=4, max_rank=16,
+                              ranks=[16, 8, 16, 4], alpha=16.0, p_none=0.15, offset_start=8,
+                              ld_out=144)
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, 4, 16)
+    h, _ = oracle.shrink(case.x, case.seq_slot, pool, None)
+    ref = case.out0.copy()
+    oracle.expand(ref, h, case.seq_slot, pool, pool.scale_table, offset_start=8)
+    d = di.linear_to_device(case)
+    out = d.out0.clone()
+    ld.lora_expand(out, torch.from_numpy(h).cuda(), d.seq_slot, d.pool,
+                   scale_table=d.pool.scale_table, offset_start=8)
+    got = di.bits(out)
+    assert_close(got, ref, "expand")
+    # GPU shrink (scale 1) then GPU expand (scale folded) == the fused delta
+    hg = torch.zeros(2, case.n, 16, dtype=torch.float32, device="cuda")
+    ld.lora_shrink(hg, d.x, d.seq_slot, d.pool)
+    two = d.out0.clone()
+    ld.lora_expand(two, hg, d.seq_slot, d.pool, scale_table=d.pool.scale_table, offset_start=8)
+    fused = d.out0.clone()
+    ld.lora_delta_fused(fused, d.x, d.seq_slot, d.pool, offset_start=8)
+    assert_close(di.bits(two), di.bits(fused), "shrink+expand vs fused")
+
+
+# ------------------------------------------------------------------- MoE --
+
+def run_moe(ld, di, mc, topk=None, lora=None):
+    dm = di.moe_to_device(mc)
+    if topk is not None:
+        dm.topk_ids = torch.from_numpy(topk).cuda()
+    if lora is not None:
+        dm.lora_ids = torch.from_numpy(lora).cuda()
+    out = torch.full((mc.T, mc.top_k, 2 * mc.I), 3.0, dtype=torch.bfloat16, device="cuda")
+    err = ld.new_error_word()
+    ld.lora_moe_fc1_delta(out, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b,
+                          mc.shared_a, dm.topk_ids, dm.lora_ids, mc.E, mc.I, mc.rank, mc.L,
+                          mc.scale, err=err)
+    return di.bits(out), ld.lora_get_error(err)
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_moe_fc1_workload(ld, di, oracle, shared):
+    mc = inputs.moe_case(shared_a=shared)
+    got, err = run_moe(ld, di, mc)
+    ref, ref_err = oracle.moe_fc1(mc.x, mc.A_banks, mc.B_banks, mc.topk_ids, mc.lora_ids, mc.I,
+                                  mc.rank, mc.scale, shared, mc.L)
+    assert err == ref_err == 0
+    assert_close(got, ref, mc.name)
+    skipped = mc.lora_ids < 0
+    assert not got[skipped].any()
+
+
+def test_moe_bad_ids(ld, di, oracle):
+    mc = inputs.moe_case(T=40, top_k=3, E=6, H=64, I=24, rank=16, L=3, p_none=0.0)
+    topk = mc.topk_ids.copy()
+    lora = mc.lora_ids.copy()
+    lora[0], lora[1] = -1, 3
+    topk[2, 1], topk[3, 0] = 6, -5
+    got, err = run_moe(ld, di, mc, topk, lora)
+    ref, ref_err = oracle.moe_fc1(mc.x, mc.A_banks, mc.B_banks, topk, lora, mc.I, mc.rank,
+                                  mc.scale, False, mc.L)
+    assert err == ref_err == (2 | 4)
+    assert_close(got, ref, "moe bad ids")
+    assert not got[0].any() and not got[1].any() and not got[2, 1].any()
