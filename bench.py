@@ -222,19 +222,22 @@ def run_ours(args, rank, world):
     sampler = ClockSampler(local)
     sampler.start()
     # untimed pre-roll so that clocks settle and the sampler sees the load
+    # (CUDAGraph.replay launches on the current stream: make it `stream`)
     t_pre = time.time()
     n_pre = 0
-    while time.time() - t_pre < 0.4 or n_pre < 1:
-        g.replay()
-        torch.cuda.synchronize(device)
-        n_pre += 1
+    with torch.cuda.stream(stream):
+        while time.time() - t_pre < 0.4 or n_pre < 1:
+            g.replay()
+            torch.cuda.synchronize(device)
+            n_pre += 1
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ldist.barrier()
     torch.cuda.synchronize(device)
     t_wall0 = time.time()
-    ev0.record(stream)
-    g.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        g.replay()
+        ev1.record(stream)
     torch.cuda.synchronize(device)
     t_wall1 = time.time()
     ldist.barrier()
