@@ -52,6 +52,8 @@ typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
 #define LORA_ERR_CUDA 4        /* a CUDA launch or copy failed                 */
 #define LORA_ERR_WORKSPACE 5   /* workspace missing or smaller than required   */
 #define LORA_ERR_UNSUPPORTED 6 /* outside the limits stated above              */
+#define LORA_ERR_TOO_LARGE 7   /* needs more scratch than the library's fixed
+                                  no-allocation buffer holds                   */
 
 /* device-detected bits, OR-ed into *err_word */
 #define LORA_DEV_ERR_SLOT 1u    /* seq_slot >= max_loras: the row gets no delta        */
@@ -188,6 +190,34 @@ int lora_moe_fc1_delta(void *out, const void *x, const int64_t *w_ptr_a, int64_t
                        const int32_t *topk_ids, const int32_t *lora_ids, int T, int top_k, int E,
                        int H, int I, int rank, int num_loras, float scale, void *workspace,
                        size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_delta_fused_noalloc -- lora_delta_fused for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this call: it
+ * exists for callers whose memory is fixed up front (a budget set at start
+ * up, an allocator that refuses allocations after warm-up, a runtime that
+ * only lends this library the tensors it already owns) and who therefore
+ * cannot provide lora_delta_fused's scratch workspace.
+ * Same arguments and results as lora_delta_fused minus the workspace: the
+ * scratch comes from a fixed buffer inside the library of
+ * lora_noalloc_scratch_bytes() bytes (4 MiB), held on every GPU that loads
+ * the library until the process exits.  A call whose workspace need
+ * (lora_workspace_size(n, max_loras)) exceeds it returns LORA_ERR_TOO_LARGE
+ * and enqueues nothing.  The call never allocates (no cudaMalloc, no
+ * allocating library routine).  The first call on a device looks the buffer
+ * up on that device (it must be the current device), so make that first
+ * call before any stream capture.  All calls share the one buffer: calls that
+ * may overlap on the GPU (different streams) race and must be serialized by
+ * the caller.  The buffer keeps the last call's contents; nothing in it needs
+ * to start at zero.
+ */
+size_t lora_noalloc_scratch_bytes(void);
+int lora_delta_fused_noalloc(void *out, int64_t ld_out, const void *x, int n, int k_in,
+                             const int32_t *seq_slot, const uint64_t *a_table,
+                             const uint64_t *b_table, const float *scale_table,
+                             const int32_t *widths, int S, int R, int max_loras,
+                             int offset_start, int add_inputs, uint32_t *err_word,
+                             lora_stream_t stream);
 
 /*
  * lora_get_error -- copy the device error word to *host_out after all work

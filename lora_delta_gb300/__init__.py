@@ -24,6 +24,7 @@ __all__ = [
     "LoraError", "LibraryMissing", "LoraPool", "lora_scale", "lora_pool_pack",
     "lora_workspace_size", "lora_route", "lora_shrink", "lora_expand", "lora_delta_fused",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_get_error", "new_error_word",
+    "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes",
 ]
 
 
@@ -222,6 +223,30 @@ def lora_delta_fused(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,
         _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
         _ptr(pool.b_table), _ptr(st), w, pool.S, pool.R, pool.max_loras, int(offset_start),
         int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_delta_fused_noalloc(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,
+                             add_inputs: bool = True, scale_table=None, err=None, stream=None):
+    """``lora_delta_fused`` for callers that cannot allocate: the scratch is the
+    library's own fixed buffer (``lora_noalloc_scratch_bytes()``), shared by all
+    calls; calls that overlap on the GPU race, and a batch that needs more scratch
+    raises LoraError(LORA_ERR_TOO_LARGE)."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n, k_in = x.shape
+    if out.shape[0] != n:
+        raise ValueError("out and x must have the same number of rows")
+    st = pool.scale_table if scale_table is None else scale_table
+    w = _widths_arg(pool.widths)
+    _check("lora_delta_fused_noalloc", lib().lora_delta_fused_noalloc(
+        _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
+        _ptr(pool.b_table), _ptr(st), w, pool.S, pool.R, pool.max_loras, int(offset_start),
+        int(bool(add_inputs)), _ptr(err), _stream(stream)))
+
+
+def lora_noalloc_scratch_bytes() -> int:
+    return int(lib().lora_noalloc_scratch_bytes())
 
 
 def lora_moe_fc1_delta(out, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, shared_a: bool,

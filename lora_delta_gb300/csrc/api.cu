@@ -195,6 +195,7 @@ const char* lora_status_string(int status) {
     case LORA_ERR_CUDA: return "LORA_ERR_CUDA";
     case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE";
     case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED";
+    case LORA_ERR_TOO_LARGE: return "LORA_ERR_TOO_LARGE";
     default: return "LORA_ERR_UNKNOWN";
   }
 }

@@ -1,0 +1,75 @@
+// lora_delta_fused_noalloc: the routed delta for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocating routine) on the path
+// that applies the delta: code that runs inside a memory budget fixed at start
+// up, custom allocators that forbid allocations after warm-up, or runtimes that
+// hand this library only the tensors they already own.  lora_delta_fused needs
+// a scratch workspace for large batches (the row clustering by slot), which
+// such a caller cannot provide.  This entry point takes that scratch from a
+// fixed array that lives in the library itself.
+//
+// The array is a file-scope __device__ variable of kNoAllocScratchBytes bytes:
+// every GPU on which the library is loaded holds it until the process exits.
+// Its address is looked up once per device with cudaGetSymbolAddress, by the
+// first call on that device, with that device current; that first call should
+// therefore come before any stream capture.  Every call shares the one array,
+// so calls that overlap on the GPU (for example on two streams) race on it;
+// serialize them.  The array keeps whatever the last call left in it; the
+// kernels that use it overwrite every entry they read (the clustering writes
+// the whole row permutation and every cluster start), so nothing in it has to
+// start at zero.
+#include <mutex>
+
+#include "lora_delta.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once).
+int scratch_for_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return LORA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return LORA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lora_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+int lora_delta_fused_noalloc(void* out, int64_t ld_out, const void* x, int n, int k_in,
+                             const int32_t* seq_slot, const uint64_t* a_table,
+                             const uint64_t* b_table, const float* scale_table,
+                             const int32_t* widths, int S, int R, int max_loras,
+                             int offset_start, int add_inputs, uint32_t* err_word,
+                             lora_stream_t stream) {
+  if (n < 0 || max_loras < 1) return LORA_ERR_ARG;
+  const size_t need = lora_workspace_size(n, max_loras);
+  if (need > kNoAllocScratchBytes) return LORA_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  const int rc = scratch_for_current_device(&scratch);
+  if (rc != LORA_OK) return rc;
+  return lora_delta_fused(out, ld_out, x, n, k_in, seq_slot, a_table, b_table, scale_table,
+                          widths, S, R, max_loras, offset_start, add_inputs, scratch,
+                          kNoAllocScratchBytes, err_word, stream);
+}
+
+}  // extern "C"
