@@ -2,7 +2,11 @@
 // dispatch onto the caller's stream.  Nothing here allocates or synchronizes
 // (lora_get_error excepted); every failure is a status code.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
+
+#include <mutex>
+#include <unordered_map>
 
 #include "bgmv.cuh"
 #include "common.cuh"
@@ -13,28 +17,77 @@ using namespace lora;
 
 namespace {
 
-constexpr int kClusterSize = 8;
-constexpr int kStageBudgetBytes = 96 * 1024;
 constexpr int kAbiVersion = 1;
+constexpr int kStageBytes = 64 * 1024;  // A rows of one shrink stage (both buffers)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Dynamic shared memory above 48 KB needs an opt-in per kernel (and device).
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  long x = strtol(v, &end, 10);
+  return (end && *end == 0) ? (int)x : dflt;
+}
+
+// Cluster size of the small-segment kernel: 16 CTAs per key when there are few
+// keys (decode: spread each adapter's bytes over many SMs), fewer when there
+// are many keys (MoE); LORA_CLUSTER_SIZE (4, 8 or 16) overrides, read once.
+int cluster_size_for(int n_keys) {
+  static const int forced = [] {
+    const int v = env_int("LORA_CLUSTER_SIZE", 0);
+    return (v == 4 || v == 8 || v == 16) ? v : 0;
+  }();
+  if (forced) return forced;
+  if (n_keys <= 48) return 16;
+  if (n_keys <= 192) return 8;
+  return 4;
+}
+bool use_pdl() {
+  static const bool on = env_int("LORA_PDL", 1) != 0;
+  return on;
+}
+
+// Per-(kernel, device) function attributes, set once: the dynamic shared
+// memory opt-in (to the largest size requested so far) and the non-portable
+// cluster size.
+struct KernelAttrCache {
+  std::mutex mu;
+  std::unordered_map<uint64_t, int> smem;  // (kernel, device) -> bytes granted
+  std::unordered_map<uint64_t, bool> cluster;
+};
+KernelAttrCache& attr_cache() {
+  static KernelAttrCache c;
+  return c;
+}
+
 template <class K>
-cudaError_t allow_smem(K kernel, int bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+cudaError_t prepare_kernel(K kernel, int smem_bytes, bool big_cluster) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t id = (reinterpret_cast<uint64_t>(reinterpret_cast<const void*>(kernel)) << 6) ^
+                      (uint64_t)dev;
+  KernelAttrCache& c = attr_cache();
+  std::lock_guard<std::mutex> lock(c.mu);
+  if (smem_bytes > 48 * 1024) {
+    auto it = c.smem.find(id);
+    if (it == c.smem.end() || it->second < smem_bytes) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+      if (e != cudaSuccess) return e;
+      c.smem[id] = smem_bytes;
+    }
+  }
+  if (big_cluster && !c.cluster[id]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    c.cluster[id] = true;
+  }
+  return cudaSuccess;
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
-
-// Plan of one delta-kernel launch.
-struct Plan {
-  DeltaArgs a;
-  int smem;
-  int n_keys;
-};
 
 int make_slices(const int32_t* widths, int S, int offset_start, Slices& sl, int* rel) {
   if (!widths || S < 1 || S > kMaxSlices) return S > kMaxSlices ? LORA_ERR_UNSUPPORTED : LORA_ERR_ARG;
@@ -45,7 +98,6 @@ int make_slices(const int32_t* widths, int S, int offset_start, Slices& sl, int*
   for (int j = 0; j < kMaxSlices; ++j) {
     sl.width[j] = 0;
     sl.off[j] = 0;
-    rel[j] = 0;
   }
   for (int j = 0; j < S; ++j) {
     if (widths[j] < 0) return LORA_ERR_ARG;
@@ -55,7 +107,7 @@ int make_slices(const int32_t* widths, int S, int offset_start, Slices& sl, int*
     rel[j] = o;
     o += widths[j];
   }
-  for (int j = S; j < kMaxSlices; ++j) rel[j] = o;
+  for (int j = S; j <= kMaxSlices; ++j) rel[j] = o;
   sl.n_cols = o;
   return LORA_OK;
 }
@@ -67,43 +119,65 @@ int check_rank(int S, int R) {
   return LORA_OK;
 }
 
-// k-range per CTA, stage width and columns per CTA for a cluster of kClusterSize.
+// Per-CTA k-range and shrink stage width (multiples of 16: whole MMA k-steps,
+// except at the end of k_in) and columns per CTA (multiple of 8: whole MMA
+// column tiles).
 void plan_tiles(DeltaArgs& a, int k_in, int n_cols, int sr_max, int mode) {
-  const int cs = kClusterSize;
-  a.kc = ((k_in + cs - 1) / cs + 7) / 8 * 8;
-  if (a.kc < 8) a.kc = 8;
-  int ks_max = kStageBudgetBytes / (2 * (sr_max + kRowsPerPass));
-  ks_max = ks_max / 8 * 8;
-  if (ks_max < 8) ks_max = 8;
-  a.ks = (mode == kModeExpand) ? 8 : (a.kc < ks_max ? a.kc : ks_max);
+  const int cs = cluster_size_for(a.n_keys);
+  a.cs = cs;
+  const int sr16 = (sr_max + 15) / 16 * 16;
+  a.kc = ((k_in + cs - 1) / cs + 15) / 16 * 16;
+  if (a.kc < 16) a.kc = 16;
+  if (mode == kModeExpand) {
+    a.kst = 16;
+    a.nbuf = 1;
+  } else if (sr16 * (a.kc + 8) * 2 <= kStageBytes) {
+    a.kst = a.kc;  // one stage: A stays resident across row passes
+    a.nbuf = 1;
+  } else {
+    int ks = kStageBytes / 2 / (sr16 * 2) - 8;
+    ks = ks >= 64 ? ks / 64 * 64 : ks / 16 * 16;
+    a.kst = ks < 16 ? 16 : ks;
+    a.nbuf = 2;
+  }
   a.cpc = ((n_cols + cs - 1) / cs + 7) / 8 * 8;
   if (a.cpc < 8) a.cpc = 8;
+  a.min_rows = 0;
+  a.max_rows = 0x7fffffff;
+  // start the weight copies before the dependency wait when nearly every key
+  // has rows (an empty key's early copies are wasted traffic)
+  a.early = (mode != kModeExpand && a.n >= 2 * a.n_keys) ? 1 : 0;
 }
 
 template <int RMAX, int MODE, class Tables>
 int launch_delta_r(const DeltaArgs& a, const Tables& tb, int n_keys, int smem,
                    cudaStream_t stream) {
   auto kernel = delta_cluster_kernel<RMAX, MODE, Tables>;
-  cudaError_t e = allow_smem(kernel, smem);
+  const int cs = a.cs;
+  cudaError_t e = prepare_kernel(kernel, smem, cs > 8);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n_keys * kClusterSize), 1, 1);
+  cfg.gridDim = dim3((unsigned)(n_keys * cs), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kClusterSize;
+  attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = use_pdl() ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kernel, a, tb);
   return cuda_status(e);
 }
 
 template <int MODE, class Tables>
-int launch_delta(const DeltaArgs& a, const Tables& tb, int n_keys, int smem, cudaStream_t s) {
+int launch_delta(const DeltaArgs& a, const Tables& tb, int n_keys, cudaStream_t s) {
+  const int smem = smem_plan(a, MODE).total;
+  if (smem > 226 * 1024) return LORA_ERR_UNSUPPORTED;  // leaves room for static smem
   if (a.R <= 16) return launch_delta_r<16, MODE>(a, tb, n_keys, smem, s);
   if (a.R <= 32) return launch_delta_r<32, MODE>(a, tb, n_keys, smem, s);
   if (a.R <= 64) return launch_delta_r<64, MODE>(a, tb, n_keys, smem, s);
@@ -115,7 +189,7 @@ int launch_route(const KeyFn& kf, int n, int n_keys, int32_t* perm, int32_t* seg
                  uint32_t* err, cudaStream_t stream) {
   const int smem = (int)route_smem_bytes(n_keys);
   auto kernel = route_kernel<KeyFn>;
-  cudaError_t e = allow_smem(kernel, smem);
+  cudaError_t e = prepare_kernel(kernel, smem, false);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   kernel<<<1, kRouteThreads, smem, stream>>>(kf, n, n_keys, perm, seg_start, err);
   return cuda_status(cudaGetLastError());
@@ -258,9 +332,8 @@ int lora_shrink(float* h, const void* x, int n, int k_in, const int32_t* seq_slo
                     (cudaStream_t)stream);
   if (rc) return rc;
   plan_tiles(a, k_in, 8, a.sr_max, kModeShrink);
-  const int smem = smem_plan(a.row_cap, a.sr_max, a.ks, kModeShrink).total;
   LinearTables tb{a_table, nullptr, scale_table, max_loras};
-  return launch_delta<kModeShrink>(a, tb, max_loras, smem, (cudaStream_t)stream);
+  return launch_delta<kModeShrink>(a, tb, max_loras, (cudaStream_t)stream);
 }
 
 int lora_expand(void* out, int64_t ld_out, const float* h, const int32_t* seq_slot,
@@ -288,9 +361,8 @@ int lora_expand(void* out, int64_t ld_out, const float* h, const int32_t* seq_sl
                     (cudaStream_t)stream);
   if (rc) return rc;
   plan_tiles(a, 8, a.sl.n_cols, a.sr_max, kModeExpand);
-  const int smem = smem_plan(a.row_cap, a.sr_max, a.ks, kModeExpand).total;
   LinearTables tb{nullptr, b_table, scale_table, max_loras};
-  return launch_delta<kModeExpand>(a, tb, max_loras, smem, (cudaStream_t)stream);
+  return launch_delta<kModeExpand>(a, tb, max_loras, (cudaStream_t)stream);
 }
 
 int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
@@ -321,9 +393,8 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
                     (cudaStream_t)stream);
   if (rc) return rc;
   plan_tiles(a, k_in, a.sl.n_cols, a.sr_max, kModeFused);
-  const int smem = smem_plan(a.row_cap, a.sr_max, a.ks, kModeFused).total;
   LinearTables tb{a_table, b_table, scale_table, max_loras};
-  return launch_delta<kModeFused>(a, tb, max_loras, smem, (cudaStream_t)stream);
+  return launch_delta<kModeFused>(a, tb, max_loras, (cudaStream_t)stream);
 }
 
 size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras) {
@@ -378,9 +449,8 @@ int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t
   a.row_cap = 0;
   a.err = err_word;
   plan_tiles(a, H, a.sl.n_cols, a.sr_max, kModeFused);
-  const int smem = smem_plan(0, a.sr_max, a.ks, kModeFused).total;
   MoeTables tb{w_ptr_a, w_ptr_b, stride_a, stride_b, E, top_k, n_slices, scale};
-  rc = launch_delta<kModeFused>(a, tb, n_keys, smem, s);
+  rc = launch_delta<kModeFused>(a, tb, n_keys, s);
   if (rc) return rc;
   // the pairs with no adapter (the no-key bucket) are written as zeros
   zero_rows_kernel<<<1024, 256, 0, s>>>(a.out, a.ld_out, 2 * I, perm, seg, n_keys);

@@ -1,25 +1,34 @@
-// The routed LoRA delta on CUDA cores, one thread-block cluster per adapter
-// key ("Module lora_delta", apply_lora_bgmv; "punica_base.py",
+// The routed LoRA delta for small row groups, one thread-block cluster per
+// adapter key ("Module lora_delta", apply_lora_bgmv; "punica_base.py",
 // add_lora_linear / add_shrink / add_expand; the MoE FC1 variant of
 // "flashinfer.fused_moe.bgmv_moe_gemm1_lora_delta").
 //
-// Work decomposition (one cluster of CS CTAs per key = slot, or (l, e) for MoE):
-//   * the key's rows are found on the device (own scan for small n, else the
-//     routing kernel's stable clusters) and handled in passes of kRowsPerPass;
-//   * shrink: CTA c contracts its 1/CS share of k_in for every row of the pass
-//     and every active (slice, rank) pair.  The A rows and x rows of that
-//     k-range are pulled into shared memory by 1-D TMA bulk copies
-//     (cp.async.bulk) completing on one mbarrier, so every byte a CTA needs is
-//     in flight at once; lanes take 16-byte vectors along k and a warp-shuffle
-//     tree reduces each dot product;
-//   * the CS partial sums meet through distributed shared memory (DSMEM): after
-//     a cluster barrier every CTA sums the CS partials in rank order, so all
-//     CTAs hold the same fp32 h, which never leaves the chip;
-//   * expand + fold: CTA c owns 1/CS of the concatenated output columns; a
-//     thread takes two adjacent columns, keeps their B rows in registers and
-//     updates out in place, RN_bf16(out + scale * (h . B)), one rounding.
-// Each key's A and B are read from HBM once per pass (once in total for the
-// usual decode case of <= kRowsPerPass rows per slot).
+// One cluster of CS CTAs per key (a slot, or an (adapter, expert) pair):
+//   * prologue, before the grid dependency wait of programmatic dependent
+//     launch: the key's table entries are resolved and, when nearly every key
+//     has rows, the CTA's share of the A rows starts streaming into shared
+//     memory and the B rows of its columns into L2 -- adapter weights are
+//     never produced by the preceding kernel, so this overlaps its tail;
+//   * the key's rows are found on the device (own ballot scan for small n,
+//     else the routing kernel's stable clusters) and handled in passes of 16;
+//     keys whose row count falls outside [min_rows, max_rows) are skipped;
+//   * shrink: CTA c contracts its 1/CS share of k_in.  A rows and x rows are
+//     staged in padded (ldmatrix-conflict-free) shared rows by 16-byte
+//     cp.async copies from all threads, and the contraction runs as
+//     mma.sync m16n8k16 tiles (16 (slice, rank) pairs x 8 rows, fp32
+//     accumulate) split over the warps by k-group;
+//   * the CS partial sums meet through distributed shared memory with two
+//     rounds of remote stores and no remote loads: each CTA pushes its
+//     partial of entry e to e's owner, each owner sums its entries over the
+//     cluster in rank order and pushes the sum into every CTA's h, so all
+//     CTAs hold the same fp32 h, which never goes to global memory;
+//   * expand + fold: CTA c owns 1/CS of the concatenated output columns.  h
+//     of the pass is split into a bf16 (hi, lo) pair -- the rank contraction
+//     keeps ~fp32 accuracy -- and multiplied by 8-column tiles of B on the
+//     tensor cores; every tile's B and out loads are issued before its MMAs,
+//     and out is updated in place, RN_bf16(out + scale * d), one rounding.
+// A key's A and B come from HBM once per call for the usual decode case of
+// at most 16 rows per slot.
 #pragma once
 
 #include "common.cuh"
@@ -28,7 +37,7 @@ namespace lora {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerPass = 16;
+constexpr int kMaxRowsPerPass = 16;
 
 enum DeltaMode { kModeFused = 0, kModeShrink = 1, kModeExpand = 2 };
 
@@ -48,13 +57,19 @@ struct LinearTables {
   const float* scale_table;
   int max_loras;
   __device__ void resolve(int key, int S, int mode, SlotView& v, uint32_t& bad) const {
+    uint64_t av[kMaxSlices], bv[kMaxSlices];
+#pragma unroll
+    for (int j = 0; j < kMaxSlices; ++j) {  // independent loads, one round trip
+      av[j] = (j < S && mode != kModeExpand) ? a_table[(size_t)j * max_loras + key] : 16u;
+      bv[j] = (j < S && mode != kModeShrink) ? b_table[(size_t)j * max_loras + key] : 16u;
+    }
     v.scale = scale_table ? scale_table[key] : 1.0f;
     v.nact = 0;
+#pragma unroll
     for (int j = 0; j < kMaxSlices; ++j) {
       v.ja[j] = -1;
       if (j >= S) continue;
-      uint64_t a = (mode != kModeExpand) ? a_table[(size_t)j * max_loras + key] : 16u;
-      uint64_t b = (mode != kModeShrink) ? b_table[(size_t)j * max_loras + key] : 16u;
+      const uint64_t a = av[j], b = bv[j];
       if ((a & 15u) || (b & 15u)) {
         bad |= LORA_DEV_ERR_ALIGN;
         continue;
@@ -114,96 +129,152 @@ struct DeltaArgs {
   int n_keys;
   int R;
   Slices sl;
-  int rel[kMaxSlices];  // slice starts relative to the first slice
+  int rel[kMaxSlices + 1];  // slice starts relative to the first slice; rel[S..] = n_cols
   int add_inputs;
-  int kc;   // k-range per CTA (multiple of 8)
-  int ks;   // k per pipeline stage (multiple of 8)
-  int cpc;  // output columns per CTA (multiple of 8)
+  int kc;     // k-range per CTA (multiple of 16)
+  int kst;    // k per shared-memory stage (multiple of 16)
+  int nbuf;   // stage buffers (1 or 2)
+  int cpc;    // output columns per CTA (multiple of 8)
+  int cs;     // CTAs per cluster
+  int early;  // start the weight copies before the grid dependency wait
   int row_cap;
-  int sr_max;  // S * R: shared-memory sizing
+  int sr_max;              // S * R: shared-memory sizing
+  int min_rows, max_rows;  // keys with a row count outside [min, max) are skipped
   uint32_t* err;
 };
 
+constexpr int kRowsPerPass = 16;  // rows of one pass: two 8-wide MMA column tiles
+
 // Shared-memory plan (bytes), identical on host and device.
 struct SmemPlan {
-  int rows_off, P_off, H_off, A_off, X_off, total;
+  int rows_off, As_off, Xs_off, Pw_off, Rx_off, H_off, total;
+  int as_stride;  // elements per A / x row in shared memory (padded)
+  int sr16;       // S * R rounded up to 16
+  int rx_per;     // (row, pair) entries owned by one CTA of the cluster
 };
-__host__ __device__ inline SmemPlan smem_plan(int row_cap, int sr_max, int ks, int mode) {
+__host__ __device__ inline SmemPlan smem_plan(const DeltaArgs& a, int mode) {
   SmemPlan p;
-  int o = 128;  // mbarrier + the pass's row ids
+  p.sr16 = (a.sr_max + 15) / 16 * 16;
+  p.as_stride = a.kst + 8;
+  p.rx_per = (kRowsPerPass * p.sr16 + a.cs - 1) / a.cs;
+  int o = 128;  // the pass's row ids (16 ints) at offset 64
   p.rows_off = o;
-  o += ((row_cap * 4 + 127) / 128) * 128;
-  p.P_off = o;
-  o += (mode == kModeExpand) ? 0 : kRowsPerPass * sr_max * 4;
+  o += ((a.row_cap * 4 + 127) / 128) * 128;
+  p.As_off = o;
+  if (mode != kModeExpand) o += a.nbuf * p.sr16 * p.as_stride * 2;
+  p.Xs_off = o;
+  if (mode != kModeExpand) o += a.nbuf * kRowsPerPass * p.as_stride * 2;
+  o = (o + 127) / 128 * 128;
+  p.Pw_off = o;
+  if (mode != kModeExpand) o += (p.sr16 > 128 ? p.sr16 : 128) * kRowsPerPass * 4;
+  p.Rx_off = o;  // partials received from the cluster: [cs][rx_per]
+  if (mode != kModeExpand) o += a.cs * p.rx_per * 4;
   p.H_off = o;
-  o += kRowsPerPass * sr_max * 4;
-  p.A_off = o;
-  o += (mode == kModeExpand) ? 0 : sr_max * ks * 2;
-  p.X_off = o;
-  o += (mode == kModeExpand) ? 0 : kRowsPerPass * ks * 2;
+  o += kRowsPerPass * p.sr16 * 4;
   p.total = o;
   return p;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-  return v;
+// 16-byte cp.async copies, issued by every thread of the CTA, of the A rows
+// (columns [k0, k0 + kw) of the key's active (slice, rank) pairs) into As.
+__device__ __forceinline__ void copy_a_rows(const DeltaArgs& a, const SlotView& v, int SRa,
+                                            int k0, int kw, __nv_bfloat16* As, int stride,
+                                            int tid) {
+  const int R = a.R;
+  const int vpr = kw / 8;
+  for (int idx = tid; idx < SRa * vpr; idx += kThreads) {
+    const int t = idx / vpr, c = idx - t * vpr;
+    const int jj = t / R, q = t - jj * R;
+    cp_async16(As + (size_t)t * stride + c * 8,
+               v.A[v.act_slice[jj]] + (size_t)q * a.k_in + k0 + c * 8);
+  }
 }
 
-__device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
-  float s = bf16lo(a.x) * bf16lo(b.x);
-  s = fmaf(bf16hi(a.x), bf16hi(b.x), s);
-  s = fmaf(bf16lo(a.y), bf16lo(b.y), s);
-  s = fmaf(bf16hi(a.y), bf16hi(b.y), s);
-  s = fmaf(bf16lo(a.z), bf16lo(b.z), s);
-  s = fmaf(bf16hi(a.z), bf16hi(b.z), s);
-  s = fmaf(bf16lo(a.w), bf16lo(b.w), s);
-  s = fmaf(bf16hi(a.w), bf16hi(b.w), s);
-  return s;
+// ... and of the pass's x rows into Xs.
+template <class Tables>
+__device__ __forceinline__ void copy_x_rows(const DeltaArgs& a, const Tables& tb, const int* prow,
+                                            int nr, int k0, int kw, __nv_bfloat16* Xs,
+                                            int stride, int tid) {
+  const int vpr = kw / 8;
+  for (int idx = tid; idx < nr * vpr; idx += kThreads) {
+    const int r = idx / vpr, c = idx - r * vpr;
+    cp_async16(Xs + (size_t)r * stride + c * 8, a.x + tb.x_row(prow[r]) * a.ld_x + k0 + c * 8);
+  }
 }
 
-__device__ __forceinline__ float dot8h(const float* h, const uint4& b) {
-  const float4 h0 = *reinterpret_cast<const float4*>(h);
-  const float4 h1 = *reinterpret_cast<const float4*>(h + 4);
-  float s = h0.x * bf16lo(b.x);
-  s = fmaf(h0.y, bf16hi(b.x), s);
-  s = fmaf(h0.z, bf16lo(b.y), s);
-  s = fmaf(h0.w, bf16hi(b.y), s);
-  s = fmaf(h1.x, bf16lo(b.z), s);
-  s = fmaf(h1.y, bf16hi(b.z), s);
-  s = fmaf(h1.z, bf16lo(b.w), s);
-  s = fmaf(h1.w, bf16hi(b.w), s);
-  return s;
+// L2 prefetch (by the lanes of one warp) of the B rows of this CTA's columns.
+__device__ __forceinline__ void prefetch_b(const DeltaArgs& a, const SlotView& v, int cb, int ce,
+                                           int lane) {
+  for (int j = lane; j < a.sl.S; j += 32) {
+    if (v.ja[j] < 0) continue;
+    const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
+    if (c1 > c0)
+      bulk_prefetch_l2(v.B[j] + (size_t)(c0 - a.rel[j]) * a.R, (uint32_t)((c1 - c0) * a.R * 2));
+  }
+}
+
+// L2 prefetch of the out segments of the pass's rows in this CTA's columns.
+template <class Tables>
+__device__ __forceinline__ void prefetch_out(const DeltaArgs& a, const Tables& tb,
+                                             const SlotView& v, const int* prow, int nr, int cb,
+                                             int ce, int lane) {
+  for (int j = 0; j < a.sl.S; ++j) {
+    if (v.ja[j] < 0) continue;
+    const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
+    if (c1 <= c0) continue;
+    for (int r = lane; r < nr; r += 32)
+      bulk_prefetch_l2(a.out + tb.out_row(prow[r]) * a.ld_out + a.sl.off[j] + (c0 - a.rel[j]),
+                       (uint32_t)((c1 - c0) * 2));
+  }
 }
 
 template <int RMAX, int MODE, class Tables>
-__global__ void __launch_bounds__(kThreads) delta_cluster_kernel(const DeltaArgs a, const Tables tb) {
+__global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
+    delta_cluster_kernel(const DeltaArgs a, const Tables tb) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ SlotView v;
+  __shared__ int warp_cnt[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
   const int key = (int)cluster_index_x();
   const uint32_t crank = cluster_rank();
-  uint32_t ncta;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
+  const int ncta = a.cs;
 
-  __shared__ SlotView v;
+  const SmemPlan plan = smem_plan(a, MODE);
+  int* prow = reinterpret_cast<int*>(smem + 64);  // this pass's row ids
+  int* rows_s = reinterpret_cast<int*>(smem + plan.rows_off);
+  __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(smem + plan.As_off);
+  __nv_bfloat16* Xs = reinterpret_cast<__nv_bfloat16*>(smem + plan.Xs_off);
+  float* Pw = reinterpret_cast<float*>(smem + plan.Pw_off);
+  float* Rx = reinterpret_cast<float*>(smem + plan.Rx_off);
+  float* H = reinterpret_cast<float*>(smem + plan.H_off);
+  const int stride = plan.as_stride, SR16 = plan.sr16;
+
+  // ---- prologue: independent of the preceding kernel's outputs ----------
   if (tid == 0) {
     uint32_t bad = 0;
     tb.resolve(key, a.sl.S, MODE, v, bad);
     if (bad && crank == 0) set_error(a.err, bad);
   }
   __syncthreads();
+  const int R = a.R;
+  const int SRa = v.nact * R;
+  const int k_lo = min(a.k_in, (int)crank * a.kc);
+  const int k_hi = min(a.k_in, k_lo + a.kc);
+  const int nst = (k_hi - k_lo + a.kst - 1) / a.kst;  // shrink stages of this CTA
+  const int cb = min(a.sl.n_cols, (int)crank * a.cpc);
+  const int ce = min(a.sl.n_cols, cb + a.cpc);
+  // Adapter weights are never produced by the preceding kernel, so their
+  // copies may start before the dependency wait and overlap its tail.
+  const bool early = MODE != kModeExpand && a.early && v.nact > 0 && nst > 0;
+  if (early) {
+    copy_a_rows(a, v, SRa, k_lo, min(a.kst, k_hi - k_lo), As, stride, tid);
+    cp_async_commit();
+  }
+  if (v.nact > 0 && MODE == kModeFused && warp == 1) prefetch_b(a, v, cb, ce, lane);
+  cudaTriggerProgrammaticLaunchCompletion();
+  cudaGridDependencySynchronize();
   if (v.nact == 0) return;  // the same decision in every CTA of the cluster
-
-  const SmemPlan plan = smem_plan(a.row_cap, a.sr_max, a.ks, MODE);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  int* prow = reinterpret_cast<int*>(smem + 16);  // this pass's row ids
-  int* rows_s = reinterpret_cast<int*>(smem + plan.rows_off);
-  float* P = reinterpret_cast<float*>(smem + plan.P_off);
-  float* H = reinterpret_cast<float*>(smem + plan.H_off);
-  __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(smem + plan.A_off);
-  __nv_bfloat16* Xs = reinterpret_cast<__nv_bfloat16*>(smem + plan.X_off);
-  __shared__ int warp_cnt[kWarps];
 
   // ---- the key's rows, in ascending row order --------------------------
   int nrows;
@@ -224,6 +295,7 @@ __global__ void __launch_bounds__(kThreads) delta_cluster_kernel(const DeltaArgs
       if (lane == 0) warp_cnt[warp] = __popc(m);
       __syncthreads();
       int before = total, sum = 0;
+#pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         before += (w < warp) ? warp_cnt[w] : 0;
         sum += warp_cnt[w];
@@ -237,150 +309,259 @@ __global__ void __launch_bounds__(kThreads) delta_cluster_kernel(const DeltaArgs
     nrows = total;
     rows = rows_s;
   }
-  if (nrows == 0) return;  // uniform across the cluster
-
-  const int R = a.R;
-  const int SRa = v.nact * R;
-  const int k_lo = (int)crank * a.kc;
-  const int k_hi = min(a.k_in, k_lo + a.kc);
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_barrier_init();
+  if (nrows == 0 || nrows < a.min_rows || nrows >= a.max_rows) {  // uniform
+    if (early) cp_async_wait<0>();  // no copy may land in a CTA that has exited
+    return;
   }
-  __syncthreads();
-  uint32_t phase = 0;
-  bool timed_out = false;
+
+  const int mt = (SRa + 15) / 16;  // 16-pair tiles of the shrink
+  const int SRk = mt * 16;         // this key's padded pair count (Pw row stride)
+  // shrink work split: G k-groups x mt pair tiles over the 8 warps
+  const int G = mt >= kWarps ? 1 : kWarps / mt;
+  const int my_g = mt >= kWarps ? 0 : warp / mt;
+  const int my_m0 = mt >= kWarps ? warp : warp % mt;
+  const bool shrink_warp = mt >= kWarps || warp < G * mt;
+  const bool timed_out = false;  // (no bounded waits in this kernel)
+  bool skip_a0 = early;  // stage-0 A rows already in shared memory (early copy / resident)
+
+  if (MODE != kModeExpand && SRa < SR16) {  // pad pair rows contract to zero
+    const int per_buf = (SR16 - SRa) * stride / 8;
+    for (int i = tid; i < a.nbuf * per_buf; i += kThreads) {
+      const int b = i / per_buf, rem = i - b * per_buf;
+      reinterpret_cast<uint4*>(As + (size_t)b * SR16 * stride + (size_t)SRa * stride)[rem] =
+          make_uint4(0, 0, 0, 0);
+    }
+  }
 
   for (int p0 = 0; p0 < nrows; p0 += kRowsPerPass) {
     const int nr = min(kRowsPerPass, nrows - p0);
-    __syncthreads();  // the previous pass's readers of prow are done
+    __syncthreads();  // the previous pass is done with prow and the buffers
     if (tid < nr) prow[tid] = rows[p0 + tid];
-    if (MODE != kModeExpand)
-      for (int i = tid; i < nr * SRa; i += kThreads) P[i] = 0.0f;
+    if (MODE != kModeExpand) {  // pad x rows of the pass contract to zero
+      const int pad = (kRowsPerPass - nr) * stride / 8;  // 16-byte units
+      for (int i = tid; i < a.nbuf * pad; i += kThreads) {
+        const int b = i / pad, rem = i - b * pad;
+        reinterpret_cast<uint4*>(Xs + (size_t)b * kRowsPerPass * stride + (size_t)nr * stride)[rem] =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    __syncthreads();
+    if (MODE != kModeShrink && warp == 2) prefetch_out(a, tb, v, prow, nr, cb, ce, lane);
 
     if (MODE != kModeExpand) {
-      // ---- shrink over this CTA's k-range ---------------------------------
-      for (int k0 = k_lo; k0 < k_hi; k0 += a.ks) {
-        const int kw = min(a.ks, k_hi - k0);
-        __syncthreads();  // stage buffers free, prow / P visible
-        if (warp == 0) {
-          if (lane == 0) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, (uint32_t)((SRa + nr) * kw * 2));
-          }
-          __syncwarp();
-          for (int t = lane; t < SRa + nr; t += 32) {
-            const __nv_bfloat16* src;
-            __nv_bfloat16* dst;
-            if (t < SRa) {
-              const int jj = t / R, q = t - jj * R;
-              src = v.A[v.act_slice[jj]] + (size_t)q * a.k_in + k0;
-              dst = As + (size_t)t * a.ks;
-            } else {
-              const int r = t - SRa;
-              src = a.x + tb.x_row(prow[r]) * a.ld_x + k0;
-              dst = Xs + (size_t)r * a.ks;
-            }
-            bulk_g2s(dst, src, (uint32_t)kw * 2u, bar);
+      // ---- copies of the first two stages ---------------------------------
+      if (nst > 0) {
+        if (!skip_a0) copy_a_rows(a, v, SRa, k_lo, min(a.kst, k_hi - k_lo), As, stride, tid);
+        copy_x_rows(a, tb, prow, nr, k_lo, min(a.kst, k_hi - k_lo), Xs, stride, tid);
+        cp_async_commit();
+        if (nst > 1) {
+          const int k1 = k_lo + a.kst;
+          copy_a_rows(a, v, SRa, k1, min(a.kst, k_hi - k1), As + (size_t)SR16 * stride, stride,
+                      tid);
+          copy_x_rows(a, tb, prow, nr, k1, min(a.kst, k_hi - k1),
+                      Xs + (size_t)kRowsPerPass * stride, stride, tid);
+          cp_async_commit();
+        }
+      }
+      skip_a0 = (nst == 1);  // a single stage keeps its A rows for the next passes
+
+      // ---- shrink on the tensor cores: partial P[pair][row] over this CTA's k
+      float acc[4][8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
+      for (int st = 0; st < nst; ++st) {
+        const int buf = st & 1;
+        const int k0 = k_lo + st * a.kst;
+        const int kw = min(a.kst, k_hi - k0);
+        if (st + 1 < nst)
+          cp_async_wait<1>();  // this stage landed; the next may still be in flight
+        else
+          cp_async_wait<0>();
+        __nv_bfloat16* Ab = As + (size_t)buf * SR16 * stride;
+        __nv_bfloat16* Xb = Xs + (size_t)buf * kRowsPerPass * stride;
+        if (kw & 15) {  // odd half k-step: zero the 8 columns after kw (never copied)
+          for (int i = tid; i < SRa + nr; i += kThreads) {
+            __nv_bfloat16* rowp = (i < SRa) ? Ab + (size_t)i * stride : Xb + (size_t)(i - SRa) * stride;
+            *reinterpret_cast<uint4*>(rowp + kw) = make_uint4(0, 0, 0, 0);
           }
         }
-        if (!mbar_wait_bounded(bar, phase)) timed_out = true;
-        phase ^= 1u;
-        for (int pr = warp; pr < SRa; pr += kWarps) {
-          float acc[kRowsPerPass];
+        __syncthreads();
+        if (shrink_warp) {
+          const int ksteps = (kw + 15) / 16;
+          const uint32_t xaddr = smem_addr(Xb + (size_t)(((lane >> 4) << 3) + (lane & 7)) * stride +
+                                           ((lane >> 3) & 1) * 8);
+          const uint32_t aaddr = smem_addr(Ab + (size_t)(my_m0 * 16 + (((lane >> 3) & 1) << 3) +
+                                                         (lane & 7)) * stride + ((lane >> 4) << 3));
+          const uint32_t mstep = 8u * 16u * (uint32_t)stride * 2u;  // 8 pair tiles, bytes
+          for (int ks = my_g; ks < ksteps; ks += G) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
 #pragma unroll
-          for (int r = 0; r < kRowsPerPass; ++r) acc[r] = 0.0f;
-          for (int kv = lane * 8; kv < kw; kv += 256) {
-            const uint4 av = *reinterpret_cast<const uint4*>(As + (size_t)pr * a.ks + kv);
-#pragma unroll
-            for (int r = 0; r < kRowsPerPass; ++r)
-              if (r < nr)
-                acc[r] += dot8(av, *reinterpret_cast<const uint4*>(Xs + (size_t)r * a.ks + kv));
-          }
-#pragma unroll
-          for (int r = 0; r < kRowsPerPass; ++r) {
-            if (r < nr) {
-              const float s = warp_sum(acc[r]);
-              if (lane == 0) P[r * SRa + pr] += s;
+            for (int i = 0; i < 4; ++i) {
+              if (my_m0 + i * kWarps < mt && (i == 0 || mt >= kWarps)) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(aaddr + i * mstep + ks * 32, a0, a1, a2, a3);
+                mma_16816(&acc[i][0], a0, a1, a2, a3, b0, b1);
+                mma_16816(&acc[i][4], a0, a1, a2, a3, b2, b3);
+              }
             }
+          }
+        }
+        __syncthreads();  // buffer `buf` free
+        if (st + 2 < nst) {
+          const int k2 = k0 + 2 * a.kst;
+          copy_a_rows(a, v, SRa, k2, min(a.kst, k_hi - k2), Ab, stride, tid);
+          copy_x_rows(a, tb, prow, nr, k2, min(a.kst, k_hi - k2), Xb, stride, tid);
+          cp_async_commit();
+        }
+      }
+      // per-warp k-group partials -> Pw[g][pair][row]
+      if (shrink_warp) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int m = my_m0 + i * kWarps;
+          if (m < mt && (i == 0 || mt >= kWarps)) {
+            float* base = Pw + ((size_t)my_g * SRk + m * 16 + gq) * kRowsPerPass + 2 * tq;
+            base[0] = acc[i][0];
+            base[1] = acc[i][1];
+            base[8 * kRowsPerPass] = acc[i][2];
+            base[8 * kRowsPerPass + 1] = acc[i][3];
+            base[8] = acc[i][4];
+            base[9] = acc[i][5];
+            base[8 * kRowsPerPass + 8] = acc[i][6];
+            base[8 * kRowsPerPass + 9] = acc[i][7];
           }
         }
       }
       __syncthreads();
-      // ---- the CS partials meet in every CTA through DSMEM ----------------
-      cluster_arrive();
+      // ---- the CS partials meet through DSMEM in two pushes: every CTA
+      // stores its partial of entry e into the receive area of e's owner;
+      // each owner sums its entries over the cluster in rank order and stores
+      // the sum into every CTA's H.  Only remote stores, no remote loads. ----
+      const int nel = nr * SRa;
+      const int per = plan.rx_per;
+      {
+        const uint32_t rx_addr = smem_addr(Rx);
+        for (int e = tid; e < nel; e += kThreads) {
+          const int r = e / SRa, p = e - r * SRa;
+          float s = 0.0f;
+          for (int g = 0; g < G; ++g) s += Pw[((size_t)g * SRk + p) * kRowsPerPass + r];
+          const int owner = e / per, slot = e - owner * per;
+          dsmem_st_f32(dsmem_map(rx_addr + 4u * (uint32_t)(crank * per + slot), owner), s);
+        }
+      }
+      cluster_arrive();  // partials delivered
       cluster_wait();
-      const uint32_t P_addr = smem_addr(P);
-      for (int i = tid; i < nr * SRa; i += kThreads) {
-        float s = 0.0f;
-        for (uint32_t c = 0; c < ncta; ++c) s += dsmem_ld_f32(dsmem_map(P_addr + 4u * i, c));
-        H[i] = s;
+      {
+        const uint32_t h_addr = smem_addr(H);
+        const int e0 = (int)crank * per;
+        for (int i = tid; i < per; i += kThreads) {
+          const int e = e0 + i;
+          if (e >= nel) break;
+          float sum = 0.0f;
+          for (int c = 0; c < ncta; ++c) sum += Rx[c * per + i];
+          const int r = e / SRa, p = e - r * SRa;
+          const uint32_t off = 4u * (uint32_t)(r * SR16 + p);
+          for (int c = 0; c < ncta; ++c) dsmem_st_f32(dsmem_map(h_addr + off, c), sum);
+        }
       }
-      __syncthreads();
-      cluster_arrive();  // this CTA is done reading the others' partials
+      cluster_arrive();  // sums delivered
+      cluster_wait();
     } else {
-      __syncthreads();
       for (int i = tid; i < nr * SRa; i += kThreads) {
-        const int r = i / SRa, t = i - r * SRa, jj = t / R, q = t - jj * R;
-        const int j = v.act_slice[jj];
-        H[i] = a.h[((size_t)j * a.n + prow[r]) * R + q];
+        const int r = i / SRa, t = i - r * SRa;
+        const int jj = t / R, q = t - jj * R;
+        H[r * SR16 + t] = a.h[((size_t)v.act_slice[jj] * a.n + prow[r]) * R + q];
       }
       __syncthreads();
     }
 
     if (MODE == kModeShrink) {
       // h[j, row, q] += scale * H, the cluster's CTAs splitting the entries.
-      for (int i = (int)crank * kThreads + tid; i < nr * SRa; i += (int)ncta * kThreads) {
+      for (int i = (int)crank * kThreads + tid; i < nr * SRa; i += ncta * kThreads) {
         const int r = i / SRa, t = i - r * SRa, jj = t / R, q = t - jj * R;
         const int j = v.act_slice[jj];
         float* dst = a.h + ((size_t)j * a.n + prow[r]) * R + q;
-        *dst = *dst + H[i] * v.scale;
+        *dst = *dst + H[r * SR16 + t] * v.scale;
       }
     } else if (!timed_out) {
-      // ---- expand + fold over this CTA's columns --------------------------
-      const int cb = (int)crank * a.cpc;
-      const int ce = min(a.sl.n_cols, cb + a.cpc);
-      for (int c2 = cb + 2 * tid; c2 < ce; c2 += 2 * kThreads) {
-        int j = 0;
-#pragma unroll
-        for (int jj = 1; jj < kMaxSlices; ++jj)
-          if (jj < a.sl.S && c2 >= a.rel[jj]) j = jj;
+      // ---- expand + fold on the tensor cores, 8 columns per tile ----------
+      // A operand: the pass's h rows of one slice as a bf16 (hi, lo) pair, so
+      // the rank contraction keeps ~fp32 accuracy (rows >= nr only feed
+      // discarded outputs); B operand: B rows, L2 hits after the prefetch.
+      constexpr int KS = RMAX / 16;
+      constexpr int NB = (4 / KS) > 0 ? (4 / KS) : 1;  // column tiles per load batch
+      const int row0 = gq, row1 = gq + 8;
+      const bool ok0 = row0 < nr, ok1 = row1 < nr;
+      const int64_t orow0 = ok0 ? tb.out_row(prow[row0]) : 0;
+      const int64_t orow1 = ok1 ? tb.out_row(prow[row1]) : 0;
+      const float sc = v.scale;
+      for (int j = 0; j < a.sl.S; ++j) {
         const int ja = v.ja[j];
         if (ja < 0) continue;
-        const int cl = c2 - a.rel[j];
-        const __nv_bfloat16* b0 = v.B[j] + (size_t)cl * R;
-        uint4 bq0[RMAX / 8], bq1[RMAX / 8];
+        const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
+        if (c1 <= c0) continue;
+        const int ntl = (c1 - c0) / 8;
+        if (warp >= ntl) continue;
+        uint32_t ahi[KS][4], alo[KS][4];
+        {
+          const float* hb = H + ja * R + 2 * tq;
 #pragma unroll
-        for (int u = 0; u < RMAX / 8; ++u) {
-          if (u * 8 < R) {
-            bq0[u] = ldg_nc_v4(b0 + u * 8);
-            bq1[u] = ldg_nc_v4(b0 + R + u * 8);
+          for (int kk = 0; kk < KS; ++kk) {
+            const bool lo_ok = kk * 16 < R, hi_ok = kk * 16 + 8 < R;
+            const float* h0 = hb + row0 * SR16 + kk * 16;
+            const float* h1 = hb + row1 * SR16 + kk * 16;
+            split_bf16x2(lo_ok ? h0[0] : 0.f, lo_ok ? h0[1] : 0.f, ahi[kk][0], alo[kk][0]);
+            split_bf16x2(lo_ok ? h1[0] : 0.f, lo_ok ? h1[1] : 0.f, ahi[kk][1], alo[kk][1]);
+            split_bf16x2(hi_ok ? h0[8] : 0.f, hi_ok ? h0[9] : 0.f, ahi[kk][2], alo[kk][2]);
+            split_bf16x2(hi_ok ? h1[8] : 0.f, hi_ok ? h1[9] : 0.f, ahi[kk][3], alo[kk][3]);
           }
         }
-        const float* Hj = H + ja * R;
-        for (int r = 0; r < nr; ++r) {
-          const float* hr = Hj + r * SRa;
-          float d0 = 0.0f, d1 = 0.0f;
+        const int cl0 = c0 - a.rel[j];
+        const __nv_bfloat16* bbase = v.B[j] + (size_t)(cl0 + gq) * R + 2 * tq;
+        __nv_bfloat16* o0base = a.out + orow0 * a.ld_out + a.sl.off[j] + cl0 + 2 * tq;
+        __nv_bfloat16* o1base = a.out + orow1 * a.ld_out + a.sl.off[j] + cl0 + 2 * tq;
+        for (int t0 = warp; t0 < ntl; t0 += kWarps * NB) {
+          uint32_t bf[NB][KS][2], ov[NB][2];
 #pragma unroll
-          for (int u = 0; u < RMAX / 8; ++u) {
-            if (u * 8 < R) {
-              d0 += dot8h(hr + u * 8, bq0[u]);
-              d1 += dot8h(hr + u * 8, bq1[u]);
+          for (int b = 0; b < NB; ++b) {  // every load of the batch first
+            const int t = t0 + b * kWarps;
+            if (t < ntl) {
+              const __nv_bfloat16* brow = bbase + (size_t)t * 8 * R;
+#pragma unroll
+              for (int kk = 0; kk < KS; ++kk) {
+                bf[b][kk][0] = (kk * 16 < R) ? ldg_nc_u32(brow + kk * 16) : 0u;
+                bf[b][kk][1] = (kk * 16 + 8 < R) ? ldg_nc_u32(brow + kk * 16 + 8) : 0u;
+              }
+              ov[b][0] = (a.add_inputs && ok0) ? *reinterpret_cast<const uint32_t*>(o0base + t * 8) : 0u;
+              ov[b][1] = (a.add_inputs && ok1) ? *reinterpret_cast<const uint32_t*>(o1base + t * 8) : 0u;
             }
           }
-          const float v0 = v.scale * d0, v1 = v.scale * d1;
-          uint32_t* o = reinterpret_cast<uint32_t*>(a.out + tb.out_row(prow[r]) * a.ld_out +
-                                                    a.sl.off[j] + cl);
-          if (a.add_inputs) {
-            const uint32_t ov = *o;
-            *o = pack_bf16x2(bf16lo(ov) + v0, bf16hi(ov) + v1);
-          } else {
-            *o = pack_bf16x2(v0, v1);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const int t = t0 + b * kWarps;
+            if (t < ntl) {
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int kk = 0; kk < KS; ++kk) {
+                if (kk * 16 < R) {
+                  mma_16816(d, ahi[kk][0], ahi[kk][1], ahi[kk][2], ahi[kk][3], bf[b][kk][0], bf[b][kk][1]);
+                  mma_16816(d, alo[kk][0], alo[kk][1], alo[kk][2], alo[kk][3], bf[b][kk][0], bf[b][kk][1]);
+                }
+              }
+              if (ok0)
+                *reinterpret_cast<uint32_t*>(o0base + t * 8) =
+                    pack_bf16x2(bf16lo(ov[b][0]) + sc * d[0], bf16hi(ov[b][0]) + sc * d[1]);
+              if (ok1)
+                *reinterpret_cast<uint32_t*>(o1base + t * 8) =
+                    pack_bf16x2(bf16lo(ov[b][1]) + sc * d[2], bf16hi(ov[b][1]) + sc * d[3]);
+            }
           }
         }
       }
     }
-    if (MODE != kModeExpand) cluster_wait();  // peers done with this CTA's partials
   }
   if (timed_out && tid == 0) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
 }
@@ -388,6 +569,7 @@ __global__ void __launch_bounds__(kThreads) delta_cluster_kernel(const DeltaArgs
 // Zeros for the MoE pairs that get no delta (the no-key bucket).
 __global__ void zero_rows_kernel(__nv_bfloat16* out, int64_t ld_out, int width,
                                  const int32_t* perm, const int32_t* seg_start, int bucket) {
+  cudaGridDependencySynchronize();
   const int s0 = seg_start[bucket], s1 = seg_start[bucket + 1];
   const int vec_per_row = width / 8;
   const int64_t total = (int64_t)(s1 - s0) * vec_per_row;
