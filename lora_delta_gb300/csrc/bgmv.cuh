@@ -144,10 +144,13 @@ struct DeltaArgs {
 };
 
 constexpr int kRowsPerPass = 16;  // rows of one pass: two 8-wide MMA column tiles
+constexpr int kBStageBytes = 32 * 1024;  // largest B slab staged in shared memory
 
 // Shared-memory plan (bytes), identical on host and device.
 struct SmemPlan {
-  int rows_off, As_off, Xs_off, Pw_off, Rx_off, H_off, total;
+  int rows_off, As_off, Xs_off, Pw_off, Rx_off, H_off, Bs_off, Os_off, total;
+  int b_staged;   // the CTA's B rows fit in shared memory
+  int o_stride;   // elements per staged out row (padded)
   int as_stride;  // elements per A / x row in shared memory (padded)
   int sr16;       // S * R rounded up to 16
   int rx_per;     // (row, pair) entries owned by one CTA of the cluster
@@ -171,6 +174,13 @@ __host__ __device__ inline SmemPlan smem_plan(const DeltaArgs& a, int mode) {
   if (mode != kModeExpand) o += a.cs * p.rx_per * 4;
   p.H_off = o;
   o += kRowsPerPass * p.sr16 * 4;
+  // expand operands: the CTA's B rows and the pass's out segments
+  p.b_staged = (mode != kModeShrink && a.cpc * a.R * 2 <= kBStageBytes) ? 1 : 0;
+  p.o_stride = a.cpc + 8;
+  p.Bs_off = o;
+  if (p.b_staged) o += a.cpc * a.R * 2;
+  p.Os_off = o;
+  if (p.b_staged && a.add_inputs) o += kRowsPerPass * p.o_stride * 2;
   p.total = o;
   return p;
 }
@@ -199,6 +209,40 @@ __device__ __forceinline__ void copy_x_rows(const DeltaArgs& a, const Tables& tb
   for (int idx = tid; idx < nr * vpr; idx += kThreads) {
     const int r = idx / vpr, c = idx - r * vpr;
     cp_async16(Xs + (size_t)r * stride + c * 8, a.x + tb.x_row(prow[r]) * a.ld_x + k0 + c * 8);
+  }
+}
+
+// cp.async copies of the B rows of this CTA's columns [cb, ce) into Bs
+// (column c at Bs[(c - cb) * R]).
+__device__ __forceinline__ void copy_b_rows(const DeltaArgs& a, const SlotView& v, int cb, int ce,
+                                            __nv_bfloat16* Bs, int tid) {
+  for (int j = 0; j < a.sl.S; ++j) {
+    if (v.ja[j] < 0) continue;
+    const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
+    if (c1 <= c0) continue;
+    const int nvec = (c1 - c0) * a.R / 8;
+    const __nv_bfloat16* src = v.B[j] + (size_t)(c0 - a.rel[j]) * a.R;
+    __nv_bfloat16* dst = Bs + (size_t)(c0 - cb) * a.R;
+    for (int i = tid; i < nvec; i += kThreads) cp_async16(dst + i * 8, src + i * 8);
+  }
+}
+
+// cp.async copies of the pass's out segments in this CTA's columns into Os
+// (row r, column c at Os[r * o_stride + (c - cb)]).
+template <class Tables>
+__device__ __forceinline__ void copy_out_rows(const DeltaArgs& a, const Tables& tb,
+                                              const SlotView& v, const int* prow, int nr, int cb,
+                                              int ce, __nv_bfloat16* Os, int o_stride, int tid) {
+  for (int j = 0; j < a.sl.S; ++j) {
+    if (v.ja[j] < 0) continue;
+    const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
+    if (c1 <= c0) continue;
+    const int vpr = (c1 - c0) / 8;
+    for (int i = tid; i < nr * vpr; i += kThreads) {
+      const int r = i / vpr, c = i - r * vpr;
+      cp_async16(Os + (size_t)r * o_stride + (c0 - cb) + c * 8,
+                 a.out + tb.out_row(prow[r]) * a.ld_out + a.sl.off[j] + (c0 - a.rel[j]) + c * 8);
+    }
   }
 }
 
@@ -248,7 +292,11 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
   float* Pw = reinterpret_cast<float*>(smem + plan.Pw_off);
   float* Rx = reinterpret_cast<float*>(smem + plan.Rx_off);
   float* H = reinterpret_cast<float*>(smem + plan.H_off);
+  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(smem + plan.Bs_off);
+  __nv_bfloat16* Os = reinterpret_cast<__nv_bfloat16*>(smem + plan.Os_off);
   const int stride = plan.as_stride, SR16 = plan.sr16;
+  const bool b_staged = plan.b_staged != 0;
+  const bool o_staged = b_staged && a.add_inputs;
 
   // ---- prologue: independent of the preceding kernel's outputs ----------
   if (tid == 0) {
@@ -269,9 +317,11 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
   const bool early = MODE != kModeExpand && a.early && v.nact > 0 && nst > 0;
   if (early) {
     copy_a_rows(a, v, SRa, k_lo, min(a.kst, k_hi - k_lo), As, stride, tid);
+    if (b_staged) copy_b_rows(a, v, cb, ce, Bs, tid);
     cp_async_commit();
   }
-  if (v.nact > 0 && MODE == kModeFused && warp == 1) prefetch_b(a, v, cb, ce, lane);
+  bool b_loaded = early && b_staged;
+  if (v.nact > 0 && MODE != kModeShrink && !b_staged && warp == 1) prefetch_b(a, v, cb, ce, lane);
   cudaTriggerProgrammaticLaunchCompletion();
   cudaGridDependencySynchronize();
   if (v.nact == 0) return;  // the same decision in every CTA of the cluster
@@ -346,7 +396,16 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       }
     }
     __syncthreads();
-    if (MODE != kModeShrink && warp == 2) prefetch_out(a, tb, v, prow, nr, cb, ce, lane);
+    if (MODE != kModeShrink) {
+      // expand operands of the pass: into shared memory when they fit, else L2
+      if (b_staged && !b_loaded) copy_b_rows(a, v, cb, ce, Bs, tid);
+      b_loaded = b_staged;
+      if (o_staged)
+        copy_out_rows(a, tb, v, prow, nr, cb, ce, Os, plan.o_stride, tid);
+      else if (warp == 2)
+        prefetch_out(a, tb, v, prow, nr, cb, ce, lane);
+      cp_async_commit();  // (its own group, so the stage waits below stay in order)
+    }
 
     if (MODE != kModeExpand) {
       // ---- copies of the first two stages ---------------------------------
@@ -490,7 +549,11 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       // ---- expand + fold on the tensor cores, 8 columns per tile ----------
       // A operand: the pass's h rows of one slice as a bf16 (hi, lo) pair, so
       // the rank contraction keeps ~fp32 accuracy (rows >= nr only feed
-      // discarded outputs); B operand: B rows, L2 hits after the prefetch.
+      // discarded outputs); B operand: B rows from shared memory (or L2).
+      if (b_staged) {
+        cp_async_wait<0>();  // B rows and out segments landed
+        __syncthreads();
+      }
       constexpr int KS = RMAX / 16;
       constexpr int NB = (4 / KS) > 0 ? (4 / KS) : 1;  // column tiles per load batch
       const int row0 = gq, row1 = gq + 8;
@@ -520,13 +583,44 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
           }
         }
         const int cl0 = c0 - a.rel[j];
-        const __nv_bfloat16* bbase = v.B[j] + (size_t)(cl0 + gq) * R + 2 * tq;
         __nv_bfloat16* o0base = a.out + orow0 * a.ld_out + a.sl.off[j] + cl0 + 2 * tq;
         __nv_bfloat16* o1base = a.out + orow1 * a.ld_out + a.sl.off[j] + cl0 + 2 * tq;
+        if (b_staged) {
+          // operands in shared memory: one tile at a time
+          const __nv_bfloat16* bsb = Bs + (size_t)(c0 - cb + gq) * R + 2 * tq;
+          const __nv_bfloat16* os0 = Os + (size_t)row0 * plan.o_stride + (c0 - cb) + 2 * tq;
+          const __nv_bfloat16* os1 = Os + (size_t)row1 * plan.o_stride + (c0 - cb) + 2 * tq;
+          for (int t = warp; t < ntl; t += kWarps) {
+            const __nv_bfloat16* brow = bsb + (size_t)t * 8 * R;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              if (kk * 16 < R) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(brow + kk * 16);
+                const uint32_t b1 =
+                    (kk * 16 + 8 < R) ? *reinterpret_cast<const uint32_t*>(brow + kk * 16 + 8) : 0u;
+                mma_16816(d, ahi[kk][0], ahi[kk][1], ahi[kk][2], ahi[kk][3], b0, b1);
+                mma_16816(d, alo[kk][0], alo[kk][1], alo[kk][2], alo[kk][3], b0, b1);
+              }
+            }
+            if (ok0) {
+              const uint32_t o = a.add_inputs ? *reinterpret_cast<const uint32_t*>(os0 + t * 8) : 0u;
+              *reinterpret_cast<uint32_t*>(o0base + t * 8) =
+                  pack_bf16x2(bf16lo(o) + sc * d[0], bf16hi(o) + sc * d[1]);
+            }
+            if (ok1) {
+              const uint32_t o = a.add_inputs ? *reinterpret_cast<const uint32_t*>(os1 + t * 8) : 0u;
+              *reinterpret_cast<uint32_t*>(o1base + t * 8) =
+                  pack_bf16x2(bf16lo(o) + sc * d[2], bf16hi(o) + sc * d[3]);
+            }
+          }
+          continue;
+        }
+        const __nv_bfloat16* bbase = v.B[j] + (size_t)(cl0 + gq) * R + 2 * tq;
         for (int t0 = warp; t0 < ntl; t0 += kWarps * NB) {
           uint32_t bf[NB][KS][2], ov[NB][2];
 #pragma unroll
-          for (int b = 0; b < NB; ++b) {  // every load of the batch first
+          for (int b = 0; b < NB; ++b) {  // every load of the batch first (L2 hits)
             const int t = t0 + b * kWarps;
             if (t < ntl) {
               const __nv_bfloat16* brow = bbase + (size_t)t * 8 * R;
