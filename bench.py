@@ -390,8 +390,8 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src):
     # prefill SGMV gate_up (8192 rows)
     case = inputs.prefill_gate_up_case()
     d = di.linear_to_device(case, device)
-    ws = torch.empty(ld.lora_workspace_size(case.n, case.max_loras), dtype=torch.uint8,
-                     device=device)
+    ws = torch.empty(ld.lora_workspace_size(case.n, len(case.widths), case.max_rank,
+                                         case.max_loras), dtype=torch.uint8, device=device)
     ms = timed(lambda: ld.lora_delta_fused(d.out0, d.x, d.seq_slot, d.pool, workspace=ws))
     ab, fl = algorithmic_bytes(case), algorithmic_flops(case)
     gbs, tfs = ab / (ms / 1e3) / 1e9, fl / (ms / 1e3) / 1e12
@@ -424,7 +424,7 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src):
         mc = inputs.moe_case(shared_a=shared)
         dm = di.moe_to_device(mc, device)
         out = torch.empty(mc.T, mc.top_k, 2 * mc.I, dtype=torch.bfloat16, device=device)
-        ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L),
+        ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L, mc.rank, shared),
                          dtype=torch.uint8, device=device)
         ms = timed(lambda: ld.lora_moe_fc1_delta(out, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b,
                                                  dm.stride_b, shared, dm.topk_ids, dm.lora_ids,

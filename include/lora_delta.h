@@ -101,13 +101,15 @@ int lora_pool_pack(void *a_slot, void *b_slot, const void *a_r, const void *b_r,
  *   widths [S] int32 (HOST): the output slice widths; slice j's columns start
  *     at offset_start + widths[0] + ... + widths[j-1] ([punica] add_expand).
  *
- * Workspace: when n > 1024 the rows are first clustered by slot on the
- * device (a stable counting sort, [punica] prefill_metadata) into a
- * caller-provided scratch buffer of lora_workspace_size(n, max_loras) bytes,
- * 256-byte aligned.  For n <= 1024 each kernel clusters its own rows and the
- * workspace may be NULL.
+ * Workspace: when n > 1024, or when a workspace is given and n >= 256, the
+ * rows are first clustered by slot on the device (a stable counting sort,
+ * [punica] prefill_metadata) into a caller-provided scratch buffer of
+ * lora_workspace_size(n, S, R, max_loras) bytes, 256-byte aligned; the same
+ * buffer holds the fp32 rank intermediate of the tensor-core path that
+ * lora_delta_fused takes for slots with many rows.  For n <= 1024 with no
+ * workspace each kernel clusters its own rows.
  */
-size_t lora_workspace_size(int n, int max_loras);
+size_t lora_workspace_size(int n, int S, int R, int max_loras);
 
 /*
  * lora_route -- the routing step on its own ([punica] prefill_metadata):
@@ -182,9 +184,10 @@ int lora_delta_fused(void *out, int64_t ld_out, const void *x, int n, int k_in,
  * and set LORA_DEV_ERR_LORA / LORA_DEV_ERR_EXPERT.  The delta stays per
  * (token, slot): no routing weights, no sum over experts.
  * Requires H, I, rank multiples of 8, rank <= 128, E * num_loras <= 3071 and
- * a workspace of lora_moe_workspace_size(T, top_k, E, num_loras) bytes.
+ * a workspace of lora_moe_workspace_size(T, top_k, E, num_loras, rank,
+ * shared_a) bytes.
  */
-size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras);
+size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras, int rank, int shared_a);
 int lora_moe_fc1_delta(void *out, const void *x, const int64_t *w_ptr_a, int64_t stride_a,
                        const int64_t *w_ptr_b, int64_t stride_b, int shared_a,
                        const int32_t *topk_ids, const int32_t *lora_ids, int T, int top_k, int E,
@@ -202,7 +205,7 @@ int lora_moe_fc1_delta(void *out, const void *x, const int64_t *w_ptr_a, int64_t
  * scratch comes from a fixed buffer inside the library of
  * lora_noalloc_scratch_bytes() bytes (4 MiB), held on every GPU that loads
  * the library until the process exits.  A call whose workspace need
- * (lora_workspace_size(n, max_loras)) exceeds it returns LORA_ERR_TOO_LARGE
+ * (lora_workspace_size(n, S, R, max_loras)) exceeds it returns LORA_ERR_TOO_LARGE
  * and enqueues nothing.  The call never allocates (no cudaMalloc, no
  * allocating library routine).  The first call on a device looks the buffer
  * up on that device (it must be the current device), so make that first

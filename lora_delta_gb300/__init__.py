@@ -76,12 +76,14 @@ def lora_scale(alpha: float, r: int, use_rslora: bool = False) -> float:
     return float(lib().lora_scale(float(alpha), int(r), int(bool(use_rslora))))
 
 
-def lora_workspace_size(n: int, max_loras: int) -> int:
-    return int(lib().lora_workspace_size(int(n), int(max_loras)))
+def lora_workspace_size(n: int, S: int, R: int, max_loras: int) -> int:
+    return int(lib().lora_workspace_size(int(n), int(S), int(R), int(max_loras)))
 
 
-def lora_moe_workspace_size(T: int, top_k: int, E: int, num_loras: int) -> int:
-    return int(lib().lora_moe_workspace_size(int(T), int(top_k), int(E), int(num_loras)))
+def lora_moe_workspace_size(T: int, top_k: int, E: int, num_loras: int, rank: int,
+                            shared_a: bool) -> int:
+    return int(lib().lora_moe_workspace_size(int(T), int(top_k), int(E), int(num_loras),
+                                             int(rank), int(bool(shared_a))))
 
 
 def _workspace(nbytes: int, workspace, device):
@@ -182,8 +184,8 @@ def lora_shrink(h, x, seq_slot, pool: LoraPool, scale_table=None, workspace=None
     _dev(x, "x", torch.bfloat16)
     _dev(seq_slot, "seq_slot", torch.int32)
     n, k_in = x.shape
-    ws, wsb = _workspace(lora_workspace_size(n, pool.max_loras) if n > 1024 else 0, workspace,
-                         x.device)
+    ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, pool.max_loras) if n > 1024
+                         else 0, workspace, x.device)
     _check("lora_shrink", lib().lora_shrink(
         _ptr(h), _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table), _ptr(scale_table),
         pool.S, pool.R, pool.max_loras, _ptr(ws), wsb, _ptr(err), _stream(stream)))
@@ -196,8 +198,8 @@ def lora_expand(out, h, seq_slot, pool: LoraPool, scale_table=None, offset_start
     _dev(h, "h", torch.float32)
     _dev(seq_slot, "seq_slot", torch.int32)
     n, ld_out = out.shape
-    ws, wsb = _workspace(lora_workspace_size(n, pool.max_loras) if n > 1024 else 0, workspace,
-                         out.device)
+    ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, pool.max_loras) if n > 1024
+                         else 0, workspace, out.device)
     w = _widths_arg(pool.widths)
     _check("lora_expand", lib().lora_expand(
         _ptr(out), ld_out, _ptr(h), _ptr(seq_slot), _ptr(pool.b_table), _ptr(scale_table), w,
@@ -216,8 +218,10 @@ def lora_delta_fused(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,
     if out.shape[0] != n:
         raise ValueError("out and x must have the same number of rows")
     st = pool.scale_table if scale_table is None else scale_table
-    ws, wsb = _workspace(lora_workspace_size(n, pool.max_loras) if n > 1024 else 0, workspace,
-                         x.device)
+    # batches of >= 256 rows get a workspace: they are clustered by slot, and
+    # slots with many rows take the tensor-core path
+    ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, pool.max_loras) if n >= 256
+                         else 0, workspace, x.device)
     w = _widths_arg(pool.widths)
     _check("lora_delta_fused", lib().lora_delta_fused(
         _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
@@ -261,7 +265,8 @@ def lora_moe_fc1_delta(out, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, s
     _dev(w_ptr_b, "w_ptr_b", torch.int64)
     T, H = x.shape
     top_k = topk_ids.shape[1]
-    ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras), workspace, x.device)
+    ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras, rank, shared_a),
+                         workspace, x.device)
     _check("lora_moe_fc1_delta", lib().lora_moe_fc1_delta(
         _ptr(out), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
         int(bool(shared_a)), _ptr(topk_ids), _ptr(lora_ids), T, top_k, int(E), H, int(I),

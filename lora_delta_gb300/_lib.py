@@ -23,14 +23,14 @@ SIGNATURES = {
     "lora_abi_version": (_i, []),
     "lora_scale": (_f, [_f, _i, _i]),
     "lora_pool_pack": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
-    "lora_workspace_size": (_sz, [_i, _i]),
+    "lora_workspace_size": (_sz, [_i, _i, _i, _i]),
     "lora_route": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp]),
     "lora_shrink": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "lora_expand": (_i, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz,
                          _vp, _vp]),
     "lora_delta_fused": (_i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                               _i, _vp, _sz, _vp, _vp]),
-    "lora_moe_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "lora_moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "lora_moe_fc1_delta": (_i, [_vp, _vp, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i, _i, _i, _i, _i,
                                 _i, _i, _f, _vp, _sz, _vp, _vp]),
     "lora_get_error": (_i, [_vp, _vp, _i, _vp]),

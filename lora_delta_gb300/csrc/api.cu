@@ -12,12 +12,13 @@
 #include "common.cuh"
 #include "lora_delta.h"
 #include "route.cuh"
+#include "sgmv.cuh"
 
 using namespace lora;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int kStageBytes = 64 * 1024;  // A rows of one shrink stage (both buffers)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -195,35 +196,151 @@ int launch_route(const KeyFn& kf, int n, int n_keys, int32_t* perm, int32_t* seg
   return cuda_status(cudaGetLastError());
 }
 
-// Workspace layout: perm [n] int32 | seg_start [n_keys + 2] int32.
-size_t ws_bytes_for(int n, int n_keys) {
-  return align256((size_t)(n > 0 ? n : 1) * 4) + align256((size_t)(n_keys + 2) * 4);
+// Workspace layout: perm [n] int32 | seg_start [n_keys + 2] int32 |
+// SGMV tiles [max_tiles] + their count | h of the tensor-core path [n, hs] fp32.
+int max_sgmv_tiles(int n, int n_keys) { return n / kTileRows + (n_keys < n ? n_keys : n) + 1; }
+
+struct Workspace {
+  int32_t* perm;
+  int32_t* seg;
+  SgmvTile* tiles;
+  int* n_tiles;
+  float* hbuf;
+};
+
+size_t ws_bytes_for(int n, int n_keys, int hs) {
+  const int nn = n > 0 ? n : 1;
+  size_t b = align256((size_t)nn * 4) + align256((size_t)(n_keys + 2) * 4);
+  b += align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16);
+  b += align256((size_t)nn * hs * 4);
+  return b;
 }
 
+Workspace carve(void* ws, int n, int n_keys) {
+  const int nn = n > 0 ? n : 1;
+  char* p = reinterpret_cast<char*>(ws);
+  Workspace w;
+  w.perm = reinterpret_cast<int32_t*>(p);
+  p += align256((size_t)nn * 4);
+  w.seg = reinterpret_cast<int32_t*>(p);
+  p += align256((size_t)(n_keys + 2) * 4);
+  w.n_tiles = reinterpret_cast<int*>(p);
+  w.tiles = reinterpret_cast<SgmvTile*>(p + 16);
+  p += align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16);
+  w.hbuf = reinterpret_cast<float*>(p);
+  return w;
+}
+
+// Rows per key from which the tensor-core (SGMV) path takes a key over from
+// the small-segment kernel; LORA_SGMV_MIN_ROWS overrides, read once.
+int sgmv_min_rows() {
+  static const int v = [] {
+    const int x = env_int("LORA_SGMV_MIN_ROWS", 64);
+    return x < 1 ? 1 : x;
+  }();
+  return v;
+}
+
+// Batches of at least this many rows are clustered by the routing kernel when
+// a workspace is given (and always above kInlineRowsMax).
+constexpr int kRouteMinRows = 256;
+
 // Common front half of the linear calls: row clustering (own scan or routing
-// kernel into the workspace).
-int prepare_rows(DeltaArgs& a, const int32_t* seq_slot, int n, int max_loras, void* workspace,
-                 size_t ws_bytes, uint32_t* err, cudaStream_t stream) {
+// kernel into the workspace).  Sets *routed when the routing kernel ran.
+int prepare_rows(DeltaArgs& a, const int32_t* seq_slot, int n, int max_loras, int hs,
+                 void* workspace, size_t ws_bytes, uint32_t* err, cudaStream_t stream,
+                 Workspace* wout) {
   a.seq_slot = seq_slot;
   a.n = n;
   a.n_keys = max_loras;
   a.err = err;
-  if (n <= kInlineRowsMax) {
+  const bool want_route = n > kInlineRowsMax || (workspace != nullptr && n >= kRouteMinRows);
+  if (!want_route) {
     a.perm = nullptr;
     a.seg_start = nullptr;
     a.row_cap = n;
     return LORA_OK;
   }
-  if (!workspace || ws_bytes < ws_bytes_for(n, max_loras)) return LORA_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < ws_bytes_for(n, max_loras, hs)) return LORA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
-  int32_t* perm = reinterpret_cast<int32_t*>(workspace);
-  int32_t* seg = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
-                                            align256((size_t)n * 4));
-  const int rc = launch_route(SlotKey{seq_slot, max_loras}, n, max_loras, perm, seg, err, stream);
+  const Workspace w = carve(workspace, n, max_loras);
+  const int rc = launch_route(SlotKey{seq_slot, max_loras}, n, max_loras, w.perm, w.seg, err, stream);
   if (rc) return rc;
-  a.perm = perm;
-  a.seg_start = seg;
+  a.perm = w.perm;
+  a.seg_start = w.seg;
   a.row_cap = 0;
+  if (wout) *wout = w;
+  return LORA_OK;
+}
+
+// Launch of the tensor-core path for the keys with >= min_rows rows.
+template <class Tables>
+int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_keys,
+                int min_rows, cudaStream_t stream) {
+  SgmvArgs s = {};
+  s.out = d.out;
+  s.ld_out = d.ld_out;
+  s.x = d.x;
+  s.ld_x = d.ld_x;
+  s.k_in = d.k_in;
+  s.perm = w.perm;
+  s.tiles = w.tiles;
+  s.n_tiles = w.n_tiles;
+  s.hbuf = w.hbuf;
+  s.hs = (d.sr_max + 15) / 16 * 16;
+  s.R = d.R;
+  s.sl = d.sl;
+  for (int j = 0; j <= kMaxSlices; ++j) s.rel[j] = d.rel[j];
+  int nch = 0;
+  for (int j = 0; j < kMaxSlices; ++j) {
+    s.chunk0[j] = nch;
+    if (j < d.sl.S) nch += (d.sl.width[j] + kExpandCols - 1) / kExpandCols;
+  }
+  s.chunk0[kMaxSlices] = nch;
+  s.add_inputs = d.add_inputs;
+  s.err = d.err;
+  const int max_tiles = max_sgmv_tiles(d.n, n_keys);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 1 : 0;
+  // tile list
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sgmv_tiles_kernel, (const int32_t*)d.seg_start, n_keys,
+                                     min_rows, w.tiles, w.n_tiles, max_tiles);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  // shrink
+  {
+    auto kernel = sgmv_shrink_kernel<Tables>;
+    const int smem = sgmv_shrink_smem(d.sr_max);
+    if ((e = prepare_kernel(kernel, smem, false)) != cudaSuccess) return LORA_ERR_CUDA;
+    cfg.gridDim = dim3((unsigned)max_tiles);
+    cfg.blockDim = dim3(kSgmvThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    if ((e = cudaLaunchKernelEx(&cfg, kernel, s, tb)) != cudaSuccess) return LORA_ERR_CUDA;
+  }
+  // expand
+  {
+    const int smem = sgmv_expand_smem(d.R);
+    cfg.gridDim = dim3((unsigned)((int64_t)max_tiles * nch));
+    cfg.blockDim = dim3(kSgmvThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    if (d.R <= 64) {
+      auto kernel = sgmv_expand_kernel<64, Tables>;
+      if ((e = prepare_kernel(kernel, smem, false)) != cudaSuccess) return LORA_ERR_CUDA;
+      e = cudaLaunchKernelEx(&cfg, kernel, s, tb, nch);
+    } else {
+      auto kernel = sgmv_expand_kernel<128, Tables>;
+      if ((e = prepare_kernel(kernel, smem, false)) != cudaSuccess) return LORA_ERR_CUDA;
+      e = cudaLaunchKernelEx(&cfg, kernel, s, tb, nch);
+    }
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+  }
   return LORA_OK;
 }
 
@@ -294,9 +411,9 @@ int lora_pool_pack(void* a_slot, void* b_slot, const void* a_r, const void* b_r,
   return cuda_status(cudaGetLastError());
 }
 
-size_t lora_workspace_size(int n, int max_loras) {
-  if (n < 0 || max_loras < 1) return 0;
-  return ws_bytes_for(n, max_loras);
+size_t lora_workspace_size(int n, int S, int R, int max_loras) {
+  if (n < 0 || max_loras < 1 || S < 1 || R < 1) return 0;
+  return ws_bytes_for(n, max_loras, (S * R + 15) / 16 * 16);
 }
 
 int lora_route(int32_t* perm, int32_t* seg_start, const int32_t* seq_slot, int n, int max_loras,
@@ -328,8 +445,8 @@ int lora_shrink(float* h, const void* x, int n, int k_in, const int32_t* seq_slo
   a.R = R;
   a.sl.S = S;
   a.sr_max = S * R;
-  rc = prepare_rows(a, seq_slot, n, max_loras, workspace, ws_bytes, err_word,
-                    (cudaStream_t)stream);
+  rc = prepare_rows(a, seq_slot, n, max_loras, (S * R + 15) / 16 * 16, workspace, ws_bytes,
+                    err_word, (cudaStream_t)stream, nullptr);
   if (rc) return rc;
   plan_tiles(a, k_in, 8, a.sr_max, kModeShrink);
   LinearTables tb{a_table, nullptr, scale_table, max_loras};
@@ -357,8 +474,8 @@ int lora_expand(void* out, int64_t ld_out, const float* h, const int32_t* seq_sl
   a.R = R;
   a.add_inputs = add_inputs ? 1 : 0;
   a.sr_max = S * R;
-  rc = prepare_rows(a, seq_slot, n, max_loras, workspace, ws_bytes, err_word,
-                    (cudaStream_t)stream);
+  rc = prepare_rows(a, seq_slot, n, max_loras, (S * R + 15) / 16 * 16, workspace, ws_bytes,
+                    err_word, (cudaStream_t)stream, nullptr);
   if (rc) return rc;
   plan_tiles(a, 8, a.sl.n_cols, a.sr_max, kModeExpand);
   LinearTables tb{nullptr, b_table, scale_table, max_loras};
@@ -389,17 +506,25 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
   a.R = R;
   a.add_inputs = add_inputs ? 1 : 0;
   a.sr_max = S * R;
-  rc = prepare_rows(a, seq_slot, n, max_loras, workspace, ws_bytes, err_word,
-                    (cudaStream_t)stream);
+  Workspace w = {};
+  rc = prepare_rows(a, seq_slot, n, max_loras, (S * R + 15) / 16 * 16, workspace, ws_bytes,
+                    err_word, (cudaStream_t)stream, &w);
   if (rc) return rc;
   plan_tiles(a, k_in, a.sl.n_cols, a.sr_max, kModeFused);
   LinearTables tb{a_table, b_table, scale_table, max_loras};
-  return launch_delta<kModeFused>(a, tb, max_loras, (cudaStream_t)stream);
+  // keys with many rows go to the tensor-core path, the others stay here
+  const bool sgmv = a.perm != nullptr && a.sr_max <= kSgmvMaxSR;
+  const int thr = sgmv_min_rows();
+  if (sgmv) a.max_rows = thr;
+  rc = launch_delta<kModeFused>(a, tb, max_loras, (cudaStream_t)stream);
+  if (rc || !sgmv) return rc;
+  return launch_sgmv(a, tb, w, max_loras, thr, (cudaStream_t)stream);
 }
 
-size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras) {
-  if (T < 0 || top_k < 0 || E < 1 || num_loras < 1) return 0;
-  return ws_bytes_for(T * top_k, E * num_loras);
+size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras, int rank, int shared_a) {
+  if (T < 0 || top_k < 0 || E < 1 || num_loras < 1 || rank < 1) return 0;
+  const int hs = ((shared_a ? 1 : 2) * rank + 15) / 16 * 16;
+  return ws_bytes_for(T * top_k, E * num_loras, hs);
 }
 
 int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t stride_a,
@@ -421,12 +546,13 @@ int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t
   if (H % 8 || I % 8 || stride_a % 8 || stride_b % 8 || !aligned16(out) || !aligned16(x))
     return LORA_ERR_ALIGN;
   const int n = (int)n64, n_keys = E * num_loras;
-  if (!workspace || ws_bytes < ws_bytes_for(n, n_keys)) return LORA_ERR_WORKSPACE;
+  const int hs = (n_slices * rank + 15) / 16 * 16;
+  if (!workspace || ws_bytes < ws_bytes_for(n, n_keys, hs)) return LORA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
   cudaStream_t s = (cudaStream_t)stream;
-  int32_t* perm = reinterpret_cast<int32_t*>(workspace);
-  int32_t* seg =
-      reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) + align256((size_t)n * 4));
+  const Workspace w = carve(workspace, n, n_keys);
+  int32_t* perm = w.perm;
+  int32_t* seg = w.seg;
   rc = launch_route(MoeKey{topk_ids, lora_ids, top_k, E, num_loras}, n, n_keys, perm, seg,
                     err_word, s);
   if (rc) return rc;

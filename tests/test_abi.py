@@ -49,8 +49,8 @@ def test_host_only_calls(library):
     assert ld.lora_scale(32.0, 16) == 2.0
     assert ld.lora_scale(32.0, 16, use_rslora=True) == 8.0
     assert ld.lora_scale(16.0, 0) == 0.0
-    assert ld.lora_workspace_size(8192, 8) >= 8192 * 4 + 10 * 4
-    assert ld.lora_moe_workspace_size(2048, 8, 64, 8) >= 2048 * 8 * 4
+    assert ld.lora_workspace_size(8192, 2, 32, 8) >= 8192 * 4 + 10 * 4 + 8192 * 64 * 4
+    assert ld.lora_moe_workspace_size(2048, 8, 64, 8, 16, False) >= 2048 * 8 * 4
 
 
 def test_host_validation_without_a_gpu(library):

@@ -308,3 +308,64 @@ def test_moe_bad_ids(ld, di, oracle):
     assert err == ref_err == (2 | 4)
     assert_close(got, ref, "moe bad ids")
     assert not got[0].any() and not got[1].any() and not got[2, 1].any()
+
+
+# ------------------------------------------------- tensor-core (SGMV) path --
+
+def _hot_slots_case(seed, n, k_in, widths, R, ranks, hot=(0, 1), **kw):
+    """Two hot slots (well over the tensor-core threshold, ragged 128-row tiles)
+    and a sprinkle of rows on the other slots (small-segment kernel)."""
+    rng = np.random.default_rng(seed + 500)
+    L = len(ranks)
+    seq = rng.integers(0, L, size=n).astype(np.int32)
+    hot_mask = rng.random(n) < 0.8
+    seq[hot_mask] = rng.choice(np.array(hot), size=int(hot_mask.sum()))
+    seq[rng.random(n) < 0.05] = -1
+    return inputs.linear_case(seed, n=n, k_in=k_in, widths=widths, max_loras=L, max_rank=R,
+                              ranks=ranks, alpha=float(R), seq_slot=seq, **kw)
+
+
+@pytest.mark.parametrize("k_in,widths,R,ranks", [
+    (200, (136, 24), 8, [8, 4, 8, 2]),            # k tail of 8, half column tiles, R < 16
+    (328, (64, 40, 24), 24, [24, 16, 24, 8]),     # R not a power of two, three slices
+    (256, (96, 160), 128, [128, 64, 96, 128]),    # largest rank: two 64-wide k-blocks
+])
+def test_sgmv_edge_shapes(ld, di, oracle, k_in, widths, R, ranks):
+    case = _hot_slots_case(3 + R, 1500, k_in, widths, R, ranks)
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
+def test_sgmv_inactive_slice_offsets_and_no_add(ld, di, oracle):
+    adapted = [[True, False], [True, True], [False, True], [True, True]]
+    case = _hot_slots_case(21, 1300, 512, (128, 64), 16, [16, 16, 8, 16], hot=(0, 2),
+                           adapted=adapted, offset_start=24, ld_out=240)
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+    got2, err2, _ = run_fused(ld, di, case, add_inputs=False)
+    check_linear(oracle, case, got2, err2, add_inputs=False)
+
+
+def test_sgmv_and_small_path_agree_on_a_hot_slot(ld, di, oracle):
+    """The same batch through the tensor-core path (workspace given) and the
+    small-segment kernel alone (no workspace, n <= 1024) agree within tolerance."""
+    case = _hot_slots_case(33, 1000, 384, (256,), 32, [32, 16, 32], hot=(0,))
+    d = di.linear_to_device(case)
+    a = d.out0.clone()
+    ws = torch.empty(ld.lora_workspace_size(case.n, 1, 32, 3), dtype=torch.uint8, device="cuda")
+    ld.lora_delta_fused(a, d.x, d.seq_slot, d.pool, workspace=ws)
+    b = d.out0.clone()
+    L = ld.lib()
+    import ctypes
+    w = (ctypes.c_int32 * 1)(256)
+    rc = L.lora_delta_fused(ctypes.c_void_p(b.data_ptr()), 256, ctypes.c_void_p(d.x.data_ptr()),
+                            case.n, 384, ctypes.c_void_p(d.seq_slot.data_ptr()),
+                            ctypes.c_void_p(d.pool.a_table.data_ptr()),
+                            ctypes.c_void_p(d.pool.b_table.data_ptr()),
+                            ctypes.c_void_p(d.pool.scale_table.data_ptr()), w, 1, 32, 3, 0, 1,
+                            None, 0, None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert_close(di.bits(a), di.bits(b), "tensor-core vs small-segment path")
+    ref, _ = oracle_delta(oracle, case)
+    assert_close(di.bits(a), ref, "tensor-core path vs oracle")
