@@ -367,14 +367,16 @@ def cpu_baseline(case, budget_s: float = 10.0):
                       f"({dt:.1f} s, OpenMP over rows, {cores} threads)"}
 
 
-def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src):
+def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src, only=None, reps=5,
+                    warm=2):
     """The other workloads of the path, each timed on its own (not the headline)."""
     import numpy as np
     import torch
     res = {}
     stream = torch.cuda.Stream(device)
+    rep_default, warm_default = reps, warm
 
-    def timed(fn, reps=5, warm=2):
+    def timed(fn, reps=rep_default, warm=warm_default):
         with torch.cuda.stream(stream):
             for _ in range(warm):
                 fn()
@@ -388,6 +390,18 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src):
         return e0.elapsed_time(e1) / reps
 
     # prefill SGMV gate_up (8192 rows)
+    if only in (None, "prefill"):
+        _prefill(ld, di, inputs, device, hbm_peak, bf16_peak, timed, res)
+    if only in (None, "skewed"):
+        _skewed(ld, di, inputs, device, hbm_peak, timed, res)
+    if only in (None, "moe"):
+        _moe(ld, di, inputs, device, hbm_peak, timed, res)
+    res["peak_source"] = peak_src
+    return res
+
+
+def _prefill(ld, di, inputs, device, hbm_peak, bf16_peak, timed, res):
+    import torch
     case = inputs.prefill_gate_up_case()
     d = di.linear_to_device(case, device)
     ws = torch.empty(ld.lora_workspace_size(case.n, len(case.widths), case.max_rank,
@@ -402,23 +416,32 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src):
                               "tensor_frac": round(tfs / bf16_peak, 5),
                               "attainable_TFLOP_per_s": round(attain, 1),
                               "roofline_frac": round(tfs / attain, 4),
-                              "launches_per_call": 2}
+                              "launches_per_call": 5}
     del d, ws
     torch.cuda.empty_cache()
 
+
+def _skewed(ld, di, inputs, device, hbm_peak, timed, res):
+    import torch
     # skewed many-adapter decode: both projections per step
     c1, c2 = inputs.skewed_case(0), inputs.skewed_case(1)
     d1, d2 = di.linear_to_device(c1, device), di.linear_to_device(c2, device)
-    ms = timed(lambda: (ld.lora_delta_fused(d1.out0, d1.x, d1.seq_slot, d1.pool),
-                        ld.lora_delta_fused(d2.out0, d2.x, d2.seq_slot, d2.pool)))
+    ws = torch.empty(max(ld.lora_workspace_size(c.n, 1, c.max_rank, c.max_loras) for c in (c1, c2)),
+                     dtype=torch.uint8, device=device)
+    ms = timed(lambda: (ld.lora_delta_fused(d1.out0, d1.x, d1.seq_slot, d1.pool, workspace=ws),
+                        ld.lora_delta_fused(d2.out0, d2.x, d2.seq_slot, d2.pool, workspace=ws)))
     ab = algorithmic_bytes(c1) + algorithmic_bytes(c2)
     res["skewed_decode"] = {"rows_per_s": round(c1.n / (ms / 1e3), 1), "ms": round(ms, 4),
                             "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
                             "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4),
-                            "launches_per_call": 2}
-    del d1, d2
+                            "launches_per_call": 10}
+    del d1, d2, ws
     torch.cuda.empty_cache()
 
+
+def _moe(ld, di, inputs, device, hbm_peak, timed, res):
+    import numpy as np
+    import torch
     # MoE FC1 (regular and shared-A / fused-B)
     for shared in (False, True):
         mc = inputs.moe_case(shared_a=shared)
@@ -443,8 +466,6 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src):
             "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 3}
         del dm, out, ws
         torch.cuda.empty_cache()
-    res["peak_source"] = peak_src
-    return res
 
 
 # ---------------------------------------------------------- reference arm --
@@ -497,6 +518,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads (prefill, skewed, MoE)")
+    ap.add_argument("--only", choices=["prefill", "skewed", "moe"], default=None,
+                    help="time one of the other workloads alone and print its numbers "
+                         "(for profiling captures; not the benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -504,6 +528,17 @@ def main():
     rank, world = ldist.init()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.only:
+        import torch
+        import lora_delta_gb300 as ld
+        from lora_delta_gb300 import device_inputs as di
+        from lora_delta_gb300 import inputs
+        device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(device)
+        hbm_peak, bf16_peak, _, peak_src = load_peaks()
+        res = other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src,
+                              only=args.only, reps=args.steps, warm=args.warmup)
+        print(json.dumps(res), flush=True)
     else:
         run_ours(args, rank, world)
 

@@ -61,6 +61,7 @@ typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
 #define LORA_DEV_ERR_LORA 4u    /* MoE adapter id >= num_loras: pair written as zeros  */
 #define LORA_DEV_ERR_TIMEOUT 8u /* a bounded wait inside a kernel gave up              */
 #define LORA_DEV_ERR_ALIGN 16u  /* a table address is not 16-byte aligned: slice skipped */
+#define LORA_DEV_ERR_INTERNAL 32u /* a launch invariant of the library failed (a bug)   */
 
 /* Human-readable name of a status code (static string). */
 const char *lora_status_string(int status);
@@ -110,6 +111,13 @@ int lora_pool_pack(void *a_slot, void *b_slot, const void *a_r, const void *b_r,
  * workspace each kernel clusters its own rows.
  */
 size_t lora_workspace_size(int n, int S, int R, int max_loras);
+
+/*
+ * lora_workspace_min_size -- the smallest workspace the linear calls accept
+ * for these sizes.  A workspace between this and lora_workspace_size works;
+ * the tensor-core path then splits k_in over fewer CTAs.
+ */
+size_t lora_workspace_min_size(int n, int S, int R, int max_loras);
 
 /*
  * lora_route -- the routing step on its own ([punica] prefill_metadata):
@@ -204,8 +212,8 @@ int lora_moe_fc1_delta(void *out, const void *x, const int64_t *w_ptr_a, int64_t
  * Same arguments and results as lora_delta_fused minus the workspace: the
  * scratch comes from a fixed buffer inside the library of
  * lora_noalloc_scratch_bytes() bytes (4 MiB), held on every GPU that loads
- * the library until the process exits.  A call whose workspace need
- * (lora_workspace_size(n, S, R, max_loras)) exceeds it returns LORA_ERR_TOO_LARGE
+ * the library until the process exits.  A call whose smallest workspace
+ * (lora_workspace_min_size(n, S, R, max_loras)) exceeds it returns LORA_ERR_TOO_LARGE
  * and enqueues nothing.  The call never allocates (no cudaMalloc, no
  * allocating library routine).  The first call on a device looks the buffer
  * up on that device (it must be the current device), so make that first

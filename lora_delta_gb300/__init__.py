@@ -22,7 +22,7 @@ from ._lib import LibraryMissing, lib, status_string
 
 __all__ = [
     "LoraError", "LibraryMissing", "LoraPool", "lora_scale", "lora_pool_pack",
-    "lora_workspace_size", "lora_route", "lora_shrink", "lora_expand", "lora_delta_fused",
+    "lora_workspace_size", "lora_workspace_min_size", "lora_route", "lora_shrink", "lora_expand", "lora_delta_fused",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_get_error", "new_error_word",
     "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes",
 ]
@@ -78,6 +78,10 @@ def lora_scale(alpha: float, r: int, use_rslora: bool = False) -> float:
 
 def lora_workspace_size(n: int, S: int, R: int, max_loras: int) -> int:
     return int(lib().lora_workspace_size(int(n), int(S), int(R), int(max_loras)))
+
+
+def lora_workspace_min_size(n: int, S: int, R: int, max_loras: int) -> int:
+    return int(lib().lora_workspace_min_size(int(n), int(S), int(R), int(max_loras)))
 
 
 def lora_moe_workspace_size(T: int, top_k: int, E: int, num_loras: int, rank: int,

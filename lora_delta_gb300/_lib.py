@@ -24,6 +24,7 @@ SIGNATURES = {
     "lora_scale": (_f, [_f, _i, _i]),
     "lora_pool_pack": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "lora_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "lora_workspace_min_size": (_sz, [_i, _i, _i, _i]),
     "lora_route": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp]),
     "lora_shrink": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "lora_expand": (_i, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz,

@@ -206,14 +206,35 @@ struct Workspace {
   SgmvTile* tiles;
   int* n_tiles;
   float* hbuf;
+  size_t bytes;  // size of the whole buffer
 };
 
-size_t ws_bytes_for(int n, int n_keys, int hs) {
+constexpr int kMaxKSplit = 8;  // planes of the SGMV shrink's partial h
+
+// Bytes before the h planes, and bytes of one plane.
+size_t ws_head_bytes(int n, int n_keys) {
   const int nn = n > 0 ? n : 1;
-  size_t b = align256((size_t)nn * 4) + align256((size_t)(n_keys + 2) * 4);
-  b += align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16);
-  b += align256((size_t)nn * hs * 4);
-  return b;
+  return align256((size_t)nn * 4) + align256((size_t)(n_keys + 2) * 4) +
+         align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16);
+}
+size_t ws_plane_bytes(int n, int hs) { return align256((size_t)(n > 0 ? n : 1) * hs * 4); }
+
+// Minimum workspace: one plane; the size query asks for kMaxKSplit planes so
+// the tensor-core shrink can split k across more CTAs.
+size_t ws_bytes_for(int n, int n_keys, int hs, int planes = 1) {
+  return ws_head_bytes(n, n_keys) + (size_t)planes * ws_plane_bytes(n, hs);
+}
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = v > 0 ? v : 148;
+  }
+  return cache[dev];
 }
 
 Workspace carve(void* ws, int n, int n_keys) {
@@ -228,6 +249,7 @@ Workspace carve(void* ws, int n, int n_keys) {
   w.tiles = reinterpret_cast<SgmvTile*>(p + 16);
   p += align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16);
   w.hbuf = reinterpret_cast<float*>(p);
+  w.bytes = 0;
   return w;
 }
 
@@ -269,7 +291,10 @@ int prepare_rows(DeltaArgs& a, const int32_t* seq_slot, int n, int max_loras, in
   a.perm = w.perm;
   a.seg_start = w.seg;
   a.row_cap = 0;
-  if (wout) *wout = w;
+  if (wout) {
+    *wout = w;
+    wout->bytes = ws_bytes;
+  }
   return LORA_OK;
 }
 
@@ -288,6 +313,21 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   s.n_tiles = w.n_tiles;
   s.hbuf = w.hbuf;
   s.hs = (d.sr_max + 15) / 16 * 16;
+  const int max_tiles = max_sgmv_tiles(d.n, n_keys);
+  {
+    // split k so that about two CTAs per SM run the shrink, within the planes
+    // the workspace holds
+    const int nkb = (d.k_in + 63) / 64;
+    int ks = (2 * sm_count() + max_tiles - 1) / max_tiles;
+    if (ks > kMaxKSplit) ks = kMaxKSplit;
+    if (ks > nkb) ks = nkb;
+    const size_t head = ws_head_bytes(d.n, n_keys), plane = ws_plane_bytes(d.n, s.hs);
+    const int fit = w.bytes > head ? (int)((w.bytes - head) / plane) : 0;
+    if (ks > fit) ks = fit;
+    if (ks < 1) ks = 1;
+    s.ksplit = ks;
+    s.plane = (int64_t)(plane / 4);
+  }
   s.R = d.R;
   s.sl = d.sl;
   for (int j = 0; j <= kMaxSlices; ++j) s.rel[j] = d.rel[j];
@@ -299,7 +339,6 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   s.chunk0[kMaxSlices] = nch;
   s.add_inputs = d.add_inputs;
   s.err = d.err;
-  const int max_tiles = max_sgmv_tiles(d.n, n_keys);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -319,16 +358,23 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
     auto kernel = sgmv_shrink_kernel<Tables>;
     const int smem = sgmv_shrink_smem(d.sr_max);
     if ((e = prepare_kernel(kernel, smem, false)) != cudaSuccess) return LORA_ERR_CUDA;
-    cfg.gridDim = dim3((unsigned)max_tiles);
+    cfg.gridDim = dim3((unsigned)(max_tiles * s.ksplit));
     cfg.blockDim = dim3(kSgmvThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     if ((e = cudaLaunchKernelEx(&cfg, kernel, s, tb)) != cudaSuccess) return LORA_ERR_CUDA;
   }
-  // expand
+  // expand: persistent, one CTA per SM
   {
     const int smem = sgmv_expand_smem(d.R);
-    cfg.gridDim = dim3((unsigned)((int64_t)max_tiles * nch));
-    cfg.blockDim = dim3(kSgmvThreads);
+    // one CTA per SM, more if needed so that no CTA spans more than
+    // kExpandMaxTiles tiles (<= kExpandMaxTiles - 2 tiles' worth of items each)
+    const int64_t items = (int64_t)max_tiles * nch;
+    int64_t grid = sm_count();
+    const int64_t need = (max_tiles + (kExpandMaxTiles - 2) - 1) / (kExpandMaxTiles - 2);
+    if (grid < need) grid = need;
+    if (grid > items) grid = items;
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kExpandThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     if (d.R <= 64) {
       auto kernel = sgmv_expand_kernel<64, Tables>;
@@ -413,7 +459,12 @@ int lora_pool_pack(void* a_slot, void* b_slot, const void* a_r, const void* b_r,
 
 size_t lora_workspace_size(int n, int S, int R, int max_loras) {
   if (n < 0 || max_loras < 1 || S < 1 || R < 1) return 0;
-  return ws_bytes_for(n, max_loras, (S * R + 15) / 16 * 16);
+  return ws_bytes_for(n, max_loras, (S * R + 15) / 16 * 16, kMaxKSplit);
+}
+
+size_t lora_workspace_min_size(int n, int S, int R, int max_loras) {
+  if (n < 0 || max_loras < 1 || S < 1 || R < 1) return 0;
+  return ws_bytes_for(n, max_loras, (S * R + 15) / 16 * 16, 1);
 }
 
 int lora_route(int32_t* perm, int32_t* seg_start, const int32_t* seq_slot, int n, int max_loras,
@@ -524,7 +575,7 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
 size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras, int rank, int shared_a) {
   if (T < 0 || top_k < 0 || E < 1 || num_loras < 1 || rank < 1) return 0;
   const int hs = ((shared_a ? 1 : 2) * rank + 15) / 16 * 16;
-  return ws_bytes_for(T * top_k, E * num_loras, hs);
+  return ws_bytes_for(T * top_k, E * num_loras, hs, kMaxKSplit);
 }
 
 int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t stride_a,

@@ -62,7 +62,7 @@ int lora_delta_fused_noalloc(void* out, int64_t ld_out, const void* x, int n, in
                              int offset_start, int add_inputs, uint32_t* err_word,
                              lora_stream_t stream) {
   if (n < 0 || max_loras < 1 || S < 1 || R < 1) return LORA_ERR_ARG;
-  const size_t need = lora_workspace_size(n, S, R, max_loras);
+  const size_t need = lora_workspace_min_size(n, S, R, max_loras);
   if (need > kNoAllocScratchBytes) return LORA_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);

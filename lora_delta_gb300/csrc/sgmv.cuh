@@ -6,16 +6,18 @@
 //
 // The rows of a key are taken in the routing kernel's stable order and cut
 // into tiles of 128 rows (the last one ragged).  Two kernels:
-//   * shrink: one CTA per tile computes h[tile rows, active (slice, rank)
-//     pairs] = x[rows] A^T over all of k_in: 64-wide k-blocks of the gathered
-//     x rows and of the key's A rows are staged by cp.async into 128-byte
-//     swizzled shared-memory tiles (4-stage ring), one thread issues the
-//     M=128 MMAs, and h goes to the workspace in fp32;
-//   * expand: one CTA per (tile, 128-column chunk of one slice) multiplies the
-//     tile's h -- split into a bf16 (hi, lo) pair so the rank contraction keeps
-//     ~fp32 accuracy -- by the chunk's B rows (both 128-byte swizzled tiles),
-//     and folds scale * d into out in place, one rounding; the out segments
-//     are staged in shared memory while the MMAs run.
+//   * shrink: CTA (tile, k-split) computes the tile's partial h[rows, active
+//     (slice, rank) pairs] = x[rows] A^T over its share of k_in: 64-wide
+//     k-blocks of the gathered x rows and of the key's A rows are staged by
+//     cp.async into 128-byte swizzled shared-memory tiles (4-stage ring), one
+//     thread issues the M=128 MMAs, and the fp32 partial goes to the split's
+//     own plane of the workspace (summed later in a fixed order: deterministic);
+//   * expand: a persistent grid walks (tile, 128-column chunk of one slice)
+//     items.  The tile's h -- the planes summed, then split into a bf16 (hi,
+//     lo) pair so the rank contraction keeps ~fp32 accuracy -- is multiplied by
+//     the chunk's B rows (both 128-byte swizzled tiles) and scale * d is folded
+//     into out in place, one rounding; the next item's B chunk and out
+//     segments stream into shared memory while the current one computes.
 // Every wait on an mbarrier is bounded; on a time-out the CTA records
 // LORA_DEV_ERR_TIMEOUT, skips its writes and still releases its TMEM.
 #pragma once
@@ -82,8 +84,10 @@ struct SgmvArgs {
   const int32_t* perm;
   const SgmvTile* tiles;
   const int* n_tiles;
-  float* hbuf;  // [sorted rows, hs] fp32
-  int hs;       // row stride of hbuf (S * R rounded up to 16)
+  float* hbuf;    // [ksplit planes][sorted rows, hs] fp32 partial sums of h
+  int64_t plane;  // elements per plane
+  int ksplit;     // k-splits of the shrink (planes to sum)
+  int hs;         // row stride of hbuf (S * R rounded up to 16)
   int R;
   Slices sl;
   int rel[kMaxSlices + 1];
@@ -99,6 +103,10 @@ __device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gsr
 }
 
 // ---------------------------------------------------------------- shrink --
+// CTA (tile, split): the tile's 128 rows against the key's A rows over the
+// split's share of the 64-wide k-blocks; the fp32 partial goes to plane
+// `split` of hbuf (the expand sums the planes in order, so the result does not
+// depend on scheduling).
 template <class Tables>
 __global__ void __launch_bounds__(kSgmvThreads)
     sgmv_shrink_kernel(const SgmvArgs a, const Tables tb) {
@@ -107,8 +115,10 @@ __global__ void __launch_bounds__(kSgmvThreads)
   __shared__ uint32_t taddr_s;
   __shared__ __align__(8) uint64_t mma_bar[kShrinkStages];
   __shared__ __align__(8) uint64_t done_bar;
+  __shared__ const __nv_bfloat16* xrow_s[kTileRows];
+  __shared__ const __nv_bfloat16* arow_s[kSgmvMaxSR];
   cudaGridDependencySynchronize();
-  const int tile_id = blockIdx.x;
+  const int tile_id = blockIdx.x / a.ksplit, split = blockIdx.x - tile_id * a.ksplit;
   if (tile_id >= *a.n_tiles) return;
   const SgmvTile tile = a.tiles[tile_id];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -120,43 +130,52 @@ __global__ void __launch_bounds__(kSgmvThreads)
     mbar_init(&done_bar, 1);
     fence_barrier_init();
   }
+  for (int r = tid; r < kTileRows; r += kSgmvThreads)
+    xrow_s[r] = r < tile.rows ? a.x + tb.x_row(a.perm[tile.pos0 + r]) * a.ld_x : nullptr;
   __syncthreads();
   const int R = a.R;
   const int SRa = v.nact * R;
   if (SRa == 0) return;
   const int N = (SRa + 15) / 16 * 16;
+  for (int t = tid; t < N; t += kSgmvThreads) {
+    const __nv_bfloat16* p = nullptr;
+    if (t < SRa) {
+      const int jj = t / R, q = t - jj * R;
+      p = v.A[v.act_slice[jj]] + (size_t)q * a.k_in;
+    }
+    arow_s[t] = p;
+  }
   uint32_t ncols = 32;
   while ((int)ncols < N) ncols <<= 1;
   if (warp == 0) tc::tmem_alloc(&taddr_s, ncols);
 
   const int xbytes = kTileRows * 128, abytes = N * 128;
   const int stage_bytes = xbytes + abytes;  // multiple of 1024
-  const int nkb = (a.k_in + 63) / 64;
+  const int nkb_all = (a.k_in + 63) / 64;
+  const int kb_begin = (int)((int64_t)nkb_all * split / a.ksplit);
+  const int kb_end = (int)((int64_t)nkb_all * (split + 1) / a.ksplit);
+  const int nkb = kb_end - kb_begin;
+  __syncthreads();  // row pointers visible
 
   // one 64-wide k-block of the gathered x rows and of the A rows, zero-filled
   // past the tile's rows, the key's pairs and k_in
   auto load_block = [&](int kb, int s) {
     uint8_t* xs = smem + (size_t)s * stage_bytes;
     uint8_t* as = xs + xbytes;
-    const int kbase = kb * 64;
+    const int kbase = (kb_begin + kb) * 64;
     for (int i = tid; i < (kTileRows + N) * 8; i += kSgmvThreads) {
       const int r = i >> 3, c = i & 7;
       const int k = kbase + c * 8;
       const bool kin = k < a.k_in;
       if (r < kTileRows) {
-        const bool ok = kin && r < tile.rows;
-        const __nv_bfloat16* src =
-            ok ? a.x + tb.x_row(a.perm[tile.pos0 + r]) * a.ld_x + k : a.x;
-        cp_async16_zfill(xs + tc::sw128_offset(r, c * 8), src, ok);
+        const __nv_bfloat16* row = xrow_s[r];
+        const bool ok = kin && row != nullptr;
+        cp_async16_zfill(xs + tc::sw128_offset(r, c * 8), ok ? row + k : a.x, ok);
       } else {
         const int t = r - kTileRows;
-        const bool ok = kin && t < SRa;
-        const __nv_bfloat16* src = a.x;
-        if (ok) {
-          const int jj = t / R, q = t - jj * R;
-          src = v.A[v.act_slice[jj]] + (size_t)q * a.k_in + k;
-        }
-        cp_async16_zfill(as + tc::sw128_offset(t, c * 8), src, ok);
+        const __nv_bfloat16* row = arow_s[t];
+        const bool ok = kin && row != nullptr;
+        cp_async16_zfill(as + tc::sw128_offset(t, c * 8), ok ? row + k : a.x, ok);
       }
     }
   };
@@ -203,10 +222,10 @@ __global__ void __launch_bounds__(kSgmvThreads)
   tc::fence_after_sync();
   const bool all_ok = __syncthreads_and(ok);
   if (!all_ok && tid == 0) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
-  // epilogue: TMEM row r -> hbuf[pos0 + r][0 .. SRa)
+  // epilogue: TMEM row r -> plane `split` of hbuf, row pos0 + r, columns [0, SRa)
   if (all_ok) {
     const int r = warp * 32 + lane;
-    float* dst = a.hbuf + (size_t)(tile.pos0 + r) * a.hs;
+    float* dst = a.hbuf + (size_t)split * a.plane + (size_t)(tile.pos0 + r) * a.hs;
     for (int c = 0; c < N; c += 16) {
       float vals[16];
       tc::tmem_ld16(taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, vals);
@@ -225,147 +244,271 @@ __global__ void __launch_bounds__(kSgmvThreads)
 }
 
 // ---------------------------------------------------------------- expand --
+// Persistent: CTA b walks a contiguous run of work items (tile, slice chunk
+// of 128 columns), tile-major.  h of a (tile, slice) is summed over the
+// shrink's planes and split into bf16 (hi, lo) once per run; the next item's
+// B chunk and out segments stream in (cp.async) while the current item's
+// MMAs and epilogue run.
+constexpr int kExpandThreads = 256;
+
+template <int RMAX>
+struct ExpandSmem {
+  static constexpr int KB = (RMAX + 63) / 64;
+  static constexpr int kNBuf = KB == 1 ? 3 : 2;       // copy buffers (copies run kNBuf-1 ahead)
+  static constexpr int kOStride = kExpandCols + 8;    // staged out row (elements)
+  static constexpr int kH = KB * kTileRows * 128;     // one of hi / lo
+  static constexpr int kB = KB * kExpandCols * 128;   // one B buffer
+  static constexpr int kO = kTileRows * kOStride * 2; // one out buffer
+  static constexpr int kTotal = 2 * kH + kNBuf * (kB + kO) + 1024;
+};
+
+constexpr int kExpandMaxTiles = 8;  // tiles one expand CTA may span (the grid ensures it)
+
 template <int RMAX, class Tables>
-__global__ void __launch_bounds__(kSgmvThreads)
+__global__ void __launch_bounds__(kExpandThreads, 1)
     sgmv_expand_kernel(const SgmvArgs a, const Tables tb, int n_chunks) {
-  constexpr int KB = (RMAX + 63) / 64;  // 64-wide k-blocks of the rank
+  using SM = ExpandSmem<RMAX>;
+  constexpr int KB = SM::KB, NBUF = SM::kNBuf, D = NBUF - 1;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ SlotView v;
+  __shared__ SlotView vt[kExpandMaxTiles];   // adapter tables of each tile's key
+  __shared__ SgmvTile tiles_s[kExpandMaxTiles];
+  __shared__ int orow_map[kExpandMaxTiles][kTileRows];  // out row of each tile row
   __shared__ uint32_t taddr_s;
-  __shared__ __align__(8) uint64_t done_bar;
-  __shared__ int orow_s[kTileRows];
+  __shared__ __align__(8) uint64_t mma_bar[2];
   cudaGridDependencySynchronize();
-  const int tile_id = blockIdx.x / n_chunks, chunk = blockIdx.x - tile_id * n_chunks;
-  if (tile_id >= *a.n_tiles) return;
-  const SgmvTile tile = a.tiles[tile_id];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int j = 0;
-#pragma unroll
-  for (int jj = 1; jj < kMaxSlices; ++jj)
-    if (jj < a.sl.S && chunk >= a.chunk0[jj]) j = jj;
-  const int c0 = (chunk - a.chunk0[j]) * kExpandCols;  // first column inside slice j
-  const int nc = min(kExpandCols, a.sl.width[j] - c0);
-  if (tid == 0) {
+  const int total = *a.n_tiles * n_chunks;
+  const int w0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int w1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  if (w0 >= w1) return;
+  const int t_first = w0 / n_chunks;
+  const int n_my_tiles = (w1 - 1) / n_chunks - t_first + 1;
+  if (n_my_tiles > kExpandMaxTiles) {  // the launch sizes the grid so that this cannot be
+    if (threadIdx.x == 0) set_error(a.err, LORA_DEV_ERR_INTERNAL);
+    return;
+  }
+  uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  uint8_t* hhi = smem;
+  uint8_t* hlo = hhi + SM::kH;
+  uint8_t* bsm = hlo + SM::kH;  // [NBUF][KB][kExpandCols rows][128 B]
+  __nv_bfloat16* osm = reinterpret_cast<__nv_bfloat16*>(bsm + NBUF * SM::kB);  // [NBUF][128][kOStride]
+  const int R = a.R;
+  if (tid < n_my_tiles) {  // this CTA's tiles and their tables
+    const SgmvTile t = a.tiles[t_first + tid];
+    tiles_s[tid] = t;
     uint32_t bad = 0;
-    tb.resolve(tile.key, a.sl.S, kModeFused, v, bad);
-    mbar_init(&done_bar, 1);
+    tb.resolve(t.key, a.sl.S, kModeFused, vt[tid], bad);
+    if (bad) set_error(a.err, bad);
+  }
+  if (tid == 0) {
+    mbar_init(&mma_bar[0], 1);
+    mbar_init(&mma_bar[1], 1);
     fence_barrier_init();
   }
-  for (int r = tid; r < kTileRows; r += kSgmvThreads)
-    orow_s[r] = r < tile.rows ? (int)tb.out_row(a.perm[tile.pos0 + r]) : 0;
-  __syncthreads();
-  const int ja = v.ja[j];
-  if (ja < 0 || nc <= 0) return;
-  const int R = a.R;
-  const int N = (nc + 15) / 16 * 16;
-  uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-  uint8_t* hhi = smem;                                 // [KB][128 rows][128 B]
-  uint8_t* hlo = hhi + KB * kTileRows * 128;
-  uint8_t* bsm = hlo + KB * kTileRows * 128;           // [KB][kExpandCols rows][128 B]
-  __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(bsm + KB * kExpandCols * 128);
-  constexpr int kOStride = kExpandCols + 8;             // staged out row (elements)
-  if (warp == 0) tc::tmem_alloc(&taddr_s, kExpandCols);
-
-  // B rows of the chunk (zero past nc and past R inside the k-block)
-  const __nv_bfloat16* bsrc = v.B[j] + (size_t)c0 * R;
-  for (int i = tid; i < KB * kExpandCols * 8; i += kSgmvThreads) {
-    const int kb = i / (kExpandCols * 8), rem = i - kb * kExpandCols * 8;
-    const int c = rem >> 3, g = rem & 7, k = kb * 64 + g * 8;
-    const bool ok = c < nc && k < R;
-    cp_async16_zfill(bsm + (size_t)kb * kExpandCols * 128 + tc::sw128_offset(c, g * 8),
-                     ok ? bsrc + (size_t)c * R + k : bsrc, ok);
+  for (int i = tid; i < n_my_tiles * kTileRows; i += kExpandThreads) {
+    const int lt = i / kTileRows, r = i - lt * kTileRows;
+    const SgmvTile t = a.tiles[t_first + lt];
+    orow_map[lt][r] = r < t.rows ? (int)tb.out_row(a.perm[t.pos0 + r]) : 0;
   }
-  cp_async_commit();
-  // out segments of the tile's rows
-  const int64_t ocol = a.sl.off[j] + c0;
-  if (a.add_inputs) {
-    for (int i = tid; i < tile.rows * (nc / 8); i += kSgmvThreads) {
-      const int r = i / (nc / 8), g = i - r * (nc / 8);
-      cp_async16(os + (size_t)r * kOStride + g * 8, a.out + (int64_t)orow_s[r] * a.ld_out + ocol + g * 8);
-    }
-  }
-  cp_async_commit();
-  // h of the tile's rows, slice ja, as a bf16 (hi, lo) pair
-  for (int i = tid; i < KB * kTileRows * 8; i += kSgmvThreads) {
-    const int kb = i / (kTileRows * 8), rem = i - kb * kTileRows * 8;
-    const int r = rem >> 3, g = rem & 7, k = kb * 64 + g * 8;
-    float hv[8];
-    if (r < tile.rows && k < R) {
-      const float* hp = a.hbuf + (size_t)(tile.pos0 + r) * a.hs + ja * R + k;
-      const float4 h0 = *reinterpret_cast<const float4*>(hp);
-      const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
-      hv[0] = h0.x; hv[1] = h0.y; hv[2] = h0.z; hv[3] = h0.w;
-      hv[4] = h1.x; hv[5] = h1.y; hv[6] = h1.z; hv[7] = h1.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) hv[e] = 0.0f;
-    }
-    uint4 hi, lo;
-    split_bf16x2(hv[0], hv[1], hi.x, lo.x);
-    split_bf16x2(hv[2], hv[3], hi.y, lo.y);
-    split_bf16x2(hv[4], hv[5], hi.z, lo.z);
-    split_bf16x2(hv[6], hv[7], hi.w, lo.w);
-    const uint32_t off = (uint32_t)kb * kTileRows * 128 + tc::sw128_offset(r, g * 8);
-    *reinterpret_cast<uint4*>(hhi + off) = hi;
-    *reinterpret_cast<uint4*>(hlo + off) = lo;
-  }
-  cp_async_wait<1>();  // B rows landed (the out segments may still be in flight)
-  fence_proxy_async_smem();
+  if (warp == 0) tc::tmem_alloc(&taddr_s, 2 * kExpandCols);  // two accumulators
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t taddr = taddr_s;
-  bool ok = true;
-  if (tid == 0) {
-    const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, N);
-    const int ksteps = (R + 15) / 16;
-    for (int pass = 0; pass < 2; ++pass) {
-      const uint8_t* hsrc = pass == 0 ? hhi : hlo;
-      for (int s = 0; s < ksteps; ++s) {
-        const int kb = s >> 2, ks = s & 3;
-        const uint32_t ha = smem_addr(hsrc + (size_t)kb * kTileRows * 128) + ks * 32;
-        const uint32_t ba = smem_addr(bsm + (size_t)kb * kExpandCols * 128) + ks * 32;
-        tc::mma_bf16(taddr, tc::sw128_desc(ha), tc::sw128_desc(ba), idesc,
-                     (pass > 0 || s > 0) ? 1u : 0u);
+
+  // Item w: (tile, slice j, first column c0, width nc) from arithmetic and the
+  // preloaded tables; every thread computes it itself.
+  struct Item {
+    int lt, j, ja, c0, nc;
+  };
+  auto item_of = [&](int w) {
+    Item it;
+    const int tile_id = w / n_chunks, chunk = w - tile_id * n_chunks;
+    it.lt = tile_id - t_first;
+    int j = 0;
+#pragma unroll
+    for (int jj = 1; jj < kMaxSlices; ++jj)
+      if (jj < a.sl.S && chunk >= a.chunk0[jj]) j = jj;
+    it.j = j;
+    it.ja = vt[it.lt].ja[j];
+    it.c0 = (chunk - a.chunk0[j]) * kExpandCols;
+    it.nc = min(kExpandCols, a.sl.width[j] - it.c0);
+    return it;
+  };
+
+  // Copies of item w into buffer buf: its B chunk (swizzled; only the K
+  // columns the MMAs read) and its out segments (16 lanes per 256-byte row).
+  auto prepare = [&](int w, int buf) {
+    const Item it = item_of(w);
+    if (it.ja < 0 || it.nc <= 0) return;
+    const __nv_bfloat16* bsrc = vt[it.lt].B[it.j] + (size_t)it.c0 * R;
+    uint8_t* bb = bsm + (size_t)buf * SM::kB;
+    const int cpr = (R + 15) >> 4 << 1;  // 16-byte pieces per B row the K-steps read
+    for (int i = tid; i < kExpandCols * cpr; i += kExpandThreads) {
+      const int c = i / cpr, k = (i - c * cpr) * 8;
+      const bool ok = c < it.nc && k < R;  // zeros past the slice's end and past R
+      cp_async16_zfill(bb + (size_t)(k >> 6) * kExpandCols * 128 + tc::sw128_offset(c, k & 63),
+                       ok ? bsrc + (size_t)c * R + k : bsrc, ok);
+    }
+    if (a.add_inputs) {
+      const int rows = tiles_s[it.lt].rows, vpr = it.nc >> 3;
+      const __nv_bfloat16* src = a.out + a.sl.off[it.j] + it.c0;
+      __nv_bfloat16* ob = osm + (size_t)buf * kTileRows * SM::kOStride;
+#pragma unroll
+      for (int u = 0; u < kTileRows * 16 / kExpandThreads; ++u) {
+        const int i = tid + u * kExpandThreads, r = i >> 4, g = i & 15;
+        if (r < rows && g < vpr)
+          cp_async16(ob + r * SM::kOStride + g * 8,
+                     src + (int64_t)orow_map[it.lt][r] * a.ld_out + g * 8);
       }
     }
-    tc::mma_commit(&done_bar);
-    if (!mbar_wait_bounded(&done_bar, 0)) ok = false;
-  }
-  cp_async_wait<0>();  // out segments landed
-  __syncthreads();
-  tc::fence_after_sync();
-  const bool all_ok = __syncthreads_and(ok);
-  if (!all_ok && tid == 0) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
-  if (all_ok) {
-    // epilogue: thread = tile row; RN_bf16(out + scale * d), 16 columns at a time
-    const int r = warp * 32 + lane;
-    const float sc = v.scale;
-    __nv_bfloat16* orow = a.out + (int64_t)orow_s[r] * a.ld_out + ocol;
-    const __nv_bfloat16* srow = os + (size_t)r * kOStride;
-    for (int c = 0; c < N; c += 16) {
-      float d[16];
-      tc::tmem_ld16(taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, d);
-      if (r < tile.rows) {
+  };
+
+  // h of (tile, slice): sum of the shrink's planes, split into bf16 (hi, lo)
+  auto load_h = [&](const SgmvTile& t, int ja) {
+    for (int i = tid; i < KB * kTileRows * 8; i += kExpandThreads) {
+      const int kb = i / (kTileRows * 8), rem = i - kb * kTileRows * 8;
+      const int r = rem >> 3, g = rem & 7, k = kb * 64 + g * 8;
+      float hv[8];
 #pragma unroll
-        for (int h = 0; h < 16; h += 8) {
-          if (c + h < nc) {
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (a.add_inputs) o = *reinterpret_cast<const uint4*>(srow + c + h);
-            uint4 res;
-            res.x = pack_bf16x2(bf16lo(o.x) + sc * d[h + 0], bf16hi(o.x) + sc * d[h + 1]);
-            res.y = pack_bf16x2(bf16lo(o.y) + sc * d[h + 2], bf16hi(o.y) + sc * d[h + 3]);
-            res.z = pack_bf16x2(bf16lo(o.z) + sc * d[h + 4], bf16hi(o.z) + sc * d[h + 5]);
-            res.w = pack_bf16x2(bf16lo(o.w) + sc * d[h + 6], bf16hi(o.w) + sc * d[h + 7]);
-            *reinterpret_cast<uint4*>(orow + c + h) = res;
-          }
+      for (int e = 0; e < 8; ++e) hv[e] = 0.0f;
+      if (r < t.rows && k < R) {
+        const float* hp = a.hbuf + (size_t)(t.pos0 + r) * a.hs + ja * R + k;
+        for (int sp = 0; sp < a.ksplit; ++sp) {
+          const float4 h0 = *reinterpret_cast<const float4*>(hp + sp * a.plane);
+          const float4 h1 = *reinterpret_cast<const float4*>(hp + sp * a.plane + 4);
+          hv[0] += h0.x; hv[1] += h0.y; hv[2] += h0.z; hv[3] += h0.w;
+          hv[4] += h1.x; hv[5] += h1.y; hv[6] += h1.z; hv[7] += h1.w;
+        }
+      }
+      uint4 hi, lo;
+      split_bf16x2(hv[0], hv[1], hi.x, lo.x);
+      split_bf16x2(hv[2], hv[3], hi.y, lo.y);
+      split_bf16x2(hv[4], hv[5], hi.z, lo.z);
+      split_bf16x2(hv[6], hv[7], hi.w, lo.w);
+      const uint32_t off = (uint32_t)kb * kTileRows * 128 + tc::sw128_offset(r, g * 8);
+      *reinterpret_cast<uint4*>(hhi + off) = hi;
+      *reinterpret_cast<uint4*>(hlo + off) = lo;
+    }
+  };
+
+  int h_lt = -1, h_ja = -1;
+  uint32_t commits[2] = {0u, 0u};  // MMA commits per accumulator (phase parity)
+  bool ok = true;
+  // issue the MMAs of item u (its copies have landed), into accumulator u & 1
+  auto issue_mma = [&](int u) {
+    const int buf = (u - w0) % NBUF, acc = (u - w0) & 1;
+    const Item it = item_of(u);
+    if (it.ja < 0 || it.nc <= 0) return;
+    if (it.lt != h_lt || it.ja != h_ja) {
+      // the previous item's MMAs read h: let them finish before it is replaced
+      if (tid == 0 && u > w0) {
+        const int pacc = (u - 1 - w0) & 1;
+        if (commits[pacc] && !mbar_wait_bounded(&mma_bar[pacc], (commits[pacc] - 1) & 1)) ok = false;
+      }
+      __syncthreads();
+      load_h(tiles_s[it.lt], it.ja);
+      h_lt = it.lt;
+      h_ja = it.ja;
+      fence_proxy_async_smem();
+      __syncthreads();
+    }
+    if (tid == 0) {
+      tc::fence_after_sync();
+      const int N = (it.nc + 15) / 16 * 16;
+      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, N);
+      const int ksteps = (R + 15) / 16;
+      const uint8_t* bb = bsm + (size_t)buf * SM::kB;
+      const uint32_t dt = taddr + (uint32_t)(acc * kExpandCols);
+      for (int pass = 0; pass < 2; ++pass) {
+        const uint8_t* hsrc = pass == 0 ? hhi : hlo;
+        for (int s = 0; s < ksteps; ++s) {
+          const int kb = s >> 2, ks = s & 3;
+          const uint32_t ha = smem_addr(hsrc + (size_t)kb * kTileRows * 128) + ks * 32;
+          const uint32_t ba = smem_addr(bb + (size_t)kb * kExpandCols * 128) + ks * 32;
+          tc::mma_bf16(dt, tc::sw128_desc(ha), tc::sw128_desc(ba), idesc,
+                       (pass > 0 || s > 0) ? 1u : 0u);
+        }
+      }
+      tc::mma_commit(&mma_bar[acc]);
+    }
+    ++commits[acc];
+  };
+
+  for (int i = 0; i < D; ++i) {
+    if (w0 + i < w1) prepare(w0 + i, i);
+    cp_async_commit();
+  }
+  cp_async_wait<D - 1>();  // copies of item w0
+  fence_proxy_async_smem();
+  __syncthreads();
+  issue_mma(w0);
+
+  for (int w = w0; w < w1; ++w) {
+    const int buf = (w - w0) % NBUF, acc = (w - w0) & 1;
+    // copies D items ahead (into the buffers item w-1 has released)
+    if (w + D < w1) prepare(w + D, (w + D - w0) % NBUF);
+    cp_async_commit();
+    // MMAs of item w+1 run while item w's epilogue reads its accumulator
+    if (w + 1 < w1) {
+      cp_async_wait<D - 1>();
+      fence_proxy_async_smem();
+      __syncthreads();
+      issue_mma(w + 1);
+    }
+    const Item it = item_of(w);
+    if (it.ja < 0 || it.nc <= 0) continue;  // uniform; no shared state read below
+    // (item w+1 uses the other accumulator, so the last commit on `acc` is item w's)
+    if (tid == 0 && !mbar_wait_bounded(&mma_bar[acc], (commits[acc] - 1) & 1)) ok = false;
+    const bool mma_ok = __syncthreads_and(ok);
+    tc::fence_after_sync();
+    // epilogue: warp (q, half) owns rows 32q.. and columns [64 half, 64 half + 64).
+    // Lane = row while the accumulator is read and combined with the staged
+    // out (in place, in shared memory); then 8 lanes per row for the stores.
+    const int rows = tiles_s[it.lt].rows;
+    const int q = warp & 3, half = warp >> 2, cbeg = half * 64;
+    __nv_bfloat16* ob = osm + (size_t)buf * kTileRows * SM::kOStride;
+    if (cbeg < it.nc) {  // uniform across the warp
+      const int r = q * 32 + lane;
+      const float sc = vt[it.lt].scale;
+      float d[64];
+      tc::tmem_ld64(taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kExpandCols + cbeg), d);
+      __nv_bfloat16* srow = ob + r * SM::kOStride;
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 8) {
+        const int c = cbeg + cc;
+        if (c < it.nc) {
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (a.add_inputs) o = *reinterpret_cast<const uint4*>(srow + c);
+          uint4 res;
+          res.x = pack_bf16x2(bf16lo(o.x) + sc * d[cc + 0], bf16hi(o.x) + sc * d[cc + 1]);
+          res.y = pack_bf16x2(bf16lo(o.y) + sc * d[cc + 2], bf16hi(o.y) + sc * d[cc + 3]);
+          res.z = pack_bf16x2(bf16lo(o.z) + sc * d[cc + 4], bf16hi(o.z) + sc * d[cc + 5]);
+          res.w = pack_bf16x2(bf16lo(o.w) + sc * d[cc + 6], bf16hi(o.w) + sc * d[cc + 7]);
+          *reinterpret_cast<uint4*>(srow + c) = res;
+        }
+      }
+      __syncwarp();
+      if (mma_ok) {
+        __nv_bfloat16* dst = a.out + a.sl.off[it.j] + it.c0;
+        const int g = lane & 7, c = cbeg + g * 8;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int rr = q * 32 + u * 4 + (lane >> 3);
+          if (rr < rows && c < it.nc)
+            *reinterpret_cast<uint4*>(dst + (int64_t)orow_map[it.lt][rr] * a.ld_out + c) =
+                *reinterpret_cast<const uint4*>(ob + rr * SM::kOStride + c);
         }
       }
     }
+    tc::fence_before_sync();
+    __syncthreads();  // accumulator `acc` and item w's buffers free
   }
+  cp_async_wait<0>();
+  if (!ok && tid == 0) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(taddr, kExpandCols);
+  if (warp == 0) tc::tmem_dealloc(taddr, 2 * kExpandCols);
 }
 
 inline int sgmv_shrink_smem(int sr_max) {
@@ -373,8 +516,7 @@ inline int sgmv_shrink_smem(int sr_max) {
   return kShrinkStages * (kTileRows * 128 + N * 128) + 1024;
 }
 inline int sgmv_expand_smem(int R) {
-  const int KB = (R + 63) / 64;
-  return KB * (2 * kTileRows * 128 + kExpandCols * 128) + kTileRows * (kExpandCols + 8) * 2 + 1024;
+  return R <= 64 ? ExpandSmem<64>::kTotal : ExpandSmem<128>::kTotal;
 }
 
 }  // namespace lora
