@@ -45,6 +45,24 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# DRAM bytes (read + write) of one launch of the decode step's kernel, from the
+# ncu capture summarised in profiles/delta_cluster_decode_qkv_n64.md, with the
+# hash of the sources it was taken on: reported only while they are unchanged.
+DECODE_TRAFFIC = {"bytes": 10650368, "sources_sha256_16": "9b24f132c990f9c0"}
+DECODE_SOURCES = ("lora_delta_gb300/csrc/bgmv.cuh", "lora_delta_gb300/csrc/common.cuh",
+                  "lora_delta_gb300/csrc/api.cu")
+
+
+def decode_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    ok = h.hexdigest()[:16] == DECODE_TRAFFIC["sources_sha256_16"]
+    return DECODE_TRAFFIC["bytes"] if ok else None
+
+
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -254,7 +272,7 @@ def run_ours(args, rank, world):
     achieved = abytes / (ms_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                "traffic": None, "peak_source": peak_src,
+                "traffic": decode_traffic(), "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": abytes,
                 "kernel": "delta_cluster_kernel<16,fused,LinearTables>"}
 

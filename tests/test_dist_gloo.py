@@ -1,0 +1,132 @@
+"""The data-parallel split, on two CPU processes over gloo.
+
+Rows of the linear delta and tokens of the MoE FC1 delta are independent
+("Module lora_delta": one adapter per row through LoraRoute;
+"bgmv_moe_gemm1_lora_delta": the delta stays per (token, slot)).  Ranks that
+each apply the delta to their own contiguous shard, with the adapter pool
+replicated, therefore reproduce the whole batch bit for bit, with no
+collective on the data path.  The test also checks the host reductions the
+benchmark's timing uses: barrier, max over ranks (the slowest rank's time) and
+sum over ranks (the rows all ranks processed).
+
+Each rank runs the oracle on its shard: what is tested here is the host-side
+sharding logic, which is the same on a GPU machine.
+"""
+from __future__ import annotations
+
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+WORLD = 2
+
+
+def _free_port() -> int:
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank: int, world: int, port: int, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    try:
+        import torch.distributed as dist
+
+        import oracle
+        from lora_delta_gb300 import dist as ldist
+        from lora_delta_gb300 import inputs
+
+        r, w = ldist.init("gloo")
+        assert (r, w) == (rank, world)
+        res = {}
+
+        # linear delta: contiguous row shards of a decode-shaped batch (67 rows:
+        # shards of 34 and 33; 3 slices, 6 slots of mixed rank, 10% unrouted)
+        case = inputs.linear_case(4321, 67, 512, (256, 128, 128), 6, 16, [16, 8, 16, 4, 16, 8],
+                                  32.0, p_none=0.1)
+        pool = oracle.build_pool(case.adapters, case.k_in, case.widths, case.max_loras,
+                                 case.max_rank)
+        lo, hi = ldist.shard_rows(case.n, r, w)
+        out = case.out0[lo:hi].copy()  # (a row slice can be a view of out0)
+        err = oracle.delta(out, case.x[lo:hi], case.seq_slot[lo:hi], pool)
+        shards = [None] * w
+        dist.all_gather_object(shards, (lo, hi, out, err))
+
+        # MoE FC1: token shards
+        mc = inputs.moe_case(T=37, top_k=4, E=8, H=256, I=64, rank=16, L=4)
+        tlo, thi = ldist.shard_rows(mc.T, r, w)
+        mo, merr = oracle.moe_fc1(np.ascontiguousarray(mc.x[tlo:thi]), mc.A_banks, mc.B_banks,
+                                  np.ascontiguousarray(mc.topk_ids[tlo:thi]),
+                                  np.ascontiguousarray(mc.lora_ids[tlo:thi]), mc.I, mc.rank,
+                                  mc.scale, mc.shared_a, mc.L)
+        mshards = [None] * w
+        dist.all_gather_object(mshards, (tlo, thi, mo, merr))
+
+        ldist.barrier()
+        res["max"] = ldist.max_over_ranks(1.5 + rank)
+        res["sum"] = ldist.sum_over_ranks(10 * (rank + 1))
+        if rank == 0:
+            whole = case.out0.copy()
+            werr = oracle.delta(whole, case.x, case.seq_slot, pool)
+            got = np.concatenate([s[2] for s in sorted(shards, key=lambda s: s[0])])
+            res["cover"] = sorted((s[0], s[1]) for s in shards)
+            res["linear_equal"] = bool(np.array_equal(got, whole))
+            res["linear_err"] = (werr, [s[3] for s in shards])
+            mwhole, mwerr = oracle.moe_fc1(mc.x, mc.A_banks, mc.B_banks, mc.topk_ids,
+                                           mc.lora_ids, mc.I, mc.rank, mc.scale, mc.shared_a,
+                                           mc.L)
+            mgot = np.concatenate([s[2] for s in sorted(mshards, key=lambda s: s[0])])
+            res["moe_equal"] = bool(np.array_equal(mgot, mwhole))
+            res["moe_cover"] = sorted((s[0], s[1]) for s in mshards)
+        dist.destroy_process_group()
+        q.put((rank, res, None))
+    except Exception as e:  # reported to the parent, which fails the test
+        q.put((rank, None, repr(e)))
+
+
+def test_shard_rows_partitions_contiguously():
+    from lora_delta_gb300.dist import shard_rows
+    for n in (0, 1, 7, 64, 67, 8192):
+        for w in (1, 2, 3, 8):
+            parts = [shard_rows(n, r, w) for r in range(w)]
+            assert parts[0][0] == 0 and parts[-1][1] == n
+            assert all(parts[i][1] == parts[i + 1][0] for i in range(w - 1))
+            sizes = [hi - lo for lo, hi in parts]
+            assert max(sizes) - min(sizes) <= 1
+
+
+def test_two_rank_shards_reproduce_the_whole_batch(oracle):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, WORLD, port, q)) for r in range(WORLD)]
+    for p in procs:
+        p.start()
+    results = {}
+    try:
+        for _ in range(WORLD):
+            rank, res, err = q.get(timeout=240)
+            assert err is None, f"rank {rank}: {err}"
+            results[rank] = res
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    for rank in range(WORLD):
+        assert results[rank]["max"] == 1.5 + (WORLD - 1)
+        assert results[rank]["sum"] == sum(10 * (r + 1) for r in range(WORLD))
+    r0 = results[0]
+    assert r0["cover"] == [(0, 34), (34, 67)]
+    assert r0["linear_equal"]
+    werr, shard_errs = r0["linear_err"]
+    assert werr == (shard_errs[0] | shard_errs[1])
+    assert r0["moe_cover"] == [(0, 19), (19, 37)]
+    assert r0["moe_equal"]
