@@ -153,13 +153,11 @@ struct SmemPlan {
   int o_stride;   // elements per staged out row (padded)
   int as_stride;  // elements per A / x row in shared memory (padded)
   int sr16;       // S * R rounded up to 16
-  int rx_per;     // (row, pair) entries owned by one CTA of the cluster
 };
 __host__ __device__ inline SmemPlan smem_plan(const DeltaArgs& a, int mode) {
   SmemPlan p;
   p.sr16 = (a.sr_max + 15) / 16 * 16;
   p.as_stride = a.kst + 8;
-  p.rx_per = (kRowsPerPass * p.sr16 + a.cs - 1) / a.cs;
   int o = 128;  // the pass's row ids (16 ints) at offset 64
   p.rows_off = o;
   o += ((a.row_cap * 4 + 127) / 128) * 128;
@@ -170,8 +168,8 @@ __host__ __device__ inline SmemPlan smem_plan(const DeltaArgs& a, int mode) {
   o = (o + 127) / 128 * 128;
   p.Pw_off = o;
   if (mode != kModeExpand) o += (p.sr16 > 128 ? p.sr16 : 128) * kRowsPerPass * 4;
-  p.Rx_off = o;  // partials received from the cluster: [cs][rx_per]
-  if (mode != kModeExpand) o += a.cs * p.rx_per * 4;
+  p.Rx_off = o;  // this CTA's partial h, read by the cluster: [kRowsPerPass][sr16]
+  if (mode != kModeExpand) o += kRowsPerPass * p.sr16 * 4;
   p.H_off = o;
   o += kRowsPerPass * p.sr16 * 4;
   // expand operands: the CTA's B rows and the pass's out segments
@@ -185,63 +183,78 @@ __host__ __device__ inline SmemPlan smem_plan(const DeltaArgs& a, int mode) {
   return p;
 }
 
-// 16-byte cp.async copies, issued by every thread of the CTA, of the A rows
-// (columns [k0, k0 + kw) of the key's active (slice, rank) pairs) into As.
+// 16-byte cp.async copies of the A rows (columns [k0, k0 + kw) of the key's
+// active (slice, rank) pairs) into As, by `nw` warps (`tid` counts from the
+// first of them).  Warp w copies rows w, w + nw, ...; its lanes cover the
+// row's 16-byte pieces.  Row t is pair (jj, q) = (t / R, t % R), tracked
+// incrementally (R >= 8 >= nw, so q wraps at most once per step), so the
+// loop carries no division and only one pointer reload per slice.
 __device__ __forceinline__ void copy_a_rows(const DeltaArgs& a, const SlotView& v, int SRa,
                                             int k0, int kw, __nv_bfloat16* As, int stride,
-                                            int tid) {
-  const int R = a.R;
-  const int vpr = kw / 8;
-  for (int idx = tid; idx < SRa * vpr; idx += kThreads) {
-    const int t = idx / vpr, c = idx - t * vpr;
-    const int jj = t / R, q = t - jj * R;
-    cp_async16(As + (size_t)t * stride + c * 8,
-               v.A[v.act_slice[jj]] + (size_t)q * a.k_in + k0 + c * 8);
+                                            int tid, int nw = kWarps) {
+  const int R = a.R, vpr = kw >> 3, warp = tid >> 5, lane = tid & 31;
+  const size_t kin = (size_t)a.k_in;
+  int jj = 0, q = warp;
+  const __nv_bfloat16* base = v.A[v.act_slice[0]] + k0 + lane * 8;
+  __nv_bfloat16* dst = As + (size_t)warp * stride + lane * 8;
+#pragma unroll 2
+  for (int t = warp; t < SRa; t += nw) {
+    const __nv_bfloat16* src = base + (size_t)q * kin;
+    for (int c = 0; c < vpr - lane; c += 32) cp_async16(dst + c * 8, src + c * 8);
+    dst += (size_t)nw * stride;
+    q += nw;
+    if (q >= R) {
+      q -= R;
+      if (++jj < v.nact) base = v.A[v.act_slice[jj]] + k0 + lane * 8;
+    }
   }
 }
 
-// ... and of the pass's x rows into Xs.
+// ... and of the pass's x rows into Xs (warp per row, as above).
 template <class Tables>
 __device__ __forceinline__ void copy_x_rows(const DeltaArgs& a, const Tables& tb, const int* prow,
                                             int nr, int k0, int kw, __nv_bfloat16* Xs,
-                                            int stride, int tid) {
-  const int vpr = kw / 8;
-  for (int idx = tid; idx < nr * vpr; idx += kThreads) {
-    const int r = idx / vpr, c = idx - r * vpr;
-    cp_async16(Xs + (size_t)r * stride + c * 8, a.x + tb.x_row(prow[r]) * a.ld_x + k0 + c * 8);
+                                            int stride, int tid, int nw = kWarps) {
+  const int vpr = kw >> 3, warp = tid >> 5, lane = tid & 31;
+  for (int r = warp; r < nr; r += nw) {
+    const __nv_bfloat16* src = a.x + tb.x_row(prow[r]) * a.ld_x + k0 + lane * 8;
+    __nv_bfloat16* dst = Xs + (size_t)r * stride + lane * 8;
+    for (int c = 0; c < vpr - lane; c += 32) cp_async16(dst + c * 8, src + c * 8);
   }
 }
 
 // cp.async copies of the B rows of this CTA's columns [cb, ce) into Bs
-// (column c at Bs[(c - cb) * R]).
+// (column c at Bs[(c - cb) * R]).  Each slice's part is one contiguous run.
 __device__ __forceinline__ void copy_b_rows(const DeltaArgs& a, const SlotView& v, int cb, int ce,
-                                            __nv_bfloat16* Bs, int tid) {
+                                            __nv_bfloat16* Bs, int tid, int nthr = kThreads) {
   for (int j = 0; j < a.sl.S; ++j) {
-    if (v.ja[j] < 0) continue;
     const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
-    if (c1 <= c0) continue;
+    if (c1 <= c0 || v.ja[j] < 0) continue;
     const int nvec = (c1 - c0) * a.R / 8;
-    const __nv_bfloat16* src = v.B[j] + (size_t)(c0 - a.rel[j]) * a.R;
-    __nv_bfloat16* dst = Bs + (size_t)(c0 - cb) * a.R;
-    for (int i = tid; i < nvec; i += kThreads) cp_async16(dst + i * 8, src + i * 8);
+    const __nv_bfloat16* src = v.B[j] + (size_t)(c0 - a.rel[j]) * a.R + tid * 8;
+    __nv_bfloat16* dst = Bs + (size_t)(c0 - cb) * a.R + tid * 8;
+#pragma unroll 4
+    for (int i = 0; i < nvec - tid; i += nthr) cp_async16(dst + i * 8, src + i * 8);
   }
 }
 
 // cp.async copies of the pass's out segments in this CTA's columns into Os
-// (row r, column c at Os[r * o_stride + (c - cb)]).
+// (row r, column c at Os[r * o_stride + (c - cb)]); warp per row.
 template <class Tables>
 __device__ __forceinline__ void copy_out_rows(const DeltaArgs& a, const Tables& tb,
                                               const SlotView& v, const int* prow, int nr, int cb,
-                                              int ce, __nv_bfloat16* Os, int o_stride, int tid) {
+                                              int ce, __nv_bfloat16* Os, int o_stride, int tid,
+                                              int nw = kWarps) {
+  const int warp = tid >> 5, lane = tid & 31;
   for (int j = 0; j < a.sl.S; ++j) {
-    if (v.ja[j] < 0) continue;
     const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
-    if (c1 <= c0) continue;
-    const int vpr = (c1 - c0) / 8;
-    for (int i = tid; i < nr * vpr; i += kThreads) {
-      const int r = i / vpr, c = i - r * vpr;
-      cp_async16(Os + (size_t)r * o_stride + (c0 - cb) + c * 8,
-                 a.out + tb.out_row(prow[r]) * a.ld_out + a.sl.off[j] + (c0 - a.rel[j]) + c * 8);
+    if (c1 <= c0 || v.ja[j] < 0) continue;
+    const int vpr = (c1 - c0) >> 3;
+    const int64_t col = a.sl.off[j] + (c0 - a.rel[j]) + lane * 8;
+    for (int r = warp; r < nr; r += nw) {
+      const __nv_bfloat16* src = a.out + tb.out_row(prow[r]) * a.ld_out + col;
+      __nv_bfloat16* dst = Os + (size_t)r * o_stride + (c0 - cb) + lane * 8;
+      for (int c = 0; c < vpr - lane; c += 32) cp_async16(dst + c * 8, src + c * 8);
     }
   }
 }
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
     delta_cluster_kernel(const DeltaArgs a, const Tables tb) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ SlotView v;
-  __shared__ int warp_cnt[kWarps];
+  __shared__ int nrows_s, rows_base_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
   const int key = (int)cluster_index_x();
@@ -313,52 +326,68 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
   const int cb = min(a.sl.n_cols, (int)crank * a.cpc);
   const int ce = min(a.sl.n_cols, cb + a.cpc);
   // Adapter weights are never produced by the preceding kernel, so their
-  // copies may start before the dependency wait and overlap its tail.
+  // copies may start before the dependency wait and overlap its tail.  Warps
+  // 1.. issue them while warp 0 waits for the dependency, finds the key's
+  // rows and starts the first pass's x / out copies.
   const bool early = MODE != kModeExpand && a.early && v.nact > 0 && nst > 0;
-  if (early) {
-    copy_a_rows(a, v, SRa, k_lo, min(a.kst, k_hi - k_lo), As, stride, tid);
-    if (b_staged) copy_b_rows(a, v, cb, ce, Bs, tid);
+  if (early && warp > 0) {
+    copy_a_rows(a, v, SRa, k_lo, min(a.kst, k_hi - k_lo), As, stride, tid - 32, kWarps - 1);
+    if (b_staged) copy_b_rows(a, v, cb, ce, Bs, tid - 32, kThreads - 32);
     cp_async_commit();
   }
   bool b_loaded = early && b_staged;
   if (v.nact > 0 && MODE != kModeShrink && !b_staged && warp == 1) prefetch_b(a, v, cb, ce, lane);
   cudaTriggerProgrammaticLaunchCompletion();
   cudaGridDependencySynchronize();
-  if (v.nact == 0) return;  // the same decision in every CTA of the cluster
+  // Without a routing pass, CTA 0 of key 0 also checks every slot for
+  // LORA_DEV_ERR_SLOT, so it scans even when key 0 adapts nothing.
+  const bool slot_check = !a.perm && key == 0 && crank == 0;
+  if (v.nact == 0 && !slot_check) return;  // the same in every CTA of the cluster
 
-  // ---- the key's rows, in ascending row order --------------------------
-  int nrows;
-  const int* rows;
-  if (a.perm) {
-    const int s0 = a.seg_start[key];
-    nrows = a.seg_start[key + 1] - s0;
-    rows = a.perm + s0;
-  } else {
-    int total = 0;
-    bool bad_slot = false;
-    for (int base = 0; base < a.n; base += kThreads) {
-      const int i = base + tid;
-      const int s = (i < a.n) ? a.seq_slot[i] : -1;
-      const bool hit = (s == key);
-      bad_slot |= (s >= a.n_keys);
-      const unsigned m = __ballot_sync(0xffffffffu, hit);
-      if (lane == 0) warp_cnt[warp] = __popc(m);
-      __syncthreads();
-      int before = total, sum = 0;
+  // ---- the key's rows, in ascending row order (warp 0) -----------------
+  if (warp == 0) {
+    int total = 0, s0 = 0;
+    if (a.perm) {
+      s0 = a.seg_start[key];
+      total = a.seg_start[key + 1] - s0;
+    } else {
+      bool bad_slot = false;
+      for (int base = 0; base < a.n; base += 32 * 8) {
+        int sl[8];
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        before += (w < warp) ? warp_cnt[w] : 0;
-        sum += warp_cnt[w];
+        for (int u = 0; u < 8; ++u) {  // independent loads, one round trip
+          const int i = base + u * 32 + lane;
+          sl[u] = i < a.n ? a.seq_slot[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool hit = sl[u] == key;
+          bad_slot |= sl[u] >= a.n_keys;
+          const unsigned m = __ballot_sync(0xffffffffu, hit);
+          if (hit) rows_s[total + __popc(m & ((1u << lane) - 1u))] = base + u * 32 + lane;
+          total += __popc(m);
+        }
       }
-      if (hit) rows_s[before + __popc(m & ((1u << lane) - 1u))] = i;
-      total += sum;
-      __syncthreads();
+      if (__any_sync(0xffffffffu, bad_slot) && key == 0 && crank == 0 && lane == 0)
+        set_error(a.err, LORA_DEV_ERR_SLOT);
     }
-    if (key == 0 && crank == 0 && __syncthreads_or(bad_slot) && tid == 0)
-      set_error(a.err, LORA_DEV_ERR_SLOT);
-    nrows = total;
-    rows = rows_s;
+    if (lane == 0) {
+      nrows_s = total;
+      rows_base_s = s0;
+    }
+    __syncwarp();
+    if (early && total > 0 && total >= a.min_rows && total < a.max_rows) {
+      const int* rows0 = a.perm ? a.perm + s0 : rows_s;
+      const int nr0 = min(kRowsPerPass, total);
+      copy_x_rows(a, tb, rows0, nr0, k_lo, min(a.kst, k_hi - k_lo), Xs, stride, lane, 1);
+      if (o_staged) copy_out_rows(a, tb, v, rows0, nr0, cb, ce, Os, plan.o_stride, lane, 1);
+      cp_async_commit();
+    }
   }
+  __syncthreads();
+  if (v.nact == 0) return;
+  const int nrows = nrows_s;
+  const int* rows = a.perm ? a.perm + rows_base_s : rows_s;
   if (nrows == 0 || nrows < a.min_rows || nrows >= a.max_rows) {  // uniform
     if (early) cp_async_wait<0>();  // no copy may land in a CTA that has exited
     return;
@@ -400,9 +429,10 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       // expand operands of the pass: into shared memory when they fit, else L2
       if (b_staged && !b_loaded) copy_b_rows(a, v, cb, ce, Bs, tid);
       b_loaded = b_staged;
-      if (o_staged)
-        copy_out_rows(a, tb, v, prow, nr, cb, ce, Os, plan.o_stride, tid);
-      else if (warp == 2)
+      if (o_staged) {
+        if (!(early && p0 == 0))  // (the first pass's were started by warp 0)
+          copy_out_rows(a, tb, v, prow, nr, cb, ce, Os, plan.o_stride, tid);
+      } else if (warp == 2)
         prefetch_out(a, tb, v, prow, nr, cb, ce, lane);
       cp_async_commit();  // (its own group, so the stage waits below stay in order)
     }
@@ -411,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       // ---- copies of the first two stages ---------------------------------
       if (nst > 0) {
         if (!skip_a0) copy_a_rows(a, v, SRa, k_lo, min(a.kst, k_hi - k_lo), As, stride, tid);
-        copy_x_rows(a, tb, prow, nr, k_lo, min(a.kst, k_hi - k_lo), Xs, stride, tid);
+        if (!(early && p0 == 0))  // (the first pass's were started by warp 0)
+          copy_x_rows(a, tb, prow, nr, k_lo, min(a.kst, k_hi - k_lo), Xs, stride, tid);
         cp_async_commit();
         if (nst > 1) {
           const int k1 = k_lo + a.kst;
@@ -425,9 +456,11 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       skip_a0 = (nst == 1);  // a single stage keeps its A rows for the next passes
 
       // ---- shrink on the tensor cores: partial P[pair][row] over this CTA's k
-      float acc[4][8];
+      // pair tiles per warp: mt <= S * R / 16 <= 8 * RMAX / 16, so at most RMAX / 16
+      constexpr int MI = RMAX / 16 < 4 ? RMAX / 16 : 4;
+      float acc[MI][8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
       for (int st = 0; st < nst; ++st) {
@@ -454,18 +487,45 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
           const uint32_t aaddr = smem_addr(Ab + (size_t)(my_m0 * 16 + (((lane >> 3) & 1) << 3) +
                                                          (lane & 7)) * stride + ((lane >> 4) << 3));
           const uint32_t mstep = 8u * 16u * (uint32_t)stride * 2u;  // 8 pair tiles, bytes
-          for (int ks = my_g; ks < ksteps; ks += G) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+          if (mt >= kWarps) {  // up to 4 pair tiles per warp: 4 independent chains
+            for (int ks = my_g; ks < ksteps; ks += G) {
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (my_m0 + i * kWarps < mt && (i == 0 || mt >= kWarps)) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(aaddr + i * mstep + ks * 32, a0, a1, a2, a3);
-                mma_16816(&acc[i][0], a0, a1, a2, a3, b0, b1);
-                mma_16816(&acc[i][4], a0, a1, a2, a3, b2, b3);
+              for (int i = 0; i < MI; ++i) {
+                if (my_m0 + i * kWarps < mt) {
+                  uint32_t a0, a1, a2, a3;
+                  ldsm_x4(aaddr + i * mstep + ks * 32, a0, a1, a2, a3);
+                  mma_16816(&acc[i][0], a0, a1, a2, a3, b0, b1);
+                  mma_16816(&acc[i][4], a0, a1, a2, a3, b2, b3);
+                }
               }
             }
+          } else {  // one pair tile: two chains over alternate k-steps
+            float acc2[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc2[e] = 0.0f;
+            int ks = my_g;
+            for (; ks + G < ksteps; ks += 2 * G) {
+              uint32_t b0, b1, b2, b3, c0, c1, c2, c3, a0, a1, a2, a3, d0, d1, d2, d3;
+              ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+              ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
+              ldsm_x4(xaddr + (ks + G) * 32, c0, c1, c2, c3);
+              ldsm_x4(aaddr + (ks + G) * 32, d0, d1, d2, d3);
+              mma_16816(&acc[0][0], a0, a1, a2, a3, b0, b1);
+              mma_16816(&acc[0][4], a0, a1, a2, a3, b2, b3);
+              mma_16816(&acc2[0], d0, d1, d2, d3, c0, c1);
+              mma_16816(&acc2[4], d0, d1, d2, d3, c2, c3);
+            }
+            if (ks < ksteps) {
+              uint32_t b0, b1, b2, b3, a0, a1, a2, a3;
+              ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+              ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
+              mma_16816(&acc[0][0], a0, a1, a2, a3, b0, b1);
+              mma_16816(&acc[0][4], a0, a1, a2, a3, b2, b3);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[0][e] += acc2[e];
           }
         }
         __syncthreads();  // buffer `buf` free
@@ -479,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       // per-warp k-group partials -> Pw[g][pair][row]
       if (shrink_warp) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < MI; ++i) {
           const int m = my_m0 + i * kWarps;
           if (m < mt && (i == 0 || mt >= kWarps)) {
             float* base = Pw + ((size_t)my_g * SRk + m * 16 + gq) * kRowsPerPass + 2 * tq;
@@ -495,39 +555,67 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
         }
       }
       __syncthreads();
-      // ---- the CS partials meet through DSMEM in two pushes: every CTA
-      // stores its partial of entry e into the receive area of e's owner;
-      // each owner sums its entries over the cluster in rank order and stores
-      // the sum into every CTA's H.  Only remote stores, no remote loads. ----
+      // ---- the cluster's partials meet in one exchange: every CTA leaves its
+      // partial (summed over its k-groups) in its own Rx; after one cluster
+      // barrier each CTA reads the ncta partials of its entries from the
+      // peers' shared memory, all loads in flight together, and sums them in
+      // rank order into H.  A second barrier phase, arrived at right after the
+      // reads and waited on only before Rx is rewritten (the next pass) or the
+      // CTA exits, keeps every Rx alive while peers may still read it. ----
       const int nel = nr * SRa;
-      const int per = plan.rx_per;
+      if (p0 > 0) cluster_wait();  // the previous pass's readers are done with Rx
+      // this thread's entries: groups of 4 consecutive pairs (SRa is a
+      // multiple of 8), group g = tid + i * kThreads as (row r, pair p)
+      const int gpr = SRa >> 2;  // groups per row
+      const int dr = kThreads / gpr, dp = (kThreads - dr * gpr) * 4;
+      const int r_first = tid / gpr, p_first = (tid - r_first * gpr) * 4;
+      {
+        int r = r_first, p = p_first;
+        for (int e = tid * 4; e < nel; e += kThreads * 4) {
+          float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int g = 0; g < G; ++g) {
+            const float* src = Pw + ((size_t)g * SRk + p) * kRowsPerPass + r;
+            s.x += src[0];
+            s.y += src[kRowsPerPass];
+            s.z += src[2 * kRowsPerPass];
+            s.w += src[3 * kRowsPerPass];
+          }
+          *reinterpret_cast<float4*>(Rx + r * SR16 + p) = s;
+          p += dp;
+          r += dr;
+          if (p >= SRa) {
+            p -= SRa;
+            ++r;
+          }
+        }
+      }
+      cluster_arrive();  // partials in place
+      cluster_wait();
       {
         const uint32_t rx_addr = smem_addr(Rx);
-        for (int e = tid; e < nel; e += kThreads) {
-          const int r = e / SRa, p = e - r * SRa;
-          float s = 0.0f;
-          for (int g = 0; g < G; ++g) s += Pw[((size_t)g * SRk + p) * kRowsPerPass + r];
-          const int owner = e / per, slot = e - owner * per;
-          dsmem_st_f32(dsmem_map(rx_addr + 4u * (uint32_t)(crank * per + slot), owner), s);
+        int r = r_first, p = p_first;
+        for (int e = tid * 4; e < nel; e += kThreads * 4) {
+          const uint32_t addr = rx_addr + 4u * (uint32_t)(r * SR16 + p);
+          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int c = 0; c < ncta; ++c) {  // rank order
+            const float4 v = dsmem_ld_f32x4(dsmem_map(addr, (uint32_t)c));
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+          }
+          *reinterpret_cast<float4*>(H + r * SR16 + p) = sum;
+          p += dp;
+          r += dr;
+          if (p >= SRa) {
+            p -= SRa;
+            ++r;
+          }
         }
       }
-      cluster_arrive();  // partials delivered
-      cluster_wait();
-      {
-        const uint32_t h_addr = smem_addr(H);
-        const int e0 = (int)crank * per;
-        for (int i = tid; i < per; i += kThreads) {
-          const int e = e0 + i;
-          if (e >= nel) break;
-          float sum = 0.0f;
-          for (int c = 0; c < ncta; ++c) sum += Rx[c * per + i];
-          const int r = e / SRa, p = e - r * SRa;
-          const uint32_t off = 4u * (uint32_t)(r * SR16 + p);
-          for (int c = 0; c < ncta; ++c) dsmem_st_f32(dsmem_map(h_addr + off, c), sum);
-        }
-      }
-      cluster_arrive();  // sums delivered
-      cluster_wait();
+      cluster_arrive_relaxed();  // done reading the peers' Rx (waited on later)
+      __syncthreads();   // H complete
     } else {
       for (int i = tid; i < nr * SRa; i += kThreads) {
         const int r = i / SRa, t = i - r * SRa;
@@ -590,28 +678,46 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
           const __nv_bfloat16* bsb = Bs + (size_t)(c0 - cb + gq) * R + 2 * tq;
           const __nv_bfloat16* os0 = Os + (size_t)row0 * plan.o_stride + (c0 - cb) + 2 * tq;
           const __nv_bfloat16* os1 = Os + (size_t)row1 * plan.o_stride + (c0 - cb) + 2 * tq;
-          for (int t = warp; t < ntl; t += kWarps) {
-            const __nv_bfloat16* brow = bsb + (size_t)t * 8 * R;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+          // batches of NS tiles: every shared-memory load first, then the
+          // NS independent MMA chains, then the stores
+          constexpr int NS = KS <= 2 ? 2 : 1;
+          for (int t0 = warp; t0 < ntl; t0 += kWarps * NS) {
+            uint32_t bf[NS][KS][2], ov[NS][2];
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-              if (kk * 16 < R) {
-                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(brow + kk * 16);
-                const uint32_t b1 =
-                    (kk * 16 + 8 < R) ? *reinterpret_cast<const uint32_t*>(brow + kk * 16 + 8) : 0u;
-                mma_16816(d, ahi[kk][0], ahi[kk][1], ahi[kk][2], ahi[kk][3], b0, b1);
-                mma_16816(d, alo[kk][0], alo[kk][1], alo[kk][2], alo[kk][3], b0, b1);
+            for (int b = 0; b < NS; ++b) {
+              const int t = t0 + b * kWarps;
+              if (t < ntl) {
+                const __nv_bfloat16* brow = bsb + (size_t)t * 8 * R;
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                  bf[b][kk][0] =
+                      (kk * 16 < R) ? *reinterpret_cast<const uint32_t*>(brow + kk * 16) : 0u;
+                  bf[b][kk][1] =
+                      (kk * 16 + 8 < R) ? *reinterpret_cast<const uint32_t*>(brow + kk * 16 + 8) : 0u;
+                }
+                ov[b][0] = (a.add_inputs && ok0) ? *reinterpret_cast<const uint32_t*>(os0 + t * 8) : 0u;
+                ov[b][1] = (a.add_inputs && ok1) ? *reinterpret_cast<const uint32_t*>(os1 + t * 8) : 0u;
               }
             }
-            if (ok0) {
-              const uint32_t o = a.add_inputs ? *reinterpret_cast<const uint32_t*>(os0 + t * 8) : 0u;
-              *reinterpret_cast<uint32_t*>(o0base + t * 8) =
-                  pack_bf16x2(bf16lo(o) + sc * d[0], bf16hi(o) + sc * d[1]);
-            }
-            if (ok1) {
-              const uint32_t o = a.add_inputs ? *reinterpret_cast<const uint32_t*>(os1 + t * 8) : 0u;
-              *reinterpret_cast<uint32_t*>(o1base + t * 8) =
-                  pack_bf16x2(bf16lo(o) + sc * d[2], bf16hi(o) + sc * d[3]);
+#pragma unroll
+            for (int b = 0; b < NS; ++b) {
+              const int t = t0 + b * kWarps;
+              if (t < ntl) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                  if (kk * 16 < R) {
+                    mma_16816(d, ahi[kk][0], ahi[kk][1], ahi[kk][2], ahi[kk][3], bf[b][kk][0], bf[b][kk][1]);
+                    mma_16816(d, alo[kk][0], alo[kk][1], alo[kk][2], alo[kk][3], bf[b][kk][0], bf[b][kk][1]);
+                  }
+                }
+                if (ok0)
+                  *reinterpret_cast<uint32_t*>(o0base + t * 8) =
+                      pack_bf16x2(bf16lo(ov[b][0]) + sc * d[0], bf16hi(ov[b][0]) + sc * d[1]);
+                if (ok1)
+                  *reinterpret_cast<uint32_t*>(o1base + t * 8) =
+                      pack_bf16x2(bf16lo(ov[b][1]) + sc * d[2], bf16hi(ov[b][1]) + sc * d[3]);
+              }
             }
           }
           continue;
@@ -658,6 +764,8 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
     }
   }
   if (timed_out && tid == 0) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
+  // the last exchange's readers are done before this CTA's Rx goes away
+  if (MODE != kModeExpand) cluster_wait();
 }
 
 // Zeros for the MoE pairs that get no delta (the no-key bucket).
