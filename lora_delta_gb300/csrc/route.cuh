@@ -5,7 +5,8 @@
 // device, with no host round trip.
 //
 // One CTA of kRouteThreads threads.  The items are cut into one contiguous
-// block per warp; pass 1 counts keys per (warp, key) with __match_any_sync,
+// block per warp, read kRouteBatch keys per lane at a time; pass 1 counts keys
+// per (warp, key) with __match_any_sync,
 // a block scan turns the counts into per-(warp, key) output positions, and
 // pass 2 scatters every item to its position -- the rank inside a warp
 // iteration comes from the match mask, so the order within a key is the
@@ -19,6 +20,7 @@ namespace lora {
 
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteBatch = 16;  // keys per lane loaded together
 
 // Key of a linear-delta row: its slot, or n_keys (no delta) for slot < 0 and
 // for slot >= max_loras (which also sets LORA_DEV_ERR_SLOT).
@@ -77,12 +79,21 @@ __global__ void __launch_bounds__(kRouteThreads)
   const int b0 = min(n, warp * per), b1 = min(n, b0 + per);
   uint32_t errbits = 0;
   uint32_t* my = cnt + warp * nkb;
-  for (int base = b0; base < b1; base += 32) {
-    const int i = base + lane;
-    const int key = (i < b1) ? key_of(i, errbits) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (key >= 0 && lane == __ffs(peers) - 1) my[key] += __popc(peers);
-    __syncwarp();
+  // kRouteBatch keys per lane are loaded before any is used, so a warp's
+  // block costs one memory round trip per 32 * kRouteBatch items
+  for (int base = b0; base < b1; base += 32 * kRouteBatch) {
+    int keys[kRouteBatch];
+#pragma unroll
+    for (int u = 0; u < kRouteBatch; ++u) {
+      const int i = base + u * 32 + lane;
+      keys[u] = (i < b1) ? key_of(i, errbits) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kRouteBatch; ++u) {
+      const unsigned peers = __match_any_sync(0xffffffffu, keys[u]);
+      if (keys[u] >= 0 && lane == __ffs(peers) - 1) my[keys[u]] += __popc(peers);
+      __syncwarp();
+    }
   }
   errbits = __reduce_or_sync(0xffffffffu, errbits);
   if (lane == 0 && errbits) set_error(err_word, errbits);
@@ -116,18 +127,26 @@ __global__ void __launch_bounds__(kRouteThreads)
   if (tid == 0) seg_start[nkb] = n;
   __syncthreads();
 
-  for (int base = b0; base < b1; base += 32) {
-    const int i = base + lane;
+  for (int base = b0; base < b1; base += 32 * kRouteBatch) {
+    int keys[kRouteBatch];
     uint32_t dummy = 0;
-    const int key = (i < b1) ? key_of(i, dummy) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (key >= 0) {
-      const unsigned below = peers & ((1u << lane) - 1u);
-      perm[my[key] + __popc(below)] = i;
+#pragma unroll
+    for (int u = 0; u < kRouteBatch; ++u) {
+      const int i = base + u * 32 + lane;
+      keys[u] = (i < b1) ? key_of(i, dummy) : -1;
     }
-    __syncwarp();
-    if (key >= 0 && lane == __ffs(peers) - 1) my[key] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kRouteBatch; ++u) {
+      const int key = keys[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (key >= 0) {
+        const unsigned below = peers & ((1u << lane) - 1u);
+        perm[my[key] + __popc(below)] = base + u * 32 + lane;
+      }
+      __syncwarp();
+      if (key >= 0 && lane == __ffs(peers) - 1) my[key] += __popc(peers);
+      __syncwarp();
+    }
   }
 }
 

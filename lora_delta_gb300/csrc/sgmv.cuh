@@ -244,37 +244,48 @@ __global__ void __launch_bounds__(kSgmvThreads)
 }
 
 // ---------------------------------------------------------------- expand --
-// Persistent: CTA b walks a contiguous run of work items (tile, slice chunk
-// of 128 columns), tile-major.  h of a (tile, slice) is summed over the
-// shrink's planes and split into bf16 (hi, lo) once per run; the next item's
-// B chunk and out segments stream in (cp.async) while the current item's
-// MMAs and epilogue run.
-constexpr int kExpandThreads = 256;
+// Persistent CTA over a contiguous range of (tile, 128-column chunk) items,
+// one role per warp group:
+//   warps 0-3  producer: per item, the B chunk and the tile's out rows (16
+//              lanes per 256-byte row) by cp.async into the 128-byte-swizzled
+//              buffers of a ring of kStages stages; each thread's copies
+//              arrive on full[stage] as they land;
+//   warp 4     MMA: one thread issues the hi and lo MMAs of an item into one
+//              of two TMEM accumulators and commits to acc_full[acc];
+//   warps 5-8  epilogue, one TMEM lane quarter (32 tile rows) each: read the
+//              accumulator, fold scale * d into the staged out rows in place,
+//              write them back (16 lanes per 256-byte row) and release the
+//              stage.  They also rebuild h -- the shrink's
+//              planes summed, split into bf16 (hi, lo) -- when an item starts
+//              a new (tile, slice), after the last MMA that read the old h.
+// Stage buffers, accumulators and h are handed over through mbarriers; every
+// wait is bounded.
+constexpr int kExpandThreads = 288;
+constexpr int kExpandProducers = 128;  // threads of warps 0-3
+constexpr int kExpandMaxTiles = 8;  // tiles one expand CTA may span (the grid ensures it)
 
 template <int RMAX>
 struct ExpandSmem {
   static constexpr int KB = (RMAX + 63) / 64;
-  static constexpr int kNBuf = KB == 1 ? 3 : 2;       // copy buffers (copies run kNBuf-1 ahead)
-  static constexpr int kOStride = kExpandCols + 8;    // staged out row (elements)
-  static constexpr int kH = KB * kTileRows * 128;     // one of hi / lo
-  static constexpr int kB = KB * kExpandCols * 128;   // one B buffer
-  static constexpr int kO = kTileRows * kOStride * 2; // one out buffer
-  static constexpr int kTotal = 2 * kH + kNBuf * (kB + kO) + 1024;
+  static constexpr int kStages = KB == 1 ? 3 : 2;
+  static constexpr int kH = KB * kTileRows * 128;          // one of hi / lo
+  static constexpr int kB = KB * kExpandCols * 128;        // one B chunk
+  static constexpr int kHalf = kTileRows * 128;            // out rows, 64 columns
+  static constexpr int kO = 2 * kHalf;                     // out rows, 128 columns
+  static constexpr int kTotal = 2 * kH + kStages * (kB + kO) + 1024;
 };
-
-constexpr int kExpandMaxTiles = 8;  // tiles one expand CTA may span (the grid ensures it)
 
 template <int RMAX, class Tables>
 __global__ void __launch_bounds__(kExpandThreads, 1)
     sgmv_expand_kernel(const SgmvArgs a, const Tables tb, int n_chunks) {
   using SM = ExpandSmem<RMAX>;
-  constexpr int KB = SM::KB, NBUF = SM::kNBuf, D = NBUF - 1;
+  constexpr int KB = SM::KB, NS = SM::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ SlotView vt[kExpandMaxTiles];   // adapter tables of each tile's key
+  __shared__ SlotView vt[kExpandMaxTiles];  // adapter tables of each tile's key
   __shared__ SgmvTile tiles_s[kExpandMaxTiles];
   __shared__ int orow_map[kExpandMaxTiles][kTileRows];  // out row of each tile row
   __shared__ uint32_t taddr_s;
-  __shared__ __align__(8) uint64_t mma_bar[2];
+  __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS], accf_bar[2], acce_bar[2], h_bar;
   cudaGridDependencySynchronize();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int total = *a.n_tiles * n_chunks;
@@ -284,14 +295,15 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   const int t_first = w0 / n_chunks;
   const int n_my_tiles = (w1 - 1) / n_chunks - t_first + 1;
   if (n_my_tiles > kExpandMaxTiles) {  // the launch sizes the grid so that this cannot be
-    if (threadIdx.x == 0) set_error(a.err, LORA_DEV_ERR_INTERNAL);
+    if (tid == 0) set_error(a.err, LORA_DEV_ERR_INTERNAL);
     return;
   }
   uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint8_t* hhi = smem;
   uint8_t* hlo = hhi + SM::kH;
-  uint8_t* bsm = hlo + SM::kH;  // [NBUF][KB][kExpandCols rows][128 B]
-  __nv_bfloat16* osm = reinterpret_cast<__nv_bfloat16*>(bsm + NBUF * SM::kB);  // [NBUF][128][kOStride]
+  uint8_t* stage0 = hlo + SM::kH;  // stage s: B chunk [KB][128][128 B], then out [2][128][128 B]
+  auto stage_b = [&](int s) { return stage0 + (size_t)s * (SM::kB + SM::kO); };
+  auto stage_o = [&](int s) { return stage0 + (size_t)s * (SM::kB + SM::kO) + SM::kB; };
   const int R = a.R;
   if (tid < n_my_tiles) {  // this CTA's tiles and their tables
     const SgmvTile t = a.tiles[t_first + tid];
@@ -300,24 +312,31 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     tb.resolve(t.key, a.sl.S, kModeFused, vt[tid], bad);
     if (bad) set_error(a.err, bad);
   }
-  if (tid == 0) {
-    mbar_init(&mma_bar[0], 1);
-    mbar_init(&mma_bar[1], 1);
-    fence_barrier_init();
-  }
   for (int i = tid; i < n_my_tiles * kTileRows; i += kExpandThreads) {
     const int lt = i / kTileRows, r = i - lt * kTileRows;
     const SgmvTile t = a.tiles[t_first + lt];
     orow_map[lt][r] = r < t.rows ? (int)tb.out_row(a.perm[t.pos0 + r]) : 0;
   }
-  if (warp == 0) tc::tmem_alloc(&taddr_s, 2 * kExpandCols);  // two accumulators
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], kExpandProducers);  // every producer thread's copies
+      mbar_init(&empty_bar[s], 4);  // the 4 epilogue warps
+    }
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(&accf_bar[c], 1);  // MMA commit
+      mbar_init(&acce_bar[c], 4);  // the 4 epilogue warps
+    }
+    mbar_init(&h_bar, 128);  // every epilogue thread
+    fence_barrier_init();
+  }
+  if (warp == 4) tc::tmem_alloc(&taddr_s, 2 * kExpandCols);  // two accumulators
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t taddr = taddr_s;
 
   // Item w: (tile, slice j, first column c0, width nc) from arithmetic and the
-  // preloaded tables; every thread computes it itself.
+  // preloaded tables; every role computes it itself.
   struct Item {
     int lt, j, ja, c0, nc;
   };
@@ -335,182 +354,195 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     it.nc = min(kExpandCols, a.sl.width[j] - it.c0);
     return it;
   };
-
-  // Copies of item w into buffer buf: its B chunk (swizzled; only the K
-  // columns the MMAs read) and its out segments (16 lanes per 256-byte row).
-  auto prepare = [&](int w, int buf) {
-    const Item it = item_of(w);
-    if (it.ja < 0 || it.nc <= 0) return;
-    const __nv_bfloat16* bsrc = vt[it.lt].B[it.j] + (size_t)it.c0 * R;
-    uint8_t* bb = bsm + (size_t)buf * SM::kB;
-    const int cpr = (R + 15) >> 4 << 1;  // 16-byte pieces per B row the K-steps read
-    for (int i = tid; i < kExpandCols * cpr; i += kExpandThreads) {
-      const int c = i / cpr, k = (i - c * cpr) * 8;
-      const bool ok = c < it.nc && k < R;  // zeros past the slice's end and past R
-      cp_async16_zfill(bb + (size_t)(k >> 6) * kExpandCols * 128 + tc::sw128_offset(c, k & 63),
-                       ok ? bsrc + (size_t)c * R + k : bsrc, ok);
-    }
-    if (a.add_inputs) {
-      const int rows = tiles_s[it.lt].rows, vpr = it.nc >> 3;
-      const __nv_bfloat16* src = a.out + a.sl.off[it.j] + it.c0;
-      __nv_bfloat16* ob = osm + (size_t)buf * kTileRows * SM::kOStride;
-#pragma unroll
-      for (int u = 0; u < kTileRows * 16 / kExpandThreads; ++u) {
-        const int i = tid + u * kExpandThreads, r = i >> 4, g = i & 15;
-        if (r < rows && g < vpr)
-          cp_async16(ob + r * SM::kOStride + g * 8,
-                     src + (int64_t)orow_map[it.lt][r] * a.ld_out + g * 8);
-      }
-    }
-  };
-
-  // h of (tile, slice): sum of the shrink's planes, split into bf16 (hi, lo)
-  auto load_h = [&](const SgmvTile& t, int ja) {
-    for (int i = tid; i < KB * kTileRows * 8; i += kExpandThreads) {
-      const int kb = i / (kTileRows * 8), rem = i - kb * kTileRows * 8;
-      const int r = rem >> 3, g = rem & 7, k = kb * 64 + g * 8;
-      float hv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) hv[e] = 0.0f;
-      if (r < t.rows && k < R) {
-        const float* hp = a.hbuf + (size_t)(t.pos0 + r) * a.hs + ja * R + k;
-        for (int sp = 0; sp < a.ksplit; ++sp) {
-          const float4 h0 = *reinterpret_cast<const float4*>(hp + sp * a.plane);
-          const float4 h1 = *reinterpret_cast<const float4*>(hp + sp * a.plane + 4);
-          hv[0] += h0.x; hv[1] += h0.y; hv[2] += h0.z; hv[3] += h0.w;
-          hv[4] += h1.x; hv[5] += h1.y; hv[6] += h1.z; hv[7] += h1.w;
-        }
-      }
-      uint4 hi, lo;
-      split_bf16x2(hv[0], hv[1], hi.x, lo.x);
-      split_bf16x2(hv[2], hv[3], hi.y, lo.y);
-      split_bf16x2(hv[4], hv[5], hi.z, lo.z);
-      split_bf16x2(hv[6], hv[7], hi.w, lo.w);
-      const uint32_t off = (uint32_t)kb * kTileRows * 128 + tc::sw128_offset(r, g * 8);
-      *reinterpret_cast<uint4*>(hhi + off) = hi;
-      *reinterpret_cast<uint4*>(hlo + off) = lo;
-    }
-  };
-
-  int h_lt = -1, h_ja = -1;
-  uint32_t commits[2] = {0u, 0u};  // MMA commits per accumulator (phase parity)
   bool ok = true;
-  // issue the MMAs of item u (its copies have landed), into accumulator u & 1
-  auto issue_mma = [&](int u) {
-    const int buf = (u - w0) % NBUF, acc = (u - w0) & 1;
-    const Item it = item_of(u);
-    if (it.ja < 0 || it.nc <= 0) return;
-    if (it.lt != h_lt || it.ja != h_ja) {
-      // the previous item's MMAs read h: let them finish before it is replaced
-      if (tid == 0 && u > w0) {
-        const int pacc = (u - 1 - w0) & 1;
-        if (commits[pacc] && !mbar_wait_bounded(&mma_bar[pacc], (commits[pacc] - 1) & 1)) ok = false;
+
+  if (warp < 4) {
+    // ---------------------------------------------------------- producer --
+    const int cpr = (R + 15) >> 4 << 1;  // 16-byte pieces per B row that the K-steps read
+    for (int w = w0; w < w1 && ok; ++w) {
+      const int i = w - w0, s = i % NS, k = i / NS;
+      const Item it = item_of(w);
+      // the epilogue released this stage's previous use
+      if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1)) {
+        ok = false;
+        break;
       }
-      __syncthreads();
-      load_h(tiles_s[it.lt], it.ja);
-      h_lt = it.lt;
-      h_ja = it.ja;
-      fence_proxy_async_smem();
-      __syncthreads();
+      if (it.ja >= 0 && it.nc > 0) {
+        const __nv_bfloat16* bsrc = vt[it.lt].B[it.j] + (size_t)it.c0 * R;
+        uint8_t* bb = stage_b(s);
+        for (int idx = tid; idx < kExpandCols * cpr; idx += kExpandProducers) {
+          const int c = idx / cpr, kk = (idx - c * cpr) * 8;
+          const bool v = c < it.nc && kk < R;  // zeros past the slice's end and past R
+          cp_async16_zfill(bb + (size_t)(kk >> 6) * kExpandCols * 128 + tc::sw128_offset(c, kk & 63),
+                           v ? bsrc + (size_t)c * R + kk : bsrc, v);
+        }
+        if (a.add_inputs) {
+          // out rows: piece p (8 columns) of row r at half p / 8, chunk (p mod 8) ^ (r mod 8)
+          const SgmvTile& t = tiles_s[it.lt];
+          const int* om = orow_map[it.lt];
+          const __nv_bfloat16* src = a.out + a.sl.off[it.j] + it.c0;
+          uint8_t* ob = stage_o(s);
+          const int p = tid & 15, np = it.nc >> 3;
+          for (int r = tid >> 4; r < t.rows; r += kExpandProducers / 16)
+            if (p < np)
+              cp_async16(ob + (p >> 3) * SM::kHalf + r * 128 + (((p & 7) ^ (r & 7)) << 4),
+                         src + (int64_t)om[r] * a.ld_out + p * 8);
+        }
+      }
+      cp_async_arrive(&full_bar[s]);
     }
-    if (tid == 0) {
-      tc::fence_after_sync();
-      const int N = (it.nc + 15) / 16 * 16;
-      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, N);
+    // nothing may land in this CTA's shared memory after it exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == 4) {
+    // --------------------------------------------------------------- MMA --
+    if (lane == 0) {
       const int ksteps = (R + 15) / 16;
-      const uint8_t* bb = bsm + (size_t)buf * SM::kB;
-      const uint32_t dt = taddr + (uint32_t)(acc * kExpandCols);
-      for (int pass = 0; pass < 2; ++pass) {
-        const uint8_t* hsrc = pass == 0 ? hhi : hlo;
-        for (int s = 0; s < ksteps; ++s) {
-          const int kb = s >> 2, ks = s & 3;
-          const uint32_t ha = smem_addr(hsrc + (size_t)kb * kTileRows * 128) + ks * 32;
-          const uint32_t ba = smem_addr(bb + (size_t)kb * kExpandCols * 128) + ks * 32;
-          tc::mma_bf16(dt, tc::sw128_desc(ha), tc::sw128_desc(ba), idesc,
-                       (pass > 0 || s > 0) ? 1u : 0u);
+      int na = 0, hv = -1, h_lt = -1, h_ja = -1;  // active items so far; h version
+      for (int w = w0; w < w1; ++w) {
+        const int i = w - w0, s = i % NS, k = i / NS;
+        const Item it = item_of(w);
+        if (it.ja < 0 || it.nc <= 0) continue;
+        if (it.lt != h_lt || it.ja != h_ja) {  // the epilogue rebuilds h first
+          ++hv;
+          h_lt = it.lt;
+          h_ja = it.ja;
+          if (!mbar_wait_bounded(&h_bar, hv & 1)) {
+            ok = false;
+            break;
+          }
+        }
+        const int acc = na & 1, u = na >> 1;
+        if (!mbar_wait_bounded(&full_bar[s], k & 1) ||
+            (u > 0 && !mbar_wait_bounded(&acce_bar[acc], (u - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        fence_proxy_async_smem();  // the B chunk came through cp.async (generic proxy)
+        const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, (it.nc + 15) / 16 * 16);
+        const uint8_t* bb = stage_b(s);
+        const uint32_t dt = taddr + (uint32_t)(acc * kExpandCols);
+        for (int pass = 0; pass < 2; ++pass) {
+          const uint8_t* hsrc = pass == 0 ? hhi : hlo;
+          for (int st = 0; st < ksteps; ++st) {
+            const int kb = st >> 2, ks = st & 3;
+            const uint32_t ha = smem_addr(hsrc + (size_t)kb * kTileRows * 128) + ks * 32;
+            const uint32_t ba = smem_addr(bb + (size_t)kb * kExpandCols * 128) + ks * 32;
+            tc::mma_bf16(dt, tc::sw128_desc(ha), tc::sw128_desc(ba), idesc,
+                         (pass > 0 || st > 0) ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&accf_bar[acc]);
+        ++na;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3;       // TMEM lane quarter of this warp (warps 5..8)
+    const int r = q * 32 + lane;  // this thread's tile row
+    const int et = tid - 160;     // index among the 128 epilogue threads
+    int na = 0, h_lt = -1, h_ja = -1;
+    for (int w = w0; w < w1 && ok; ++w) {
+      const int i = w - w0, s = i % NS, k = i / NS;
+      const Item it = item_of(w);
+      if (it.ja < 0 || it.nc <= 0) {
+        // nothing to compute: release the stage once its (empty) fill completed
+        if (!mbar_wait_bounded(&full_bar[s], k & 1)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        continue;
+      }
+      const SgmvTile& t = tiles_s[it.lt];
+      if (it.lt != h_lt || it.ja != h_ja) {
+        // every MMA that read the old h has completed (its accumulator was
+        // waited for below), and the MMA thread waits for this arrival
+        h_lt = it.lt;
+        h_ja = it.ja;
+        for (int e = et; e < KB * kTileRows * 8; e += 128) {
+          const int kb = e / (kTileRows * 8), rem = e - kb * kTileRows * 8;
+          const int hr = rem >> 3, g = rem & 7, kk = kb * 64 + g * 8;
+          float hv[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) hv[x] = 0.0f;
+          if (hr < t.rows && kk < R) {
+            const float* hp = a.hbuf + (size_t)(t.pos0 + hr) * a.hs + it.ja * R + kk;
+            for (int sp = 0; sp < a.ksplit; ++sp) {
+              const float4 h0 = *reinterpret_cast<const float4*>(hp + sp * a.plane);
+              const float4 h1 = *reinterpret_cast<const float4*>(hp + sp * a.plane + 4);
+              hv[0] += h0.x; hv[1] += h0.y; hv[2] += h0.z; hv[3] += h0.w;
+              hv[4] += h1.x; hv[5] += h1.y; hv[6] += h1.z; hv[7] += h1.w;
+            }
+          }
+          uint4 hi, lo;
+          split_bf16x2(hv[0], hv[1], hi.x, lo.x);
+          split_bf16x2(hv[2], hv[3], hi.y, lo.y);
+          split_bf16x2(hv[4], hv[5], hi.z, lo.z);
+          split_bf16x2(hv[6], hv[7], hi.w, lo.w);
+          const uint32_t off = (uint32_t)kb * kTileRows * 128 + tc::sw128_offset(hr, g * 8);
+          *reinterpret_cast<uint4*>(hhi + off) = hi;
+          *reinterpret_cast<uint4*>(hlo + off) = lo;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&h_bar);
+      }
+      const int acc = na & 1, u = na >> 1;
+      if (!mbar_wait_bounded(&accf_bar[acc], u & 1) || !mbar_wait_bounded(&full_bar[s], k & 1)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      // fold scale * d into the staged out rows (in place; 16-byte chunk c of
+      // row r sits at chunk c ^ (r mod 8))
+      const float sc = vt[it.lt].scale;
+      uint8_t* ob = stage_o(s);
+      const int nh = it.nc > 64 ? 2 : 1;
+      for (int hf = 0; hf < nh; ++hf) {
+        float d[64];
+        tc::tmem_ld64(taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kExpandCols + hf * 64),
+                      d);
+        uint8_t* rowp = ob + hf * SM::kHalf + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4* p = reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4));
+          const uint4 o = a.add_inputs ? *p : make_uint4(0, 0, 0, 0);
+          uint4 res;
+          res.x = pack_bf16x2(bf16lo(o.x) + sc * d[8 * c + 0], bf16hi(o.x) + sc * d[8 * c + 1]);
+          res.y = pack_bf16x2(bf16lo(o.y) + sc * d[8 * c + 2], bf16hi(o.y) + sc * d[8 * c + 3]);
+          res.z = pack_bf16x2(bf16lo(o.z) + sc * d[8 * c + 4], bf16hi(o.z) + sc * d[8 * c + 5]);
+          res.w = pack_bf16x2(bf16lo(o.w) + sc * d[8 * c + 6], bf16hi(o.w) + sc * d[8 * c + 7]);
+          *p = res;
         }
       }
-      tc::mma_commit(&mma_bar[acc]);
-    }
-    ++commits[acc];
-  };
-
-  for (int i = 0; i < D; ++i) {
-    if (w0 + i < w1) prepare(w0 + i, i);
-    cp_async_commit();
-  }
-  cp_async_wait<D - 1>();  // copies of item w0
-  fence_proxy_async_smem();
-  __syncthreads();
-  issue_mma(w0);
-
-  for (int w = w0; w < w1; ++w) {
-    const int buf = (w - w0) % NBUF, acc = (w - w0) & 1;
-    // copies D items ahead (into the buffers item w-1 has released)
-    if (w + D < w1) prepare(w + D, (w + D - w0) % NBUF);
-    cp_async_commit();
-    // MMAs of item w+1 run while item w's epilogue reads its accumulator
-    if (w + 1 < w1) {
-      cp_async_wait<D - 1>();
-      fence_proxy_async_smem();
-      __syncthreads();
-      issue_mma(w + 1);
-    }
-    const Item it = item_of(w);
-    if (it.ja < 0 || it.nc <= 0) continue;  // uniform; no shared state read below
-    // (item w+1 uses the other accumulator, so the last commit on `acc` is item w's)
-    if (tid == 0 && !mbar_wait_bounded(&mma_bar[acc], (commits[acc] - 1) & 1)) ok = false;
-    const bool mma_ok = __syncthreads_and(ok);
-    tc::fence_after_sync();
-    // epilogue: warp (q, half) owns rows 32q.. and columns [64 half, 64 half + 64).
-    // Lane = row while the accumulator is read and combined with the staged
-    // out (in place, in shared memory); then 8 lanes per row for the stores.
-    const int rows = tiles_s[it.lt].rows;
-    const int q = warp & 3, half = warp >> 2, cbeg = half * 64;
-    __nv_bfloat16* ob = osm + (size_t)buf * kTileRows * SM::kOStride;
-    if (cbeg < it.nc) {  // uniform across the warp
-      const int r = q * 32 + lane;
-      const float sc = vt[it.lt].scale;
-      float d[64];
-      tc::tmem_ld64(taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kExpandCols + cbeg), d);
-      __nv_bfloat16* srow = ob + r * SM::kOStride;
-#pragma unroll
-      for (int cc = 0; cc < 64; cc += 8) {
-        const int c = cbeg + cc;
-        if (c < it.nc) {
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (a.add_inputs) o = *reinterpret_cast<const uint4*>(srow + c);
-          uint4 res;
-          res.x = pack_bf16x2(bf16lo(o.x) + sc * d[cc + 0], bf16hi(o.x) + sc * d[cc + 1]);
-          res.y = pack_bf16x2(bf16lo(o.y) + sc * d[cc + 2], bf16hi(o.y) + sc * d[cc + 3]);
-          res.z = pack_bf16x2(bf16lo(o.z) + sc * d[cc + 4], bf16hi(o.z) + sc * d[cc + 5]);
-          res.w = pack_bf16x2(bf16lo(o.w) + sc * d[cc + 6], bf16hi(o.w) + sc * d[cc + 7]);
-          *reinterpret_cast<uint4*>(srow + c) = res;
-        }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[acc]);  // accumulator free for the MMA thread
+      // write back the warp's 32 rows: 16 lanes per 256-byte row, two rows per step
+      const int* om = orow_map[it.lt];
+      __nv_bfloat16* dst0 = a.out + a.sl.off[it.j] + it.c0;
+      const int p = lane & 15, np = it.nc >> 3;
+#pragma unroll 4
+      for (int u = 0; u < 16; ++u) {  // (rows written by other lanes: the __syncwarp above)
+        const int rr = q * 32 + u * 2 + (lane >> 4);
+        if (rr < t.rows && p < np)
+          *reinterpret_cast<uint4*>(dst0 + (int64_t)om[rr] * a.ld_out + p * 8) =
+              *reinterpret_cast<const uint4*>(ob + (p >> 3) * SM::kHalf + rr * 128 +
+                                              (((p & 7) ^ (rr & 7)) << 4));
       }
       __syncwarp();
-      if (mma_ok) {
-        __nv_bfloat16* dst = a.out + a.sl.off[it.j] + it.c0;
-        const int g = lane & 7, c = cbeg + g * 8;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int rr = q * 32 + u * 4 + (lane >> 3);
-          if (rr < rows && c < it.nc)
-            *reinterpret_cast<uint4*>(dst + (int64_t)orow_map[it.lt][rr] * a.ld_out + c) =
-                *reinterpret_cast<const uint4*>(ob + rr * SM::kOStride + c);
-        }
-      }
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // stage read: free for the producer
+      ++na;
     }
-    tc::fence_before_sync();
-    __syncthreads();  // accumulator `acc` and item w's buffers free
+    __syncwarp();
   }
-  cp_async_wait<0>();
-  if (!ok && tid == 0) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
+  if (!ok) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(taddr, 2 * kExpandCols);
+  if (warp == 4) tc::tmem_dealloc(taddr, 2 * kExpandCols);
 }
-
 inline int sgmv_shrink_smem(int sr_max) {
   const int N = (sr_max + 15) / 16 * 16;
   return kShrinkStages * (kTileRows * 128 + N * 128) + 1024;

@@ -186,6 +186,17 @@ def test_bad_slot_sets_error_and_skips(ld, di, oracle):
     check_linear(oracle, case, got, err)
 
 
+def test_bad_slot_is_flagged_when_slot_0_adapts_nothing(ld, di, oracle):
+    """The out-of-range check does not depend on slot 0 having an adapter."""
+    seq = np.array([1, 5, -1, 1, 2, 2, 1, 2], dtype=np.int32)
+    case = inputs.linear_case(19, n=8, k_in=64, widths=(32,), max_loras=3, max_rank=8,
+                              ranks=[8, 8, 8], alpha=8.0, seq_slot=seq,
+                              adapted=[[False], [True], [True]])
+    got, err, _ = run_fused(ld, di, case)
+    assert err & 1
+    check_linear(oracle, case, got, err)
+
+
 def test_misaligned_table_entry_is_skipped_and_flagged(ld, di, oracle):
     case = inputs.linear_case(10, n=16, k_in=64, widths=(32,), max_loras=2, max_rank=8,
                               ranks=[8, 8], alpha=8.0, seq_slot=np.array([0, 1] * 8, np.int32))
