@@ -246,22 +246,26 @@ __global__ void __launch_bounds__(kSgmvThreads)
 // ---------------------------------------------------------------- expand --
 // Persistent CTA over a contiguous range of (tile, 128-column chunk) items,
 // one role per warp group:
-//   warps 0-3  producer: per item, the B chunk and the tile's out rows (16
+//   producer warps: per item, the B chunk and the tile's out rows (16
 //              lanes per 256-byte row) by cp.async into the 128-byte-swizzled
 //              buffers of a ring of kStages stages; each thread's copies
 //              arrive on full[stage] as they land;
-//   warp 4     MMA: one thread issues the hi and lo MMAs of an item into one
+//   MMA warp:  one thread issues the hi and lo MMAs of an item into one
 //              of two TMEM accumulators and commits to acc_full[acc];
-//   warps 5-8  epilogue, one TMEM lane quarter (32 tile rows) each: read the
-//              accumulator, fold scale * d into the staged out rows in place,
-//              write them back (16 lanes per 256-byte row) and release the
-//              stage.  They also rebuild h -- the shrink's
+//   8 epilogue warps, one (TMEM lane quarter = 32 tile rows, 64-column
+//              half) each: read the accumulator, fold scale * d into the
+//              staged out rows in place, write them back (8 lanes per
+//              128-byte row segment) and release the stage.  They also
+//              rebuild h -- the shrink's
 //              planes summed, split into bf16 (hi, lo) -- when an item starts
 //              a new (tile, slice), after the last MMA that read the old h.
 // Stage buffers, accumulators and h are handed over through mbarriers; every
 // wait is bounded.
-constexpr int kExpandThreads = 288;
-constexpr int kExpandProducers = 128;  // threads of warps 0-3
+constexpr int kExpandProducers = 256;  // warps [0, kMmaWarp)
+constexpr int kMmaWarp = kExpandProducers / 32;
+constexpr int kExpandEpilogue = 256;   // warps (kMmaWarp, ...]
+constexpr int kEpiWarp0 = kMmaWarp + 1;
+constexpr int kExpandThreads = kExpandProducers + 32 + kExpandEpilogue;
 constexpr int kExpandMaxTiles = 8;  // tiles one expand CTA may span (the grid ensures it)
 
 template <int RMAX>
@@ -320,16 +324,16 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full_bar[s], kExpandProducers);  // every producer thread's copies
-      mbar_init(&empty_bar[s], 4);  // the 4 epilogue warps
+      mbar_init(&empty_bar[s], kExpandEpilogue / 32);  // the epilogue warps
     }
     for (int c = 0; c < 2; ++c) {
       mbar_init(&accf_bar[c], 1);  // MMA commit
-      mbar_init(&acce_bar[c], 4);  // the 4 epilogue warps
+      mbar_init(&acce_bar[c], kExpandEpilogue / 32);  // the epilogue warps
     }
-    mbar_init(&h_bar, 128);  // every epilogue thread
+    mbar_init(&h_bar, kExpandEpilogue);  // every epilogue thread
     fence_barrier_init();
   }
-  if (warp == 4) tc::tmem_alloc(&taddr_s, 2 * kExpandCols);  // two accumulators
+  if (warp == kMmaWarp) tc::tmem_alloc(&taddr_s, 2 * kExpandCols);  // two accumulators
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   };
   bool ok = true;
 
-  if (warp < 4) {
+  if (warp < kMmaWarp) {
     // ---------------------------------------------------------- producer --
     const int cpr = (R + 15) >> 4 << 1;  // 16-byte pieces per B row that the K-steps read
     for (int w = w0; w < w1 && ok; ++w) {
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     }
     // nothing may land in this CTA's shared memory after it exits
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA --
     if (lane == 0) {
       const int ksteps = (R + 15) / 16;
@@ -439,9 +443,10 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue --
-    const int q = warp & 3;       // TMEM lane quarter of this warp (warps 5..8)
-    const int r = q * 32 + lane;  // this thread's tile row
-    const int et = tid - 160;     // index among the 128 epilogue threads
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int hf = (warp - kEpiWarp0) >> 2;  // 64-column half
+    const int r = q * 32 + lane;             // this thread's tile row
+    const int et = tid - kEpiWarp0 * 32;     // index among the epilogue threads
     int na = 0, h_lt = -1, h_ja = -1;
     for (int w = w0; w < w1 && ok; ++w) {
       const int i = w - w0, s = i % NS, k = i / NS;
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         // waited for below), and the MMA thread waits for this arrival
         h_lt = it.lt;
         h_ja = it.ja;
-        for (int e = et; e < KB * kTileRows * 8; e += 128) {
+        for (int e = et; e < KB * kTileRows * 8; e += kExpandEpilogue) {
           const int kb = e / (kTileRows * 8), rem = e - kb * kTileRows * 8;
           const int hr = rem >> 3, g = rem & 7, kk = kb * 64 + g * 8;
           float hv[8];
@@ -495,16 +500,16 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      // fold scale * d into the staged out rows (in place; 16-byte chunk c of
-      // row r sits at chunk c ^ (r mod 8))
+      // fold scale * d into this warp's rows and half of the staged out tile
+      // (in place; 16-byte chunk c of row r sits at chunk c ^ (r mod 8))
       const float sc = vt[it.lt].scale;
-      uint8_t* ob = stage_o(s);
-      const int nh = it.nc > 64 ? 2 : 1;
-      for (int hf = 0; hf < nh; ++hf) {
+      uint8_t* hb = stage_o(s) + hf * SM::kHalf;
+      const bool mine = hf * 64 < it.nc;  // uniform across the warp
+      if (mine) {
         float d[64];
         tc::tmem_ld64(taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kExpandCols + hf * 64),
                       d);
-        uint8_t* rowp = ob + hf * SM::kHalf + r * 128;
+        uint8_t* rowp = hb + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint4* p = reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4));
@@ -520,17 +525,18 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar[acc]);  // accumulator free for the MMA thread
-      // write back the warp's 32 rows: 16 lanes per 256-byte row, two rows per step
-      const int* om = orow_map[it.lt];
-      __nv_bfloat16* dst0 = a.out + a.sl.off[it.j] + it.c0;
-      const int p = lane & 15, np = it.nc >> 3;
+      if (mine) {
+        // write back the warp's 32 row segments: 8 lanes per 128 bytes, 4 rows per step
+        const int* om = orow_map[it.lt];
+        __nv_bfloat16* dst0 = a.out + a.sl.off[it.j] + it.c0 + hf * 64;
+        const int p = lane & 7, np = min(8, (it.nc - hf * 64) >> 3);
 #pragma unroll 4
-      for (int u = 0; u < 16; ++u) {  // (rows written by other lanes: the __syncwarp above)
-        const int rr = q * 32 + u * 2 + (lane >> 4);
-        if (rr < t.rows && p < np)
-          *reinterpret_cast<uint4*>(dst0 + (int64_t)om[rr] * a.ld_out + p * 8) =
-              *reinterpret_cast<const uint4*>(ob + (p >> 3) * SM::kHalf + rr * 128 +
-                                              (((p & 7) ^ (rr & 7)) << 4));
+        for (int v = 0; v < 8; ++v) {  // (rows written by other lanes: the __syncwarp above)
+          const int rr = q * 32 + v * 4 + (lane >> 3);
+          if (rr < t.rows && p < np)
+            *reinterpret_cast<uint4*>(dst0 + (int64_t)om[rr] * a.ld_out + p * 8) =
+                *reinterpret_cast<const uint4*>(hb + rr * 128 + ((p ^ (rr & 7)) << 4));
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);  // stage read: free for the producer
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   if (!ok) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 4) tc::tmem_dealloc(taddr, 2 * kExpandCols);
+  if (warp == kMmaWarp) tc::tmem_dealloc(taddr, 2 * kExpandCols);
 }
 inline int sgmv_shrink_smem(int sr_max) {
   const int N = (sr_max + 15) / 16 * 16;
