@@ -57,10 +57,32 @@ struct KernelAttrCache {
   std::mutex mu;
   std::unordered_map<uint64_t, int> smem;  // (kernel, device) -> bytes granted
   std::unordered_map<uint64_t, bool> cluster;
+  std::unordered_map<uint64_t, int> occupancy;  // (kernel, device, smem) -> CTAs per SM
 };
 KernelAttrCache& attr_cache() {
   static KernelAttrCache c;
   return c;
+}
+
+// Resident CTAs per SM of `kernel` with `threads` threads and `smem_bytes` of
+// dynamic shared memory (after prepare_kernel); at least 1.
+template <class K>
+int ctas_per_sm(K kernel, int threads, int smem_bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  const uint64_t id = (reinterpret_cast<uint64_t>(reinterpret_cast<const void*>(kernel)) << 6) ^
+                      ((uint64_t)dev << 40) ^ (uint64_t)smem_bytes;
+  KernelAttrCache& c = attr_cache();
+  std::lock_guard<std::mutex> lock(c.mu);
+  auto it = c.occupancy.find(id);
+  if (it != c.occupancy.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, (size_t)smem_bytes) !=
+          cudaSuccess ||
+      n < 1)
+    n = 1;
+  c.occupancy[id] = n;
+  return n;
 }
 
 template <class K>
@@ -314,18 +336,22 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   s.hbuf = w.hbuf;
   s.hs = (d.sr_max + 15) / 16 * 16;
   const int max_tiles = max_sgmv_tiles(d.n, n_keys);
+  // the shrink runs persistent: `slots` resident CTAs walk (tile, split)
+  // items; the tile kernel picks the split from the true tile count, within
+  // the planes the workspace holds
+  const int shrink_smem = sgmv_shrink_smem(d.sr_max);
+  if (prepare_kernel(sgmv_shrink_kernel<Tables>, shrink_smem, false) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  const int slots = ctas_per_sm(sgmv_shrink_kernel<Tables>, kShrinkThreads, shrink_smem) * sm_count();
+  int ks_max = kMaxKSplit;
   {
-    // split k so that about two CTAs per SM run the shrink, within the planes
-    // the workspace holds
     const int nkb = (d.k_in + 63) / 64;
-    int ks = (2 * sm_count() + max_tiles - 1) / max_tiles;
-    if (ks > kMaxKSplit) ks = kMaxKSplit;
-    if (ks > nkb) ks = nkb;
+    if (ks_max > nkb) ks_max = nkb;
     const size_t head = ws_head_bytes(d.n, n_keys), plane = ws_plane_bytes(d.n, s.hs);
     const int fit = w.bytes > head ? (int)((w.bytes - head) / plane) : 0;
-    if (ks > fit) ks = fit;
-    if (ks < 1) ks = 1;
-    s.ksplit = ks;
+    if (ks_max > fit) ks_max = fit;
+    if (ks_max < 1) ks_max = 1;
+    s.ksplit = w.n_tiles + 1;
     s.plane = (int64_t)(plane / 4);
   }
   s.R = d.R;
@@ -351,16 +377,15 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, sgmv_tiles_kernel, (const int32_t*)d.seg_start, n_keys,
-                                     min_rows, w.tiles, w.n_tiles, max_tiles);
+                                     min_rows, w.tiles, w.n_tiles, max_tiles, slots, ks_max);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   // shrink
   {
     auto kernel = sgmv_shrink_kernel<Tables>;
-    const int smem = sgmv_shrink_smem(d.sr_max);
-    if ((e = prepare_kernel(kernel, smem, false)) != cudaSuccess) return LORA_ERR_CUDA;
-    cfg.gridDim = dim3((unsigned)(max_tiles * s.ksplit));
-    cfg.blockDim = dim3(kSgmvThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
+    const int64_t most = (int64_t)max_tiles * ks_max;  // items at most
+    cfg.gridDim = dim3((unsigned)(most < slots ? most : slots));
+    cfg.blockDim = dim3(kShrinkThreads);
+    cfg.dynamicSmemBytes = (size_t)shrink_smem;
     if ((e = cudaLaunchKernelEx(&cfg, kernel, s, tb)) != cudaSuccess) return LORA_ERR_CUDA;
   }
   // expand: persistent, one CTA per SM

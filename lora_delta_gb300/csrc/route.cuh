@@ -81,6 +81,10 @@ __global__ void __launch_bounds__(kRouteThreads)
   uint32_t* my = cnt + warp * nkb;
   // kRouteBatch keys per lane are loaded before any is used, so a warp's
   // block costs one memory round trip per 32 * kRouteBatch items
+  // With at most 32 key values, lane k counts key k from one ballot per key
+  // value; otherwise __match_any_sync groups the lanes by key.
+  const bool few = nkb <= 32;
+  uint32_t mine = 0;  // (few keys) this lane's count of key `lane`
   for (int base = b0; base < b1; base += 32 * kRouteBatch) {
     int keys[kRouteBatch];
 #pragma unroll
@@ -90,11 +94,19 @@ __global__ void __launch_bounds__(kRouteThreads)
     }
 #pragma unroll
     for (int u = 0; u < kRouteBatch; ++u) {
-      const unsigned peers = __match_any_sync(0xffffffffu, keys[u]);
-      if (keys[u] >= 0 && lane == __ffs(peers) - 1) my[keys[u]] += __popc(peers);
-      __syncwarp();
+      if (few) {
+        for (int kk = 0; kk < nkb; ++kk) {
+          const unsigned m = __ballot_sync(0xffffffffu, keys[u] == kk);
+          if (lane == kk) mine += __popc(m);
+        }
+      } else {
+        const unsigned peers = __match_any_sync(0xffffffffu, keys[u]);
+        if (keys[u] >= 0 && lane == __ffs(peers) - 1) my[keys[u]] += __popc(peers);
+        __syncwarp();
+      }
     }
   }
+  if (few && lane < nkb) my[lane] = mine;
   errbits = __reduce_or_sync(0xffffffffu, errbits);
   if (lane == 0 && errbits) set_error(err_word, errbits);
   __syncthreads();
@@ -127,6 +139,8 @@ __global__ void __launch_bounds__(kRouteThreads)
   if (tid == 0) seg_start[nkb] = n;
   __syncthreads();
 
+  uint32_t next = (few && lane < nkb) ? my[lane] : 0u;  // (few keys) next position of key `lane`
+  const unsigned lt = (1u << lane) - 1u;
   for (int base = b0; base < b1; base += 32 * kRouteBatch) {
     int keys[kRouteBatch];
     uint32_t dummy = 0;
@@ -138,14 +152,23 @@ __global__ void __launch_bounds__(kRouteThreads)
 #pragma unroll
     for (int u = 0; u < kRouteBatch; ++u) {
       const int key = keys[u];
-      const unsigned peers = __match_any_sync(0xffffffffu, key);
-      if (key >= 0) {
-        const unsigned below = peers & ((1u << lane) - 1u);
-        perm[my[key] + __popc(below)] = base + u * 32 + lane;
+      if (few) {
+        unsigned peers = 0, cnt = 0;
+        for (int kk = 0; kk < nkb; ++kk) {
+          const unsigned m = __ballot_sync(0xffffffffu, key == kk);
+          if (key == kk) peers = m;
+          if (lane == kk) cnt = __popc(m);
+        }
+        const uint32_t at = __shfl_sync(0xffffffffu, next, key < 0 ? 0 : key);
+        if (key >= 0) perm[at + __popc(peers & lt)] = base + u * 32 + lane;
+        next += cnt;
+      } else {
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (key >= 0) perm[my[key] + __popc(peers & lt)] = base + u * 32 + lane;
+        __syncwarp();
+        if (key >= 0 && lane == __ffs(peers) - 1) my[key] += __popc(peers);
+        __syncwarp();
       }
-      __syncwarp();
-      if (key >= 0 && lane == __ffs(peers) - 1) my[key] += __popc(peers);
-      __syncwarp();
     }
   }
 }

@@ -29,7 +29,6 @@
 namespace lora {
 
 constexpr int kTileRows = 128;      // MMA M
-constexpr int kSgmvThreads = 128;   // 4 warps = the 4 TMEM lane quarters
 constexpr int kShrinkStages = 4;
 constexpr int kExpandCols = 128;    // output columns per expand CTA
 constexpr int kSgmvMaxSR = 256;     // MMA N of the shrink
@@ -41,9 +40,12 @@ struct SgmvTile {
 // ---------------------------------------------------------------- tiles --
 // Tile list from the routing kernel's cluster starts: keys with at least
 // min_rows rows get ceil(rows / 128) tiles.  One CTA.
+// n_tiles[0] = tiles, n_tiles[1] = k-splits of the shrink: enough (tile,
+// split) items to fill the `slots` resident shrink CTAs, at most ks_max.
 __global__ void __launch_bounds__(256)
     sgmv_tiles_kernel(const int32_t* __restrict__ seg_start, int n_keys, int min_rows,
-                      SgmvTile* __restrict__ tiles, int* __restrict__ n_tiles, int max_tiles) {
+                      SgmvTile* __restrict__ tiles, int* __restrict__ n_tiles, int max_tiles,
+                      int slots, int ks_max) {
   __shared__ int warp_sums[8];
   cudaGridDependencySynchronize();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -72,7 +74,11 @@ __global__ void __launch_bounds__(256)
       ++base;
     }
   }
-  if (tid == 255) *n_tiles = min(base, max_tiles);
+  if (tid == 255) {
+    const int nt = min(base, max_tiles);
+    n_tiles[0] = nt;
+    n_tiles[1] = nt > 0 ? max(1, min(ks_max, slots / nt)) : 1;
+  }
 }
 
 struct SgmvArgs {
@@ -84,9 +90,9 @@ struct SgmvArgs {
   const int32_t* perm;
   const SgmvTile* tiles;
   const int* n_tiles;
-  float* hbuf;    // [ksplit planes][sorted rows, hs] fp32 partial sums of h
-  int64_t plane;  // elements per plane
-  int ksplit;     // k-splits of the shrink (planes to sum)
+  float* hbuf;         // [ksplit planes][sorted rows, hs] fp32 partial sums of h
+  int64_t plane;       // elements per plane
+  const int* ksplit;   // k-splits of the shrink (planes to sum), set by the tile kernel
   int hs;         // row stride of hbuf (S * R rounded up to 16)
   int R;
   Slices sl;
@@ -106,141 +112,153 @@ __device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gsr
 // CTA (tile, split): the tile's 128 rows against the key's A rows over the
 // split's share of the 64-wide k-blocks; the fp32 partial goes to plane
 // `split` of hbuf (the expand sums the planes in order, so the result does not
-// depend on scheduling).
+// depend on scheduling).  Producer warps stream each k-block of the gathered
+// x rows and of the A rows by cp.async into a ring of swizzled stages and
+// arrive on full[stage] as their copies land; one thread issues the MMAs of a
+// block and commits them to empty[stage].  No CTA-wide barrier inside the
+// loop.  Afterwards warps 0-3 (the TMEM lane quarters) write the accumulator.
+constexpr int kShrinkProducers = 256;
+constexpr int kShrinkMmaWarp = kShrinkProducers / 32;
+constexpr int kShrinkThreads = kShrinkProducers + 32;
+
 template <class Tables>
-__global__ void __launch_bounds__(kSgmvThreads)
+__global__ void __launch_bounds__(kShrinkThreads)
     sgmv_shrink_kernel(const SgmvArgs a, const Tables tb) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ SlotView v;
   __shared__ uint32_t taddr_s;
-  __shared__ __align__(8) uint64_t mma_bar[kShrinkStages];
-  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ __align__(8) uint64_t full_bar[kShrinkStages], empty_bar[kShrinkStages], done_bar;
   __shared__ const __nv_bfloat16* xrow_s[kTileRows];
   __shared__ const __nv_bfloat16* arow_s[kSgmvMaxSR];
   cudaGridDependencySynchronize();
-  const int tile_id = blockIdx.x / a.ksplit, split = blockIdx.x - tile_id * a.ksplit;
-  if (tile_id >= *a.n_tiles) return;
-  const SgmvTile tile = a.tiles[tile_id];
+  const int ks = *a.ksplit, n_items = *a.n_tiles * ks;
+  if ((int)blockIdx.x >= n_items) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   if (tid == 0) {
-    uint32_t bad = 0;
-    tb.resolve(tile.key, a.sl.S, kModeFused, v, bad);
-    for (int s = 0; s < kShrinkStages; ++s) mbar_init(&mma_bar[s], 1);
+    for (int s = 0; s < kShrinkStages; ++s) {
+      mbar_init(&full_bar[s], kShrinkProducers);  // every producer thread's copies
+      mbar_init(&empty_bar[s], 1);                // the MMA commit
+    }
     mbar_init(&done_bar, 1);
     fence_barrier_init();
   }
-  for (int r = tid; r < kTileRows; r += kSgmvThreads)
-    xrow_s[r] = r < tile.rows ? a.x + tb.x_row(a.perm[tile.pos0 + r]) * a.ld_x : nullptr;
-  __syncthreads();
-  const int R = a.R;
-  const int SRa = v.nact * R;
-  if (SRa == 0) return;
-  const int N = (SRa + 15) / 16 * 16;
-  for (int t = tid; t < N; t += kSgmvThreads) {
-    const __nv_bfloat16* p = nullptr;
-    if (t < SRa) {
-      const int jj = t / R, q = t - jj * R;
-      p = v.A[v.act_slice[jj]] + (size_t)q * a.k_in;
-    }
-    arow_s[t] = p;
-  }
-  uint32_t ncols = 32;
-  while ((int)ncols < N) ncols <<= 1;
-  if (warp == 0) tc::tmem_alloc(&taddr_s, ncols);
-
-  const int xbytes = kTileRows * 128, abytes = N * 128;
-  const int stage_bytes = xbytes + abytes;  // multiple of 1024
-  const int nkb_all = (a.k_in + 63) / 64;
-  const int kb_begin = (int)((int64_t)nkb_all * split / a.ksplit);
-  const int kb_end = (int)((int64_t)nkb_all * (split + 1) / a.ksplit);
-  const int nkb = kb_end - kb_begin;
-  __syncthreads();  // row pointers visible
-
-  // one 64-wide k-block of the gathered x rows and of the A rows, zero-filled
-  // past the tile's rows, the key's pairs and k_in
-  auto load_block = [&](int kb, int s) {
-    uint8_t* xs = smem + (size_t)s * stage_bytes;
-    uint8_t* as = xs + xbytes;
-    const int kbase = (kb_begin + kb) * 64;
-    for (int i = tid; i < (kTileRows + N) * 8; i += kSgmvThreads) {
-      const int r = i >> 3, c = i & 7;
-      const int k = kbase + c * 8;
-      const bool kin = k < a.k_in;
-      if (r < kTileRows) {
-        const __nv_bfloat16* row = xrow_s[r];
-        const bool ok = kin && row != nullptr;
-        cp_async16_zfill(xs + tc::sw128_offset(r, c * 8), ok ? row + k : a.x, ok);
-      } else {
-        const int t = r - kTileRows;
-        const __nv_bfloat16* row = arow_s[t];
-        const bool ok = kin && row != nullptr;
-        cp_async16_zfill(as + tc::sw128_offset(t, c * 8), ok ? row + k : a.x, ok);
-      }
-    }
-  };
-
-  for (int s = 0; s < kShrinkStages - 1; ++s) {
-    if (s < nkb) load_block(s, s);
-    cp_async_commit();
-  }
+  if (warp == 0) tc::tmem_alloc(&taddr_s, kSgmvMaxSR);  // room for any N
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t taddr = taddr_s;
-  const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, N);
+  const int R = a.R;
+  const int nkb_all = (a.k_in + 63) / 64;
+  int kbg = 0;  // k-blocks streamed through the stage ring so far
+  int nd = 0;   // items committed to done_bar so far
   bool ok = true;
-  for (int kb = 0; kb < nkb; ++kb) {
-    const int s = kb % kShrinkStages;
-    cp_async_wait<kShrinkStages - 2>();  // block kb landed (this thread's copies)
-    fence_proxy_async_smem();            // make them visible to the tensor core
-    if (tid == 0 && kb >= 1) {           // the MMAs of block kb-1 released its stage
-      const int sp = (kb - 1) % kShrinkStages;
-      if (!mbar_wait_bounded(&mma_bar[sp], (uint32_t)(((kb - 1) / kShrinkStages) & 1))) ok = false;
+  // persistent: items (tile, split), tile-major
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int tile_id = item / ks, split = item - tile_id * ks;
+    const SgmvTile tile = a.tiles[tile_id];
+    // the previous item is done (accumulator read, row tables no longer used);
+    // after a timed-out wait anywhere in the CTA, all threads stop together
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {
+      uint32_t bad = 0;
+      tb.resolve(tile.key, a.sl.S, kModeFused, v, bad);
+      if (bad) set_error(a.err, bad);
+    }
+    for (int r = tid; r < kTileRows; r += kShrinkThreads)
+      xrow_s[r] = r < tile.rows ? a.x + tb.x_row(a.perm[tile.pos0 + r]) * a.ld_x : nullptr;
+    __syncthreads();
+    const int SRa = v.nact * R;
+    if (SRa == 0) continue;  // (uniform) no active slice: no planes for this tile
+    const int N = (SRa + 15) / 16 * 16;
+    for (int t = tid; t < N; t += kShrinkThreads) {
+      const __nv_bfloat16* p = nullptr;
+      if (t < SRa) {
+        const int jj = t / R, q = t - jj * R;
+        p = v.A[v.act_slice[jj]] + (size_t)q * a.k_in;
+      }
+      arow_s[t] = p;
     }
     __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-      const uint32_t xa = smem_addr(smem + (size_t)s * stage_bytes);
-      const uint32_t aa = xa + xbytes;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(taddr, tc::sw128_desc(xa + ks * 32), tc::sw128_desc(aa + ks * 32), idesc,
-                     (kb > 0 || ks > 0) ? 1u : 0u);
-      tc::mma_commit(&mma_bar[s]);
-    }
-    const int nxt = kb + kShrinkStages - 1;  // refill the stage block kb-1 used
-    if (nxt < nkb) load_block(nxt, nxt % kShrinkStages);
-    cp_async_commit();
-  }
-  if (tid == 0) {
-    tc::mma_commit(&done_bar);
-    if (!mbar_wait_bounded(&done_bar, 0)) ok = false;
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-  tc::fence_after_sync();
-  const bool all_ok = __syncthreads_and(ok);
-  if (!all_ok && tid == 0) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
-  // epilogue: TMEM row r -> plane `split` of hbuf, row pos0 + r, columns [0, SRa)
-  if (all_ok) {
-    const int r = warp * 32 + lane;
-    float* dst = a.hbuf + (size_t)split * a.plane + (size_t)(tile.pos0 + r) * a.hs;
-    for (int c = 0; c < N; c += 16) {
-      float vals[16];
-      tc::tmem_ld16(taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, vals);
-      if (r < tile.rows) {
-#pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          if (c + i < SRa)
-            *reinterpret_cast<float4*>(dst + c + i) =
-                make_float4(vals[i], vals[i + 1], vals[i + 2], vals[i + 3]);
+    const int xbytes = kTileRows * 128;
+    const int stage_bytes = xbytes + N * 128;  // multiple of 1024
+    const int kb_begin = (int)((int64_t)nkb_all * split / ks);
+    const int nkb = (int)((int64_t)nkb_all * (split + 1) / ks) - kb_begin;
+    if (warp < kShrinkMmaWarp) {
+      // -------------------------------------------------------- producer --
+      // piece (row, 16-byte chunk c) of a block: rows of x then of A,
+      // zero-filled past the tile's rows, the key's pairs and k_in
+      const int c = tid & 7;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int g = kbg + kb, s = g % kShrinkStages, k = g / kShrinkStages;
+        if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        uint8_t* xs = smem + (size_t)s * stage_bytes;
+        uint8_t* as = xs + xbytes;
+        const int kk = (kb_begin + kb) * 64 + c * 8;
+        const bool kin = kk < a.k_in;
+        for (int r = tid >> 3; r < kTileRows + N; r += kShrinkProducers / 8) {
+          const __nv_bfloat16* row = r < kTileRows ? xrow_s[r] : arow_s[r - kTileRows];
+          const bool v_ok = kin && row != nullptr;
+          uint8_t* dst = r < kTileRows ? xs + tc::sw128_offset(r, c * 8)
+                                       : as + tc::sw128_offset(r - kTileRows, c * 8);
+          cp_async16_zfill(dst, v_ok ? row + kk : a.x, v_ok);
+        }
+        cp_async_arrive(&full_bar[s]);
       }
+    } else if (lane == 0) {
+      // ------------------------------------------------------------- MMA --
+      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, N);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int g = kbg + kb, s = g % kShrinkStages, k = g / kShrinkStages;
+        if (!mbar_wait_bounded(&full_bar[s], k & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        fence_proxy_async_smem();  // the block came through cp.async (generic proxy)
+        const uint32_t xa = smem_addr(smem + (size_t)s * stage_bytes);
+        const uint32_t aa = xa + xbytes;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          tc::mma_bf16(taddr, tc::sw128_desc(xa + q * 32), tc::sw128_desc(aa + q * 32), idesc,
+                       (kb > 0 || q > 0) ? 1u : 0u);
+        tc::mma_commit(&empty_bar[s]);  // the stage is free once these MMAs are done
+      }
+      tc::mma_commit(&done_bar);
     }
+    kbg += nkb;
+    // -------------------------------------------------------------- epilogue
+    // warps 0-3: TMEM lane quarter q = tile rows 32q.., columns [0, SRa) ->
+    // plane `split` of hbuf, row pos0 + r
+    if (warp < 4) {
+      if (!mbar_wait_bounded(&done_bar, nd & 1)) ok = false;
+      tc::fence_after_sync();
+      const int r = warp * 32 + lane;
+      float* dst = a.hbuf + (size_t)split * a.plane + (size_t)(tile.pos0 + r) * a.hs;
+      if (ok)
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float vals[16];
+          tc::tmem_ld16(taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, vals);
+          if (r < tile.rows) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              if (c0 + i < SRa)
+                *reinterpret_cast<float4*>(dst + c0 + i) =
+                    make_float4(vals[i], vals[i + 1], vals[i + 2], vals[i + 3]);
+          }
+        }
+      tc::fence_before_sync();
+    }
+    ++nd;
   }
+  if (warp < kShrinkMmaWarp) asm volatile("cp.async.wait_all;" ::: "memory");
+  if (!ok) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(taddr, ncols);
+  if (warp == 0) tc::tmem_dealloc(taddr, kSgmvMaxSR);
 }
 
 // ---------------------------------------------------------------- expand --
@@ -293,6 +311,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   cudaGridDependencySynchronize();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int total = *a.n_tiles * n_chunks;
+  const int ksplit = *a.ksplit;  // planes of h to sum
   const int w0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int w1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   if (w0 >= w1) return;
@@ -475,7 +494,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
           for (int x = 0; x < 8; ++x) hv[x] = 0.0f;
           if (hr < t.rows && kk < R) {
             const float* hp = a.hbuf + (size_t)(t.pos0 + hr) * a.hs + it.ja * R + kk;
-            for (int sp = 0; sp < a.ksplit; ++sp) {
+            for (int sp = 0; sp < ksplit; ++sp) {
               const float4 h0 = *reinterpret_cast<const float4*>(hp + sp * a.plane);
               const float4 h1 = *reinterpret_cast<const float4*>(hp + sp * a.plane + 4);
               hv[0] += h0.x; hv[1] += h0.y; hv[2] += h0.z; hv[3] += h0.w;
