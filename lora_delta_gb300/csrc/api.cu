@@ -65,7 +65,7 @@ KernelAttrCache& attr_cache() {
 }
 
 // Resident CTAs per SM of `kernel` with `threads` threads and `smem_bytes` of
-// dynamic shared memory (after prepare_kernel); at least 1.
+// dynamic shared memory, ignoring tensor memory; at least 1.
 template <class K>
 int ctas_per_sm(K kernel, int threads, int smem_bytes) {
   int dev = 0;
@@ -76,11 +76,27 @@ int ctas_per_sm(K kernel, int threads, int smem_bytes) {
   std::lock_guard<std::mutex> lock(c.mu);
   auto it = c.occupancy.find(id);
   if (it != c.occupancy.end()) return it->second;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, (size_t)smem_bytes) !=
-          cudaSuccess ||
-      n < 1)
-    n = 1;
+  // From the SM's shared memory, registers and threads (the runtime's
+  // occupancy query answers 1 for any kernel that allocates tensor memory,
+  // although CTAs whose columns fit share an SM).
+  int n = 1;
+  cudaFuncAttributes fa;
+  int smem_sm = 0, resv = 0, regs_sm = 0, thr_sm = 0;
+  if (cudaFuncGetAttributes(&fa, kernel) == cudaSuccess &&
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
+          cudaSuccess &&
+      cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) ==
+          cudaSuccess &&
+      cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) == cudaSuccess) {
+    const long per_cta = (long)smem_bytes + (long)fa.sharedSizeBytes + resv;
+    const int warps = (threads + 31) / 32;
+    const int regs = ((fa.numRegs * 32 + 255) / 256) * 256 * warps;  // 256-register granules
+    n = (int)(smem_sm / per_cta);
+    if (regs > 0 && regs_sm / regs < n) n = regs_sm / regs;
+    if (thr_sm / (warps * 32) < n) n = thr_sm / (warps * 32);
+    if (n < 1) n = 1;
+  }
   c.occupancy[id] = n;
   return n;
 }
@@ -98,6 +114,10 @@ cudaError_t prepare_kernel(K kernel, int smem_bytes, bool big_cluster) {
     auto it = c.smem.find(id);
     if (it == c.smem.end() || it->second < smem_bytes) {
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+      if (e != cudaSuccess) return e;
+      // all of the unified L1 as shared memory, so that several such CTAs fit
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
       c.smem[id] = smem_bytes;
     }
@@ -342,7 +362,10 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   const int shrink_smem = sgmv_shrink_smem(d.sr_max);
   if (prepare_kernel(sgmv_shrink_kernel<Tables>, shrink_smem, false) != cudaSuccess)
     return LORA_ERR_CUDA;
-  const int slots = ctas_per_sm(sgmv_shrink_kernel<Tables>, kShrinkThreads, shrink_smem) * sm_count();
+  // (each shrink CTA holds kSgmvMaxSR of the SM's 512 TMEM columns)
+  int per_sm = ctas_per_sm(sgmv_shrink_kernel<Tables>, kShrinkThreads, shrink_smem);
+  if (per_sm > 512 / kSgmvMaxSR) per_sm = 512 / kSgmvMaxSR;
+  const int slots = per_sm * sm_count();
   int ks_max = kMaxKSplit;
   {
     const int nkb = (d.k_in + 63) / 64;
