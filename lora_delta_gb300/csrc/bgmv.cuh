@@ -592,26 +592,39 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       cluster_arrive();  // partials in place
       cluster_wait();
       {
+        // 4 lanes per 4-entry group; lane qq reads peers qq, qq + 4, qq + 8,
+        // qq + 12 (all in flight together), then two xor-shuffles add the
+        // lanes: one round trip, the same summation order in every CTA
         const uint32_t rx_addr = smem_addr(Rx);
-        int r = r_first, p = p_first;
-        for (int e = tid * 4; e < nel; e += kThreads * 4) {
+        const int ngrp = nel >> 2, qq = lane & 3;
+        for (int gb = (tid >> 2); gb - (lane >> 2) < ngrp; gb += kThreads / 4) {
+          const bool valid = gb < ngrp;  // (the warp's lanes stay together)
+          const int e = 4 * (valid ? gb : 0);
+          const int r = e / SRa, p = e - r * SRa;
           const uint32_t addr = rx_addr + 4u * (uint32_t)(r * SR16 + p);
-          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-          for (int c = 0; c < ncta; ++c) {  // rank order
-            const float4 v = dsmem_ld_f32x4(dsmem_map(addr, (uint32_t)c));
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
+          float4 part[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = qq + 4 * u;
+            part[u] = (valid && c < ncta) ? dsmem_ld_f32x4(dsmem_map(addr, (uint32_t)c))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          *reinterpret_cast<float4*>(H + r * SR16 + p) = sum;
-          p += dp;
-          r += dr;
-          if (p >= SRa) {
-            p -= SRa;
-            ++r;
+          float4 v = part[0];
+#pragma unroll
+          for (int u = 1; u < 4; ++u) {
+            v.x += part[u].x;
+            v.y += part[u].y;
+            v.z += part[u].z;
+            v.w += part[u].w;
           }
+#pragma unroll
+          for (int off = 1; off < 4; off <<= 1) {
+            v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
+            v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
+            v.z += __shfl_xor_sync(0xffffffffu, v.z, off);
+            v.w += __shfl_xor_sync(0xffffffffu, v.w, off);
+          }
+          if (valid && qq == 0) *reinterpret_cast<float4*>(H + r * SR16 + p) = v;
         }
       }
       cluster_arrive_relaxed();  // done reading the peers' Rx (waited on later)
