@@ -345,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
   if (v.nact == 0 && !slot_check) return;  // the same in every CTA of the cluster
 
   // ---- the key's rows, in ascending row order (warp 0) -----------------
+  // Warp 0 also starts the first pass's x / out copies when they are few
+  // (decode-sized: at most 8 per lane); larger ones are left to every warp.
+  const bool warp0_copies =
+      early && kRowsPerPass * (min(a.kst, k_hi - k_lo) / 8 + (o_staged ? a.cpc / 8 : 0)) <= 256;
   if (warp == 0) {
     int total = 0, s0 = 0;
     if (a.perm) {
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       rows_base_s = s0;
     }
     __syncwarp();
-    if (early && total > 0 && total >= a.min_rows && total < a.max_rows) {
+    if (warp0_copies && total > 0 && total >= a.min_rows && total < a.max_rows) {
       const int* rows0 = a.perm ? a.perm + s0 : rows_s;
       const int nr0 = min(kRowsPerPass, total);
       copy_x_rows(a, tb, rows0, nr0, k_lo, min(a.kst, k_hi - k_lo), Xs, stride, lane, 1);
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       if (b_staged && !b_loaded) copy_b_rows(a, v, cb, ce, Bs, tid);
       b_loaded = b_staged;
       if (o_staged) {
-        if (!(early && p0 == 0))  // (the first pass's were started by warp 0)
+        if (!(warp0_copies && p0 == 0))  // (the first pass's were started by warp 0)
           copy_out_rows(a, tb, v, prow, nr, cb, ce, Os, plan.o_stride, tid);
       } else if (warp == 2)
         prefetch_out(a, tb, v, prow, nr, cb, ce, lane);
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       // ---- copies of the first two stages ---------------------------------
       if (nst > 0) {
         if (!skip_a0) copy_a_rows(a, v, SRa, k_lo, min(a.kst, k_hi - k_lo), As, stride, tid);
-        if (!(early && p0 == 0))  // (the first pass's were started by warp 0)
+        if (!(warp0_copies && p0 == 0))  // (the first pass's were started by warp 0)
           copy_x_rows(a, tb, prow, nr, k_lo, min(a.kst, k_hi - k_lo), Xs, stride, tid);
         cp_async_commit();
         if (nst > 1) {
