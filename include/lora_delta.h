@@ -134,6 +134,19 @@ int lora_route(int32_t *perm, int32_t *seg_start, const int32_t *seq_slot, int n
                int max_loras, uint32_t *err_word, lora_stream_t stream);
 
 /*
+ * lora_route_with_scratch -- lora_route for large batches: the same output
+ * (bit for bit), but batches of 2048 rows or more are sorted by many CTAs in
+ * chunks of 1024 rows, using a caller-provided scratch buffer of
+ * lora_route_scratch_size(n, max_loras) bytes (16-byte aligned; one count per
+ * (chunk, slot)).  Errors as lora_route, plus LORA_ERR_WORKSPACE when the
+ * scratch is missing or too small.  ([punica] prefill_metadata.)
+ */
+size_t lora_route_scratch_size(int n, int max_loras);
+int lora_route_with_scratch(int32_t *perm, int32_t *seg_start, const int32_t *seq_slot, int n,
+                            int max_loras, void *scratch, size_t scratch_bytes,
+                            uint32_t *err_word, lora_stream_t stream);
+
+/*
  * lora_shrink -- [punica] add_shrink: for every slice j and routed row i
  *   h[j, i, q] += scale_s * sum_k x[i, k] * A_j,s[q, k],   q < R
  * ("y[i] += (x @ lora_a_stacked[i]) * scale" with A in the [R, k_in] pool

@@ -22,7 +22,8 @@ from ._lib import LibraryMissing, lib, status_string
 
 __all__ = [
     "LoraError", "LibraryMissing", "LoraPool", "lora_scale", "lora_pool_pack",
-    "lora_workspace_size", "lora_workspace_min_size", "lora_route", "lora_shrink", "lora_expand", "lora_delta_fused",
+    "lora_workspace_size", "lora_workspace_min_size", "lora_route", "lora_route_scratch_size",
+    "lora_route_with_scratch", "lora_shrink", "lora_expand", "lora_delta_fused",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_get_error", "new_error_word",
     "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes",
 ]
@@ -176,6 +177,30 @@ def lora_route(seq_slot: torch.Tensor, max_loras: int, perm=None, seg_start=None
                  if seg_start is None else seg_start)
     _check("lora_route", lib().lora_route(_ptr(perm), _ptr(seg_start), _ptr(seq_slot), n,
                                           int(max_loras), _ptr(err), _stream(stream)))
+    return perm, seg_start
+
+
+def lora_route_scratch_size(n: int, max_loras: int) -> int:
+    return int(lib().lora_route_scratch_size(int(n), int(max_loras)))
+
+
+def lora_route_with_scratch(seq_slot: torch.Tensor, max_loras: int, scratch=None, perm=None,
+                            seg_start=None, err=None, stream=None):
+    """lora_route for large batches (many CTAs), with caller scratch; same result."""
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n = seq_slot.numel()
+    dev = seq_slot.device
+    perm = torch.empty(max(n, 1), dtype=torch.int32, device=dev) if perm is None else perm
+    seg_start = (torch.empty(max_loras + 2, dtype=torch.int32, device=dev)
+                 if seg_start is None else seg_start)
+    nbytes = lora_route_scratch_size(n, max_loras)
+    if scratch is None:
+        scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _check("lora_route_with_scratch",
+           lib().lora_route_with_scratch(_ptr(perm), _ptr(seg_start), _ptr(seq_slot), n,
+                                         int(max_loras), _ptr(scratch),
+                                         scratch.numel() * scratch.element_size(), _ptr(err),
+                                         _stream(stream)))
     return perm, seg_start
 
 

@@ -26,6 +26,8 @@ SIGNATURES = {
     "lora_workspace_size": (_sz, [_i, _i, _i, _i]),
     "lora_workspace_min_size": (_sz, [_i, _i, _i, _i]),
     "lora_route": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp]),
+    "lora_route_scratch_size": (_sz, [_i, _i]),
+    "lora_route_with_scratch": (_i, [_vp, _vp, _vp, _i, _i, _vp, _sz, _vp, _vp]),
     "lora_shrink": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "lora_expand": (_i, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz,
                          _vp, _vp]),

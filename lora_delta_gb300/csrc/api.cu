@@ -244,8 +244,46 @@ int launch_route(const KeyFn& kf, int n, int n_keys, int32_t* perm, int32_t* seg
   return cuda_status(cudaGetLastError());
 }
 
+// Scratch of the chunked sort: one count per (chunk, key).
+constexpr int kRouteChunkedMinItems = 2 * kRouteChunk;  // below this one CTA sorts
+size_t route_counts_bytes(int n, int n_keys) {
+  const int nb = (n + kRouteChunk - 1) / kRouteChunk;
+  return (size_t)(nb > 0 ? nb : 1) * (size_t)(n_keys + 1) * 4;
+}
+
+// The routing sort with scratch `counts` (route_counts_bytes): chunked over
+// many CTAs for large batches, one CTA otherwise.
+template <class KeyFn>
+int launch_route_scratch(const KeyFn& kf, int n, int n_keys, int32_t* perm, int32_t* seg_start,
+                         uint32_t* counts, uint32_t* err, cudaStream_t stream) {
+  if (n < kRouteChunkedMinItems) return launch_route(kf, n, n_keys, perm, seg_start, err, stream);
+  const int nb = (n + kRouteChunk - 1) / kRouteChunk;
+  const int smem_c = (int)route_smem_bytes(n_keys), smem_s = (int)route_chunk_smem_bytes(n_keys);
+  auto kc = route_count_kernel<KeyFn>;
+  auto ks = route_scatter_kernel<KeyFn>;
+  if (prepare_kernel(kc, smem_c, false) != cudaSuccess ||
+      prepare_kernel(ks, smem_s, false) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  kc<<<nb, kRouteThreads, smem_c, stream>>>(kf, n, n_keys, counts, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nb);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = (size_t)smem_s;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, ks, kf, n, n_keys, (const uint32_t*)counts, perm, seg_start);
+  return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
 // Workspace layout: perm [n] int32 | seg_start [n_keys + 2] int32 |
-// SGMV tiles [max_tiles] + their count | h of the tensor-core path [n, hs] fp32.
+// SGMV tiles [max_tiles] + their count | routing-sort counts [chunks, n_keys + 1] |
+// h planes of the tensor-core path [planes][n, hs] fp32.
 int max_sgmv_tiles(int n, int n_keys) { return n / kTileRows + (n_keys < n ? n_keys : n) + 1; }
 
 struct Workspace {
@@ -253,6 +291,7 @@ struct Workspace {
   int32_t* seg;
   SgmvTile* tiles;
   int* n_tiles;
+  uint32_t* rcounts;
   float* hbuf;
   size_t bytes;  // size of the whole buffer
 };
@@ -263,7 +302,8 @@ constexpr int kMaxKSplit = 8;  // planes of the SGMV shrink's partial h
 size_t ws_head_bytes(int n, int n_keys) {
   const int nn = n > 0 ? n : 1;
   return align256((size_t)nn * 4) + align256((size_t)(n_keys + 2) * 4) +
-         align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16);
+         align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16) +
+         align256(route_counts_bytes(nn, n_keys));
 }
 size_t ws_plane_bytes(int n, int hs) { return align256((size_t)(n > 0 ? n : 1) * hs * 4); }
 
@@ -296,6 +336,8 @@ Workspace carve(void* ws, int n, int n_keys) {
   w.n_tiles = reinterpret_cast<int*>(p);
   w.tiles = reinterpret_cast<SgmvTile*>(p + 16);
   p += align256((size_t)max_sgmv_tiles(nn, n_keys) * sizeof(SgmvTile) + 16);
+  w.rcounts = reinterpret_cast<uint32_t*>(p);
+  p += align256(route_counts_bytes(nn, n_keys));
   w.hbuf = reinterpret_cast<float*>(p);
   w.bytes = 0;
   return w;
@@ -334,7 +376,8 @@ int prepare_rows(DeltaArgs& a, const int32_t* seq_slot, int n, int max_loras, in
   if (!workspace || ws_bytes < ws_bytes_for(n, max_loras, hs)) return LORA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
   const Workspace w = carve(workspace, n, max_loras);
-  const int rc = launch_route(SlotKey{seq_slot, max_loras}, n, max_loras, w.perm, w.seg, err, stream);
+  const int rc = launch_route_scratch(SlotKey{seq_slot, max_loras}, n, max_loras, w.perm, w.seg,
+                                      w.rcounts, err, stream);
   if (rc) return rc;
   a.perm = w.perm;
   a.seg_start = w.seg;
@@ -521,6 +564,24 @@ size_t lora_workspace_min_size(int n, int S, int R, int max_loras) {
   return ws_bytes_for(n, max_loras, (S * R + 15) / 16 * 16, 1);
 }
 
+size_t lora_route_scratch_size(int n, int max_loras) {
+  if (n < 0 || max_loras < 1) return 0;
+  return route_counts_bytes(n, max_loras);
+}
+
+int lora_route_with_scratch(int32_t* perm, int32_t* seg_start, const int32_t* seq_slot, int n,
+                            int max_loras, void* scratch, size_t scratch_bytes,
+                            uint32_t* err_word, lora_stream_t stream) {
+  if (n < 0 || !seg_start || (n > 0 && (!perm || !seq_slot))) return LORA_ERR_ARG;
+  int rc = check_max_loras(max_loras);
+  if (rc) return rc;
+  if (!scratch || scratch_bytes < route_counts_bytes(n, max_loras)) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(scratch) & 15u) != 0) return LORA_ERR_ALIGN;
+  return launch_route_scratch(SlotKey{seq_slot, max_loras}, n, max_loras, perm, seg_start,
+                              reinterpret_cast<uint32_t*>(scratch), err_word,
+                              (cudaStream_t)stream);
+}
+
 int lora_route(int32_t* perm, int32_t* seg_start, const int32_t* seq_slot, int n, int max_loras,
                uint32_t* err_word, lora_stream_t stream) {
   if (n < 0 || !seg_start || (n > 0 && (!perm || !seq_slot))) return LORA_ERR_ARG;
@@ -658,8 +719,8 @@ int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t
   const Workspace w = carve(workspace, n, n_keys);
   int32_t* perm = w.perm;
   int32_t* seg = w.seg;
-  rc = launch_route(MoeKey{topk_ids, lora_ids, top_k, E, num_loras}, n, n_keys, perm, seg,
-                    err_word, s);
+  rc = launch_route_scratch(MoeKey{topk_ids, lora_ids, top_k, E, num_loras}, n, n_keys, perm,
+                            seg, w.rcounts, err_word, s);
   if (rc) return rc;
 
   DeltaArgs a = {};

@@ -64,25 +64,17 @@ inline size_t route_smem_bytes(int n_keys) {
   return sizeof(uint32_t) * (size_t)kRouteWarps * (size_t)(n_keys + 1);
 }
 
-template <class KeyFn>
-__global__ void __launch_bounds__(kRouteThreads)
-    route_kernel(KeyFn key_of, int n, int n_keys, int32_t* __restrict__ perm,
-                 int32_t* __restrict__ seg_start, uint32_t* err_word) {
-  extern __shared__ uint32_t cnt[];  // [kRouteWarps][n_keys + 1]
-  __shared__ uint32_t warp_sums[kRouteWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nkb = n_keys + 1;
-  for (int i = tid; i < kRouteWarps * nkb; i += kRouteThreads) cnt[i] = 0;
-  __syncthreads();
+// Per-warp pieces shared by the one-CTA sort and the chunked sort.  A warp
+// owns the items [b0, b1) and reads kRouteBatch keys per lane before using
+// them (one memory round trip per 32 * kRouteBatch items).  With at most 32
+// key values, lane k counts key k from one ballot per key value; otherwise
+// __match_any_sync groups the lanes by key.
 
-  const int per = (n + kRouteWarps - 1) / kRouteWarps;
-  const int b0 = min(n, warp * per), b1 = min(n, b0 + per);
-  uint32_t errbits = 0;
-  uint32_t* my = cnt + warp * nkb;
-  // kRouteBatch keys per lane are loaded before any is used, so a warp's
-  // block costs one memory round trip per 32 * kRouteBatch items
-  // With at most 32 key values, lane k counts key k from one ballot per key
-  // value; otherwise __match_any_sync groups the lanes by key.
+// my[k] += number of items of key k in [b0, b1).
+template <class KeyFn>
+__device__ __forceinline__ void warp_count(const KeyFn& key_of, int b0, int b1, int nkb,
+                                           uint32_t* my, uint32_t& errbits) {
+  const int lane = threadIdx.x & 31;
   const bool few = nkb <= 32;
   uint32_t mine = 0;  // (few keys) this lane's count of key `lane`
   for (int base = b0; base < b1; base += 32 * kRouteBatch) {
@@ -106,39 +98,17 @@ __global__ void __launch_bounds__(kRouteThreads)
       }
     }
   }
-  if (few && lane < nkb) my[lane] = mine;
-  errbits = __reduce_or_sync(0xffffffffu, errbits);
-  if (lane == 0 && errbits) set_error(err_word, errbits);
-  __syncthreads();
+  if (few && lane < nkb) my[lane] += mine;
+  __syncwarp();
+}
 
-  // Block-wide exclusive scan over keys of the per-key totals; each thread
-  // owns a contiguous run of keys.
-  const int kpt = (nkb + kRouteThreads - 1) / kRouteThreads;
-  const int k0 = min(nkb, tid * kpt), k1 = min(nkb, k0 + kpt);
-  uint32_t tsum = 0;
-  for (int k = k0; k < k1; ++k)
-    for (int w = 0; w < kRouteWarps; ++w) tsum += cnt[w * nkb + k];
-  uint32_t incl = tsum;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  uint32_t run = incl - tsum;
-  for (int w = 0; w < warp; ++w) run += warp_sums[w];
-  for (int k = k0; k < k1; ++k) {
-    seg_start[k] = (int32_t)run;
-    for (int w = 0; w < kRouteWarps; ++w) {
-      const uint32_t c = cnt[w * nkb + k];
-      cnt[w * nkb + k] = run;
-      run += c;
-    }
-  }
-  if (tid == 0) seg_start[nkb] = n;
-  __syncthreads();
-
+// Scatter the items of [b0, b1) to perm; my[k] holds the next position of
+// key k and is advanced.
+template <class KeyFn>
+__device__ __forceinline__ void warp_scatter(const KeyFn& key_of, int b0, int b1, int nkb,
+                                             uint32_t* my, int32_t* __restrict__ perm) {
+  const int lane = threadIdx.x & 31;
+  const bool few = nkb <= 32;
   uint32_t next = (few && lane < nkb) ? my[lane] : 0u;  // (few keys) next position of key `lane`
   const unsigned lt = (1u << lane) - 1u;
   for (int base = b0; base < b1; base += 32 * kRouteBatch) {
@@ -171,6 +141,158 @@ __global__ void __launch_bounds__(kRouteThreads)
       }
     }
   }
+}
+
+// Block-wide exclusive scan over keys [0, nkb) of total(k); each thread owns
+// a contiguous run of keys; returns, in `first`, the scan value at this
+// thread's first key (k0) and in k0 / k1 its run.
+template <class TotalFn>
+__device__ __forceinline__ uint32_t block_scan_keys(int nkb, const TotalFn& total, int& k0,
+                                                    int& k1, uint32_t* warp_sums) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kpt = (nkb + kRouteThreads - 1) / kRouteThreads;
+  k0 = min(nkb, tid * kpt);
+  k1 = min(nkb, k0 + kpt);
+  uint32_t tsum = 0;
+  for (int k = k0; k < k1; ++k) tsum += total(k);
+  uint32_t incl = tsum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - tsum;
+  for (int w = 0; w < warp; ++w) run += warp_sums[w];
+  return run;
+}
+
+// One CTA sorts all n items: one contiguous block per warp.
+template <class KeyFn>
+__global__ void __launch_bounds__(kRouteThreads)
+    route_kernel(KeyFn key_of, int n, int n_keys, int32_t* __restrict__ perm,
+                 int32_t* __restrict__ seg_start, uint32_t* err_word) {
+  extern __shared__ uint32_t cnt[];  // [kRouteWarps][n_keys + 1]
+  __shared__ uint32_t warp_sums[kRouteWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nkb = n_keys + 1;
+  for (int i = tid; i < kRouteWarps * nkb; i += kRouteThreads) cnt[i] = 0;
+  __syncthreads();
+  const int per = (n + kRouteWarps - 1) / kRouteWarps;
+  const int b0 = min(n, warp * per), b1 = min(n, b0 + per);
+  uint32_t errbits = 0;
+  uint32_t* my = cnt + warp * nkb;
+  warp_count(key_of, b0, b1, nkb, my, errbits);
+  errbits = __reduce_or_sync(0xffffffffu, errbits);
+  if (lane == 0 && errbits) set_error(err_word, errbits);
+  __syncthreads();
+  int k0, k1;
+  uint32_t run = block_scan_keys(
+      nkb,
+      [&](int k) {
+        uint32_t t = 0;
+        for (int w = 0; w < kRouteWarps; ++w) t += cnt[w * nkb + k];
+        return t;
+      },
+      k0, k1, warp_sums);
+  for (int k = k0; k < k1; ++k) {
+    seg_start[k] = (int32_t)run;
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const uint32_t c = cnt[w * nkb + k];
+      cnt[w * nkb + k] = run;
+      run += c;
+    }
+  }
+  if (tid == 0) seg_start[nkb] = n;
+  __syncthreads();
+  warp_scatter(key_of, b0, b1, nkb, my, perm);
+}
+
+// ------------------------------------------------------- chunked sort ---
+// For large batches: chunks of kRouteChunk items, one CTA each, in two
+// kernels.  route_count_kernel writes chunk b's count of every key to
+// counts[b][key]; route_scatter_kernel scans those counts (key-major, then
+// chunk) into each chunk's starting position per key and scatters the chunk
+// exactly as the one-CTA kernel does.  Chunk-major, then warp, then lane
+// order: the same stable order.
+constexpr int kRouteChunk = 1024;
+constexpr int kRoutePerWarp = kRouteChunk / kRouteWarps;
+
+inline size_t route_chunk_smem_bytes(int n_keys) {
+  return sizeof(uint32_t) * ((size_t)kRouteWarps + 1) * (size_t)(n_keys + 1);
+}
+
+template <class KeyFn>
+__global__ void __launch_bounds__(kRouteThreads)
+    route_count_kernel(KeyFn key_of, int n, int n_keys, uint32_t* __restrict__ counts,
+                       uint32_t* err_word) {
+  extern __shared__ uint32_t cnt[];  // [kRouteWarps][n_keys + 1]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nkb = n_keys + 1;
+  for (int i = tid; i < kRouteWarps * nkb; i += kRouteThreads) cnt[i] = 0;
+  __syncthreads();
+  const int b0 = min(n, (int)blockIdx.x * kRouteChunk + warp * kRoutePerWarp);
+  const int b1 = min(n, b0 + kRoutePerWarp);
+  uint32_t errbits = 0;
+  warp_count(key_of, b0, b1, nkb, cnt + warp * nkb, errbits);
+  errbits = __reduce_or_sync(0xffffffffu, errbits);
+  if (lane == 0 && errbits) set_error(err_word, errbits);
+  __syncthreads();
+  for (int k = tid; k < nkb; k += kRouteThreads) {
+    uint32_t t = 0;
+    for (int w = 0; w < kRouteWarps; ++w) t += cnt[w * nkb + k];
+    counts[(size_t)blockIdx.x * nkb + k] = t;
+  }
+}
+
+template <class KeyFn>
+__global__ void __launch_bounds__(kRouteThreads)
+    route_scatter_kernel(KeyFn key_of, int n, int n_keys, const uint32_t* __restrict__ counts,
+                         int32_t* __restrict__ perm, int32_t* __restrict__ seg_start) {
+  extern __shared__ uint32_t cnt[];  // [kRouteWarps][n_keys + 1], then before[n_keys + 1]
+  __shared__ uint32_t warp_sums[kRouteWarps];
+  cudaGridDependencySynchronize();
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nkb = n_keys + 1, nblk = (int)gridDim.x, blk = (int)blockIdx.x;
+  uint32_t* before = cnt + kRouteWarps * nkb;  // this chunk's start within each key
+  for (int i = tid; i < kRouteWarps * nkb; i += kRouteThreads) cnt[i] = 0;
+  for (int k = tid; k < nkb; k += kRouteThreads) {
+    uint32_t b = 0;
+    for (int c = 0; c < blk; ++c) b += counts[(size_t)c * nkb + k];
+    before[k] = b;
+  }
+  __syncthreads();
+  const int b0 = min(n, blk * kRouteChunk + warp * kRoutePerWarp);
+  const int b1 = min(n, b0 + kRoutePerWarp);
+  uint32_t dummy = 0;
+  uint32_t* my = cnt + warp * nkb;
+  warp_count(key_of, b0, b1, nkb, my, dummy);
+  __syncthreads();
+  int k0, k1;
+  uint32_t run = block_scan_keys(
+      nkb,
+      [&](int k) {
+        uint32_t t = 0;
+        for (int c = 0; c < nblk; ++c) t += counts[(size_t)c * nkb + k];
+        return t;
+      },
+      k0, k1, warp_sums);
+  for (int k = k0; k < k1; ++k) {
+    if (blk == 0) seg_start[k] = (int32_t)run;
+    uint32_t at = run + before[k];
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const uint32_t c = cnt[w * nkb + k];
+      cnt[w * nkb + k] = at;
+      at += c;
+    }
+    uint32_t t = 0;
+    for (int c = 0; c < nblk; ++c) t += counts[(size_t)c * nkb + k];
+    run += t;
+  }
+  if (blk == 0 && tid == 0) seg_start[nkb] = n;
+  __syncthreads();
+  warp_scatter(key_of, b0, b1, nkb, my, perm);
 }
 
 }  // namespace lora

@@ -88,6 +88,38 @@ def test_route_bit_exact(ld, oracle, n, L):
     assert e == ref_err
 
 
+@pytest.mark.parametrize("n,L", [(2048, 8), (5003, 8), (20000, 8), (16384, 512), (9000, 3071),
+                                 (100, 8)])
+def test_chunked_route_bit_exact(ld, oracle, n, L):
+    """The many-CTA routing sort gives the one-CTA sort's output bit for bit
+    (the same stable order) and the oracle's segments."""
+    rng = np.random.default_rng(7 * n + L)
+    seq = rng.integers(-2, L + 2, size=n).astype(np.int32)
+    seq_d = torch.from_numpy(seq).cuda()
+    err = ld.new_error_word()
+    perm, seg = ld.lora_route_with_scratch(seq_d, L, err=err)
+    e = ld.lora_get_error(err)
+    perm1, seg1 = ld.lora_route(seq_d, L)
+    ref_perm, ref_seg, ref_err = oracle.segments(seq, L)
+    seg = seg.cpu().numpy()
+    assert np.array_equal(seg, seg1.cpu().numpy())
+    assert np.array_equal(seg[: L + 1], ref_seg)
+    assert seg[L + 1] == n
+    p = perm.cpu().numpy()
+    assert np.array_equal(p[: ref_seg[-1]], ref_perm)
+    assert np.array_equal(p[:n], perm1.cpu().numpy()[:n])
+    assert e == ref_err
+
+
+def test_chunked_route_rejects_missing_scratch(ld):
+    seq = torch.zeros(5000, dtype=torch.int32, device="cuda")
+    perm = torch.empty(5000, dtype=torch.int32, device="cuda")
+    seg = torch.empty(10, dtype=torch.int32, device="cuda")
+    rc = ld.lib().lora_route_with_scratch(perm.data_ptr(), seg.data_ptr(), seq.data_ptr(), 5000,
+                                          8, None, 0, None, None)
+    assert rc == 5  # LORA_ERR_WORKSPACE
+
+
 # ------------------------------------------------------- the fused delta --
 
 def test_tiny_workload(ld, di, oracle):
