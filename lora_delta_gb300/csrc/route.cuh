@@ -65,27 +65,27 @@ inline size_t route_smem_bytes(int n_keys) {
 }
 
 // Per-warp pieces shared by the one-CTA sort and the chunked sort.  A warp
-// owns the items [b0, b1) and reads kRouteBatch keys per lane before using
-// them (one memory round trip per 32 * kRouteBatch items).  With at most 32
+// owns the items [b0, b1) and reads BATCH keys per lane before using them
+// (one memory round trip per 32 * BATCH items).  With at most 32
 // key values, lane k counts key k from one ballot per key value; otherwise
 // __match_any_sync groups the lanes by key.
 
 // my[k] += number of items of key k in [b0, b1).
-template <class KeyFn>
+template <int BATCH, class KeyFn>
 __device__ __forceinline__ void warp_count(const KeyFn& key_of, int b0, int b1, int nkb,
                                            uint32_t* my, uint32_t& errbits) {
   const int lane = threadIdx.x & 31;
   const bool few = nkb <= 32;
   uint32_t mine = 0;  // (few keys) this lane's count of key `lane`
-  for (int base = b0; base < b1; base += 32 * kRouteBatch) {
-    int keys[kRouteBatch];
+  for (int base = b0; base < b1; base += 32 * BATCH) {
+    int keys[BATCH];
 #pragma unroll
-    for (int u = 0; u < kRouteBatch; ++u) {
+    for (int u = 0; u < BATCH; ++u) {
       const int i = base + u * 32 + lane;
       keys[u] = (i < b1) ? key_of(i, errbits) : -1;
     }
 #pragma unroll
-    for (int u = 0; u < kRouteBatch; ++u) {
+    for (int u = 0; u < BATCH; ++u) {
       if (few) {
         for (int kk = 0; kk < nkb; ++kk) {
           const unsigned m = __ballot_sync(0xffffffffu, keys[u] == kk);
@@ -104,23 +104,23 @@ __device__ __forceinline__ void warp_count(const KeyFn& key_of, int b0, int b1, 
 
 // Scatter the items of [b0, b1) to perm; my[k] holds the next position of
 // key k and is advanced.
-template <class KeyFn>
+template <int BATCH, class KeyFn>
 __device__ __forceinline__ void warp_scatter(const KeyFn& key_of, int b0, int b1, int nkb,
                                              uint32_t* my, int32_t* __restrict__ perm) {
   const int lane = threadIdx.x & 31;
   const bool few = nkb <= 32;
   uint32_t next = (few && lane < nkb) ? my[lane] : 0u;  // (few keys) next position of key `lane`
   const unsigned lt = (1u << lane) - 1u;
-  for (int base = b0; base < b1; base += 32 * kRouteBatch) {
-    int keys[kRouteBatch];
+  for (int base = b0; base < b1; base += 32 * BATCH) {
+    int keys[BATCH];
     uint32_t dummy = 0;
 #pragma unroll
-    for (int u = 0; u < kRouteBatch; ++u) {
+    for (int u = 0; u < BATCH; ++u) {
       const int i = base + u * 32 + lane;
       keys[u] = (i < b1) ? key_of(i, dummy) : -1;
     }
 #pragma unroll
-    for (int u = 0; u < kRouteBatch; ++u) {
+    for (int u = 0; u < BATCH; ++u) {
       const int key = keys[u];
       if (few) {
         unsigned peers = 0, cnt = 0;
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kRouteThreads)
   const int b0 = min(n, warp * per), b1 = min(n, b0 + per);
   uint32_t errbits = 0;
   uint32_t* my = cnt + warp * nkb;
-  warp_count(key_of, b0, b1, nkb, my, errbits);
+  warp_count<kRouteBatch>(key_of, b0, b1, nkb, my, errbits);
   errbits = __reduce_or_sync(0xffffffffu, errbits);
   if (lane == 0 && errbits) set_error(err_word, errbits);
   __syncthreads();
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kRouteThreads)
   }
   if (tid == 0) seg_start[nkb] = n;
   __syncthreads();
-  warp_scatter(key_of, b0, b1, nkb, my, perm);
+  warp_scatter<kRouteBatch>(key_of, b0, b1, nkb, my, perm);
 }
 
 // ------------------------------------------------------- chunked sort ---
@@ -220,7 +220,7 @@ constexpr int kRouteChunk = 1024;
 constexpr int kRoutePerWarp = kRouteChunk / kRouteWarps;
 
 inline size_t route_chunk_smem_bytes(int n_keys) {
-  return sizeof(uint32_t) * ((size_t)kRouteWarps + 1) * (size_t)(n_keys + 1);
+  return sizeof(uint32_t) * ((size_t)kRouteWarps + 2) * (size_t)(n_keys + 1);
 }
 
 template <class KeyFn>
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kRouteThreads)
   const int b0 = min(n, (int)blockIdx.x * kRouteChunk + warp * kRoutePerWarp);
   const int b1 = min(n, b0 + kRoutePerWarp);
   uint32_t errbits = 0;
-  warp_count(key_of, b0, b1, nkb, cnt + warp * nkb, errbits);
+  warp_count<kRoutePerWarp / 32>(key_of, b0, b1, nkb, cnt + warp * nkb, errbits);
   errbits = __reduce_or_sync(0xffffffffu, errbits);
   if (lane == 0 && errbits) set_error(err_word, errbits);
   __syncthreads();
@@ -250,34 +250,36 @@ template <class KeyFn>
 __global__ void __launch_bounds__(kRouteThreads)
     route_scatter_kernel(KeyFn key_of, int n, int n_keys, const uint32_t* __restrict__ counts,
                          int32_t* __restrict__ perm, int32_t* __restrict__ seg_start) {
-  extern __shared__ uint32_t cnt[];  // [kRouteWarps][n_keys + 1], then before[n_keys + 1]
+  // [kRouteWarps][n_keys + 1] per-warp counts, then before[n_keys + 1] (this
+  // chunk's start within each key) and total[n_keys + 1]
+  extern __shared__ uint32_t cnt[];
   __shared__ uint32_t warp_sums[kRouteWarps];
   cudaGridDependencySynchronize();
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nkb = n_keys + 1, nblk = (int)gridDim.x, blk = (int)blockIdx.x;
-  uint32_t* before = cnt + kRouteWarps * nkb;  // this chunk's start within each key
+  uint32_t* before = cnt + kRouteWarps * nkb;
+  uint32_t* total = before + nkb;
   for (int i = tid; i < kRouteWarps * nkb; i += kRouteThreads) cnt[i] = 0;
-  for (int k = tid; k < nkb; k += kRouteThreads) {
-    uint32_t b = 0;
-    for (int c = 0; c < blk; ++c) b += counts[(size_t)c * nkb + k];
+  for (int k = tid; k < nkb; k += kRouteThreads) {  // one pass, loads in flight together
+    uint32_t b = 0, t = 0;
+#pragma unroll 8
+    for (int c = 0; c < nblk; ++c) {
+      const uint32_t v = counts[(size_t)c * nkb + k];
+      t += v;
+      b += c < blk ? v : 0u;
+    }
     before[k] = b;
+    total[k] = t;
   }
   __syncthreads();
   const int b0 = min(n, blk * kRouteChunk + warp * kRoutePerWarp);
   const int b1 = min(n, b0 + kRoutePerWarp);
   uint32_t dummy = 0;
   uint32_t* my = cnt + warp * nkb;
-  warp_count(key_of, b0, b1, nkb, my, dummy);
+  warp_count<kRoutePerWarp / 32>(key_of, b0, b1, nkb, my, dummy);
   __syncthreads();
   int k0, k1;
-  uint32_t run = block_scan_keys(
-      nkb,
-      [&](int k) {
-        uint32_t t = 0;
-        for (int c = 0; c < nblk; ++c) t += counts[(size_t)c * nkb + k];
-        return t;
-      },
-      k0, k1, warp_sums);
+  uint32_t run = block_scan_keys(nkb, [&](int k) { return total[k]; }, k0, k1, warp_sums);
   for (int k = k0; k < k1; ++k) {
     if (blk == 0) seg_start[k] = (int32_t)run;
     uint32_t at = run + before[k];
@@ -286,13 +288,11 @@ __global__ void __launch_bounds__(kRouteThreads)
       cnt[w * nkb + k] = at;
       at += c;
     }
-    uint32_t t = 0;
-    for (int c = 0; c < nblk; ++c) t += counts[(size_t)c * nkb + k];
-    run += t;
+    run += total[k];
   }
   if (blk == 0 && tid == 0) seg_start[nkb] = n;
   __syncthreads();
-  warp_scatter(key_of, b0, b1, nkb, my, perm);
+  warp_scatter<kRoutePerWarp / 32>(key_of, b0, b1, nkb, my, perm);
 }
 
 }  // namespace lora
