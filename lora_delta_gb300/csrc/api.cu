@@ -19,7 +19,6 @@ using namespace lora;
 namespace {
 
 constexpr int kAbiVersion = 2;
-constexpr int kStageBytes = 64 * 1024;  // A rows of one shrink stage (both buffers)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -50,6 +49,24 @@ int cluster_size_for(int n_keys) {
   if (n_keys <= 48) return 16;
   if (n_keys <= 192) return 8;
   return 4;
+}
+// Shared memory for the A rows of the cluster kernel's shrink stages (both
+// buffers); LORA_STAGE_KB overrides (16..192), read once.
+int stage_bytes() {
+  static const int v = [] {
+    const int kb = env_int("LORA_STAGE_KB", 64);
+    return (kb >= 16 && kb <= 192 ? kb : 64) * 1024;
+  }();
+  return v;
+}
+// Largest B slab the cluster kernel stages in shared memory; LORA_BSTAGE_KB
+// overrides (8..96), read once.
+int b_stage_bytes() {
+  static const int v = [] {
+    const int kb = env_int("LORA_BSTAGE_KB", 32);
+    return (kb >= 8 && kb <= 96 ? kb : 32) * 1024;
+  }();
+  return v;
 }
 bool use_pdl() {
   static const bool on = env_int("LORA_PDL", 1) != 0;
@@ -180,15 +197,16 @@ void plan_tiles(DeltaArgs& a, int k_in, int n_cols, int sr_max, int mode) {
   if (mode == kModeExpand) {
     a.kst = 16;
     a.nbuf = 1;
-  } else if (sr16 * (a.kc + 8) * 2 <= kStageBytes) {
+  } else if (sr16 * (a.kc + 8) * 2 <= stage_bytes()) {
     a.kst = a.kc;  // one stage: A stays resident across row passes
     a.nbuf = 1;
   } else {
-    int ks = kStageBytes / 2 / (sr16 * 2) - 8;
+    int ks = stage_bytes() / 2 / (sr16 * 2) - 8;
     ks = ks >= 64 ? ks / 64 * 64 : ks / 16 * 16;
     a.kst = ks < 16 ? 16 : ks;
     a.nbuf = 2;
   }
+  a.b_stage_max = b_stage_bytes();
   a.cpc = ((n_cols + cs - 1) / cs + 7) / 8 * 8;
   if (a.cpc < 8) a.cpc = 8;
   a.min_rows = 0;

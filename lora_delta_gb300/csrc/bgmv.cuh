@@ -138,13 +138,13 @@ struct DeltaArgs {
   int cs;     // CTAs per cluster
   int early;  // start the weight copies before the grid dependency wait
   int row_cap;
+  int b_stage_max;         // largest B slab (bytes) staged in shared memory
   int sr_max;              // S * R: shared-memory sizing
   int min_rows, max_rows;  // keys with a row count outside [min, max) are skipped
   uint32_t* err;
 };
 
 constexpr int kRowsPerPass = 16;  // rows of one pass: two 8-wide MMA column tiles
-constexpr int kBStageBytes = 32 * 1024;  // largest B slab staged in shared memory
 
 // Shared-memory plan (bytes), identical on host and device.
 struct SmemPlan {
@@ -173,7 +173,7 @@ __host__ __device__ inline SmemPlan smem_plan(const DeltaArgs& a, int mode) {
   p.H_off = o;
   o += kRowsPerPass * p.sr16 * 4;
   // expand operands: the CTA's B rows and the pass's out segments
-  p.b_staged = (mode != kModeShrink && a.cpc * a.R * 2 <= kBStageBytes) ? 1 : 0;
+  p.b_staged = (mode != kModeShrink && a.cpc * a.R * 2 <= a.b_stage_max) ? 1 : 0;
   p.o_stride = a.cpc + 8;
   p.Bs_off = o;
   if (p.b_staged) o += a.cpc * a.R * 2;
