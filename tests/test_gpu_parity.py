@@ -311,6 +311,54 @@ def test_expand_matches_oracle_and_composes(ld, di, oracle):
     assert_close(di.bits(two), di.bits(fused), "shrink+expand vs fused")
 
 
+# ------------------------------------------- logits and embedding variants --
+
+@pytest.mark.parametrize("n", [48, 1500])
+def test_logits_variant_at_vocabulary_width(ld, di, oracle, n):
+    """"punica_base.py", add_lora_logits: buffer = (x A^T) * scale, y += buffer
+    B^T, with the LM head's vocabulary-wide output as one slice of 32064
+    columns (its last 128-column chunk is ragged: 64 columns).  48 rows stay
+    on the small-segment path; 1500 rows over 5 slots (~270 each) take the
+    tensor-core path.  The scale may sit in the shrink (the page's form) or
+    in the fold: the two-step form with the scale in lora_shrink matches."""
+    case = inputs.linear_case(31, n=n, k_in=1024, widths=(32064,), max_loras=5, max_rank=16,
+                              ranks=[16, 8, 16, 16, 4], alpha=16.0, p_none=0.1, name="logits")
+    got, err, d = run_fused(ld, di, case)
+    rows = None if n < 100 else np.sort(np.random.default_rng(3).choice(n, 128, replace=False))
+    check_linear(oracle, case, got, err, rows=rows)
+    if n < 100:
+        hg = torch.zeros(1, n, 16, dtype=torch.float32, device="cuda")
+        ld.lora_shrink(hg, d.x, d.seq_slot, d.pool, scale_table=d.pool.scale_table)
+        two = d.out0.clone()
+        ld.lora_expand(two, hg, d.seq_slot, d.pool, scale_table=None)
+        assert_close(di.bits(two), got, "logits, scale in the shrink")
+
+
+def test_embedding_variant_expands_looked_up_rows(ld, di, oracle):
+    """"punica_base.py", add_lora_embedding: y += x B^T, expand only, where x is
+    the rank-space row an embedding lookup gives each token:
+    x[i] = A_emb[slot_i][token_i] (taken here as an fp32 table)."""
+    rng = np.random.default_rng(41)
+    n, vocab, R, L, hidden = 700, 3000, 16, 4, 2048
+    seq = rng.integers(-1, L, size=n).astype(np.int32)
+    tokens = rng.integers(0, vocab, size=n)
+    a_emb = (rng.standard_normal((L, vocab, R)) / 4).astype(np.float32)
+    h = np.zeros((1, n, R), dtype=np.float32)
+    ok = seq >= 0
+    h[0, ok] = a_emb[seq[ok], tokens[ok]]
+    case = inputs.linear_case(42, n=n, k_in=64, widths=(hidden,), max_loras=L, max_rank=R,
+                              ranks=[16] * L, alpha=16.0, seq_slot=seq, name="embedding")
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, L, R)
+    ref = case.out0.copy()
+    oracle.expand(ref, h, seq, pool, None)  # no scale: y += x B^T
+    d = di.linear_to_device(case)
+    out = d.out0.clone()
+    ld.lora_expand(out, torch.from_numpy(h).cuda(), d.seq_slot, d.pool, scale_table=None)
+    got = di.bits(out)
+    assert_close(got, ref, "embedding")
+    assert np.array_equal(got[~ok], case.out0[~ok])
+
+
 # ------------------------------------------------------------------- MoE --
 
 def run_moe(ld, di, mc, topk=None, lora=None):
