@@ -136,6 +136,9 @@ def algorithmic_bytes(case, rows_mask=None):
     import numpy as np
     seq = case.seq_slot if rows_mask is None else case.seq_slot[rows_mask]
     routed = (seq >= 0) & (seq < case.max_loras)
+    # rows whose slot adapts no slice are untouched: they move nothing
+    live = np.array([a is not None and any(a.adapted) for a in case.adapters] + [False])
+    routed &= live[np.where(routed, seq, len(case.adapters))]
     slots = np.unique(seq[routed])
     n_routed = int(routed.sum())
     per_slot = 0
@@ -412,6 +415,8 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src, only=
         _prefill(ld, di, inputs, device, hbm_peak, bf16_peak, timed, res)
     if only in (None, "skewed"):
         _skewed(ld, di, inputs, device, hbm_peak, timed, res)
+    if only in (None, "fold"):
+        _fold(ld, di, inputs, device, hbm_peak, timed, res)
     if only in (None, "moe"):
         _moe(ld, di, inputs, device, hbm_peak, timed, res)
     res["peak_source"] = peak_src
@@ -454,6 +459,25 @@ def _skewed(ld, di, inputs, device, hbm_peak, timed, res):
                             "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4),
                             "launches_per_call": 10}
     del d1, d2, ws
+    torch.cuda.empty_cache()
+
+
+def _fold(ld, di, inputs, device, hbm_peak, timed, res):
+    import torch
+    # expert-sorted MoE fold (w13): 2048 tokens x top-8 of 64 experts, one
+    # adapter per expert (10% unadapted), rows grouped by device offsets
+    case, offsets = inputs.expert_sorted_case()
+    d = di.linear_to_device(case, device)
+    off = torch.from_numpy(offsets).to(device)
+    ws = torch.empty(ld.lora_workspace_size(case.n, 1, case.max_rank, case.max_loras),
+                     dtype=torch.uint8, device=device)
+    ms = timed(lambda: ld.lora_delta_segmented(d.out0, d.x, off, d.pool, workspace=ws))
+    ab = algorithmic_bytes(case)
+    gbs = ab / (ms / 1e3) / 1e9
+    res["moe_expert_fold_w13"] = {"rows_per_s": round(case.n / (ms / 1e3), 1), "ms": round(ms, 4),
+                                  "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+                                  "launches_per_call": 5}
+    del d, ws
     torch.cuda.empty_cache()
 
 
@@ -536,7 +560,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads (prefill, skewed, MoE)")
-    ap.add_argument("--only", choices=["prefill", "skewed", "moe"], default=None,
+    ap.add_argument("--only", choices=["prefill", "skewed", "moe", "fold"], default=None,
                     help="time one of the other workloads alone and print its numbers "
                          "(for profiling captures; not the benchmark line)")
     args = ap.parse_args()

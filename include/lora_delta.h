@@ -62,6 +62,7 @@ typedef struct CUstream_st *lora_stream_t; /* == cudaStream_t */
 #define LORA_DEV_ERR_TIMEOUT 8u /* a bounded wait inside a kernel gave up              */
 #define LORA_DEV_ERR_ALIGN 16u  /* a table address is not 16-byte aligned: slice skipped */
 #define LORA_DEV_ERR_INTERNAL 32u /* a launch invariant of the library failed (a bug)   */
+#define LORA_DEV_ERR_SEGMENT 64u  /* segment starts not nondecreasing in [0, n]: clamped  */
 
 /* Human-readable name of a status code (static string). */
 const char *lora_status_string(int status);
@@ -179,14 +180,37 @@ int lora_expand(void *out, int64_t ld_out, const float *h, const int32_t *seq_sl
  * slice j whose A and B table entries are both nonzero,
  *   out[i, off_j : off_j + w_j] = RN_bf16(out + scale_s * (x[i] A_j,s^T) B_j,s^T)
  * (RN_bf16(scale_s * ...) when add_inputs == 0).  Both contractions run at
- * the padded rank R; the rank-R intermediate stays in fp32 on chip and
- * never goes to global memory.  x [n, k_in] bf16, out [n, ld_out] bf16.
+ * the padded rank R, and the rank-R intermediate is fp32.  For slots with
+ * few rows it stays on chip; slots with many rows go to the tensor-core path,
+ * whose intermediate passes through fp32 planes in the workspace.  x [n, k_in]
+ * bf16, out [n, ld_out] bf16.
  */
 int lora_delta_fused(void *out, int64_t ld_out, const void *x, int n, int k_in,
                      const int32_t *seq_slot, const uint64_t *a_table, const uint64_t *b_table,
                      const float *scale_table, const int32_t *widths, int S, int R,
                      int max_loras, int offset_start, int add_inputs, void *workspace,
                      size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_delta_segmented -- the delta on rows already grouped by adapter, such
+ * as the expert-sorted rows of a grouped MoE GEMM ("expert_apply.rs",
+ * apply_expert_lora_sorted / expert_delta_workitems, with the row blocks read
+ * from device memory instead of a host copy).  Rows seg_start[s] ..
+ * seg_start[s+1] - 1 take adapter s (table entries j * n_segs + s, as in
+ * lora_delta_fused with max_loras = n_segs); rows from seg_start[n_segs] on
+ * are untouched.  seg_start [n_segs + 1] int32 (device) must start at 0 and
+ * be nondecreasing up to at most n; otherwise the starts are clamped into
+ * that form (no row outside the batch is read or written) and
+ * LORA_DEV_ERR_SEGMENT is set.  Arithmetic, layouts and the other arguments
+ * as lora_delta_fused; a workspace of lora_workspace_size(n, S, R, n_segs)
+ * bytes is required (no routing sort runs).
+ */
+int lora_delta_segmented(void *out, int64_t ld_out, const void *x, int n, int k_in,
+                         const int32_t *seg_start, int n_segs, const uint64_t *a_table,
+                         const uint64_t *b_table, const float *scale_table,
+                         const int32_t *widths, int S, int R, int offset_start, int add_inputs,
+                         void *workspace, size_t ws_bytes, uint32_t *err_word,
+                         lora_stream_t stream);
 
 /*
  * lora_moe_fc1_delta -- [flashinfer] bgmv_moe_gemm1_lora_delta.  For every

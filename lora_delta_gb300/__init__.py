@@ -24,6 +24,7 @@ __all__ = [
     "LoraError", "LibraryMissing", "LoraPool", "lora_scale", "lora_pool_pack",
     "lora_workspace_size", "lora_workspace_min_size", "lora_route", "lora_route_scratch_size",
     "lora_route_with_scratch", "lora_shrink", "lora_expand", "lora_delta_fused",
+    "lora_delta_segmented",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_get_error", "new_error_word",
     "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes",
 ]
@@ -255,6 +256,29 @@ def lora_delta_fused(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,
     _check("lora_delta_fused", lib().lora_delta_fused(
         _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
         _ptr(pool.b_table), _ptr(st), w, pool.S, pool.R, pool.max_loras, int(offset_start),
+        int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_delta_segmented(out, x, seg_start, pool: LoraPool, offset_start: int = 0,
+                         add_inputs: bool = True, scale_table=None, workspace=None, err=None,
+                         stream=None):
+    """The delta on rows grouped by adapter: rows seg_start[s]..seg_start[s+1]
+    take pool slot s (e.g. expert-sorted MoE rows, one adapter per expert)."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(seg_start, "seg_start", torch.int32)
+    n, k_in = x.shape
+    if out.shape[0] != n:
+        raise ValueError("out and x must have the same number of rows")
+    n_segs = seg_start.numel() - 1
+    if n_segs != pool.max_loras:
+        raise ValueError("seg_start must have pool.max_loras + 1 entries")
+    st = pool.scale_table if scale_table is None else scale_table
+    ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, n_segs), workspace, x.device)
+    w = _widths_arg(pool.widths)
+    _check("lora_delta_segmented", lib().lora_delta_segmented(
+        _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seg_start), n_segs, _ptr(pool.a_table),
+        _ptr(pool.b_table), _ptr(st), w, pool.S, pool.R, int(offset_start),
         int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
 
 

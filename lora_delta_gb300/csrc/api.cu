@@ -433,7 +433,11 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   int per_sm = ctas_per_sm(sgmv_shrink_kernel<Tables>, kShrinkThreads, shrink_smem);
   if (per_sm > 512 / kSgmvMaxSR) per_sm = 512 / kSgmvMaxSR;
   const int slots = per_sm * sm_count();
-  int ks_max = kMaxKSplit;
+  static const int ks_cap = [] {
+    const int v = env_int("LORA_SHRINK_KS_MAX", kMaxKSplit);
+    return v >= 1 && v <= kMaxKSplit ? v : kMaxKSplit;
+  }();
+  int ks_max = ks_cap;
   {
     const int nkb = (d.k_in + 63) / 64;
     if (ks_max > nkb) ks_max = nkb;
@@ -535,6 +539,40 @@ __global__ void pool_pack_kernel(__nv_bfloat16* __restrict__ a_slot,
 }
 
 __global__ void clear_word_kernel(uint32_t* w) { *w = 0u; }
+
+// Plan of a call on rows already grouped by adapter ("expert_apply.rs",
+// expert_delta_workitems, done on the device from the device offsets): the
+// identity row permutation, and the segment starts made nondecreasing within
+// [0, n] (a start out of order or past n is clamped, nothing is read outside
+// the batch, and LORA_DEV_ERR_SEGMENT is set); rows past the last segment
+// form the no-adapter bucket.
+__global__ void segment_plan_kernel(const int32_t* __restrict__ offsets, int n_segs, int n,
+                                    int32_t* __restrict__ perm, int32_t* __restrict__ seg,
+                                    uint32_t* err) {
+  __shared__ int off_s[kMaxKeys + 1];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) perm[i] = i;
+  if (blockIdx.x != 0) return;
+  for (int s = threadIdx.x; s <= n_segs; s += blockDim.x) off_s[s] = offsets[s];  // one round trip
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int prev = 0;
+    bool bad = false;
+    for (int s = 0; s <= n_segs; ++s) {
+      int v = off_s[s];
+      if (s == 0 && v != 0) bad = true;  // segment 0 starts at row 0
+      if (v < prev || v > n) {
+        bad = true;
+        v = v < prev ? prev : n;
+      }
+      if (s == 0) v = 0;
+      seg[s] = v;
+      prev = v;
+    }
+    seg[n_segs + 1] = n;
+    if (bad) set_error(err, LORA_DEV_ERR_SEGMENT);
+  }
+}
 
 extern "C" {
 
@@ -664,6 +702,56 @@ int lora_expand(void* out, int64_t ld_out, const float* h, const int32_t* seq_sl
   plan_tiles(a, 8, a.sl.n_cols, a.sr_max, kModeExpand);
   LinearTables tb{nullptr, b_table, scale_table, max_loras};
   return launch_delta<kModeExpand>(a, tb, max_loras, (cudaStream_t)stream);
+}
+
+int lora_delta_segmented(void* out, int64_t ld_out, const void* x, int n, int k_in,
+                         const int32_t* seg_start, int n_segs, const uint64_t* a_table,
+                         const uint64_t* b_table, const float* scale_table, const int32_t* widths,
+                         int S, int R, int offset_start, int add_inputs, void* workspace,
+                         size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (n < 0 || k_in < 0) return LORA_ERR_ARG;
+  if (n == 0) return LORA_OK;
+  if (!out || !x || !seg_start || !a_table || !b_table) return LORA_ERR_ARG;
+  int rc = check_max_loras(n_segs);
+  if (rc) return rc;
+  DeltaArgs a = {};
+  if ((rc = make_slices(widths, S, offset_start, a.sl, a.rel))) return rc;
+  if ((rc = check_rank(S, R))) return rc;
+  if (ld_out < (int64_t)offset_start + a.sl.n_cols) return LORA_ERR_SHAPE;
+  if (k_in % 8 || ld_out % 8 || !aligned16(out) || !aligned16(x)) return LORA_ERR_ALIGN;
+  if (a.sl.n_cols == 0) return LORA_OK;
+  const int hs = (S * R + 15) / 16 * 16;
+  if (!workspace || ws_bytes < ws_bytes_for(n, n_segs, hs)) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
+  cudaStream_t st = (cudaStream_t)stream;
+  Workspace w = carve(workspace, n, n_segs);
+  w.bytes = ws_bytes;
+  segment_plan_kernel<<<(n + 1023) / 1024, 1024, 0, st>>>(seg_start, n_segs, n, w.perm, w.seg,
+                                                         err_word);
+  if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
+  a.out = (__nv_bfloat16*)out;
+  a.ld_out = ld_out;
+  a.x = (const __nv_bfloat16*)x;
+  a.ld_x = k_in;
+  a.k_in = k_in;
+  a.R = R;
+  a.add_inputs = add_inputs ? 1 : 0;
+  a.sr_max = S * R;
+  a.seq_slot = nullptr;
+  a.n = n;
+  a.n_keys = n_segs;
+  a.err = err_word;
+  a.perm = w.perm;
+  a.seg_start = w.seg;
+  a.row_cap = 0;
+  plan_tiles(a, k_in, a.sl.n_cols, a.sr_max, kModeFused);
+  LinearTables tb{a_table, b_table, scale_table, n_segs};
+  const bool sgmv = a.sr_max <= kSgmvMaxSR;
+  const int thr = sgmv_min_rows();
+  if (sgmv) a.max_rows = thr;
+  rc = launch_delta<kModeFused>(a, tb, n_segs, st);
+  if (rc || !sgmv) return rc;
+  return launch_sgmv(a, tb, w, n_segs, thr, st);
 }
 
 int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,

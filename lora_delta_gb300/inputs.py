@@ -244,3 +244,30 @@ def moe_case(shared_a: bool = False, seed: int = 1238, T: int = 2048, top_k: int
                    + f" T={T} top_k={top_k} E={E} H={H} I={I} rank={rank}",
                    seed=seed, T=T, top_k=top_k, E=E, H=H, I=I, rank=rank, L=L, scale=scale,
                    shared_a=shared_a, x=x, topk_ids=topk, lora_ids=lora, A_banks=A, B_banks=B)
+
+
+def expert_sorted_case(seed: int = 1239, T: int = 2048, top_k: int = 8, E: int = 64,
+                       k_in: int = 2048, width: int = 1536, rank: int = 16,
+                       p_unadapted: float = 0.1, alpha: float = 32.0, tail_rows: int = 0):
+    """Expert-sorted rows of a grouped MoE GEMM ("expert_apply.rs",
+    apply_expert_lora_sorted): T tokens each route to top_k distinct experts
+    of E (uniform); the T * top_k (token, slot) rows are sorted by expert, so
+    expert e owns rows offsets[e] .. offsets[e+1] - 1.  One adapter per expert
+    (rank `rank`, padded to itself), a fraction p_unadapted of experts with
+    none; x [rows, k_in] (the sorted grouped-GEMM input), out0 [rows, width]
+    (its output, w13 = 2I by default).  `tail_rows` extra rows follow the last
+    expert's block (no adapter).  Returns (LinearCase with seq_slot = the
+    row's expert, or -1 for tail rows, offsets [E + 1] int32)."""
+    rng = np.random.default_rng(seed + 20_000)
+    topk = np.stack([rng.permutation(E)[:top_k] for _ in range(T)])
+    counts = np.bincount(topk.ravel(), minlength=E)
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    n = int(offsets[-1]) + tail_rows
+    seq = np.full(n, -1, dtype=np.int32)
+    seq[: offsets[-1]] = np.repeat(np.arange(E, dtype=np.int32), counts)
+    adapted_expert = rng.random(E) >= p_unadapted
+    ranks = [rank if adapted_expert[e] else 0 for e in range(E)]
+    case = linear_case(seed, n, k_in, (width,), E, rank, ranks, alpha, seq_slot=seq,
+                       name=f"expert-sorted fold {n} rows, {E} experts")
+    return case, offsets

@@ -359,6 +359,46 @@ def test_embedding_variant_expands_looked_up_rows(ld, di, oracle):
     assert np.array_equal(got[~ok], case.out0[~ok])
 
 
+# ------------------------------------------------ expert-sorted fold --
+
+def run_segmented(ld, di, case, offsets, add_inputs=True):
+    d = di.linear_to_device(case)
+    out = d.out0.clone()
+    err = ld.new_error_word()
+    ld.lora_delta_segmented(out, d.x, torch.from_numpy(offsets).cuda(), d.pool,
+                            add_inputs=add_inputs, err=err)
+    return di.bits(out), ld.lora_get_error(err)
+
+
+@pytest.mark.parametrize("T,top_k,add", [(512, 8, True), (64, 2, False)])
+def test_segmented_expert_fold(ld, di, oracle, T, top_k, add):
+    """"expert_apply.rs", apply_expert_lora_sorted: each expert's block of
+    sorted rows gets that expert's adapter, the blocks read from device
+    offsets.  512 tokens x 8: ~64 rows per expert (both paths); 64 tokens x 2:
+    many empty experts.  20% of experts unadapted; 37 rows past the last block."""
+    case, offsets = inputs.expert_sorted_case(seed=17, T=T, top_k=top_k, E=64, k_in=1024,
+                                              width=768, p_unadapted=0.2, tail_rows=37)
+    got, err = run_segmented(ld, di, case, offsets, add_inputs=add)
+    check_linear(oracle, case, got, err, add_inputs=add)
+
+
+def test_segmented_expert_fold_full_size_sampled(ld, di, oracle):
+    """2048 tokens x top-8 of 64 experts: 16,384 sorted rows, w13 width 1536."""
+    case, offsets = inputs.expert_sorted_case()
+    got, err = run_segmented(ld, di, case, offsets)
+    rows = np.sort(np.random.default_rng(5).choice(case.n, 192, replace=False))
+    check_linear(oracle, case, got, err, rows=rows)
+
+
+def test_segmented_bad_offsets_are_clamped_and_flagged(ld, di):
+    case, offsets = inputs.expert_sorted_case(seed=18, T=64, top_k=4, E=16, k_in=256, width=256)
+    bad = offsets.copy()
+    bad[5] = bad[7] + 50  # out of order
+    bad[-1] = case.n + 1000  # past the batch
+    _, err = run_segmented(ld, di, case, bad)
+    assert err & 64  # LORA_DEV_ERR_SEGMENT
+
+
 # ------------------------------------------------------------------- MoE --
 
 def run_moe(ld, di, mc, topk=None, lora=None):
