@@ -848,8 +848,21 @@ int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t
   a.err = err_word;
   plan_tiles(a, H, a.sl.n_cols, a.sr_max, kModeFused);
   MoeTables tb{w_ptr_a, w_ptr_b, stride_a, stride_b, E, top_k, n_slices, scale};
+  // With LORA_MOE_SGMV_MIN_ROWS set, keys with at least that many pairs go to
+  // the tensor-core path.  Off by default: at the ~26 pairs per key of a
+  // top-8-of-64 routing the cluster kernel is faster (0.139 against 0.187 ms
+  // on GB300), and the tensor-core kernels cost ~10 us of launches per call
+  // even when no key qualifies.
+  static const int moe_thr = env_int("LORA_MOE_SGMV_MIN_ROWS", 0);
+  const bool sgmv = moe_thr >= 1 && a.sr_max <= kSgmvMaxSR;
+  if (sgmv) a.max_rows = moe_thr;
   rc = launch_delta<kModeFused>(a, tb, n_keys, s);
   if (rc) return rc;
+  if (sgmv) {
+    Workspace wb = w;
+    wb.bytes = ws_bytes;
+    if ((rc = launch_sgmv(a, tb, wb, n_keys, moe_thr, s))) return rc;
+  }
   // the pairs with no adapter (the no-key bucket) are written as zeros
   zero_rows_kernel<<<1024, 256, 0, s>>>(a.out, a.ld_out, 2 * I, perm, seg, n_keys);
   return cuda_status(cudaGetLastError());
