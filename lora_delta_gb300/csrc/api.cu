@@ -788,6 +788,9 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
   const bool sgmv = a.perm != nullptr && a.sr_max <= kSgmvMaxSR;
   const int thr = sgmv_min_rows();
   if (sgmv) a.max_rows = thr;
+  // when the average slot has enough rows for the tensor-core path, most
+  // slots will leave the cluster kernel at once: no early weight copies
+  if (sgmv && n >= (int64_t)thr * max_loras) a.early = 0;
   rc = launch_delta<kModeFused>(a, tb, max_loras, (cudaStream_t)stream);
   if (rc || !sgmv) return rc;
   return launch_sgmv(a, tb, w, max_loras, thr, (cudaStream_t)stream);
