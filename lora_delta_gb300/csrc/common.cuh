@@ -18,6 +18,7 @@ constexpr int kMaxKeys = 3071;
 constexpr int kInlineRowsMax = 1024;  // rows a kernel clusters on its own
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitSleepNs = 20000;  // longest sleep of one poll
 
 // ------------------------------------------------------------------ bf16 --
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -120,13 +121,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, letting the thread sleep up to `ns` nanoseconds for the
+// phase to complete (fewer polls while a role waits for another).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; gives up after
 // kWaitLimitNs and returns false (the caller records LORA_DEV_ERR_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
