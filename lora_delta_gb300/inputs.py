@@ -271,3 +271,59 @@ def expert_sorted_case(seed: int = 1239, T: int = 2048, top_k: int = 8, E: int =
     case = linear_case(seed, n, k_in, (width,), E, rank, ranks, alpha, seq_slot=seq,
                        name=f"expert-sorted fold {n} rows, {E} experts")
     return case, offsets
+
+
+def moe_y0(seed: int, shape) -> np.ndarray:
+    """The expert GEMM's output that an in-place MoE delta updates (w13:
+    [T, top_k, 2I]; w2: [T, top_k, H]), N(0, 1) in bf16."""
+    return _normal_bf16(np.random.default_rng(seed + 30_000), shape)
+
+
+@dataclass
+class MoeDownCase:
+    """Routed-MoE down projection (w2): one activation row per (token, slot),
+    x [T * top_k, I]; banks ``A_banks = [A_down]`` [E, L, rank, I] and
+    ``B_banks = [B_down]`` [E, L, H, rank]; y0 [T, top_k, H] the down GEMM's
+    output; topk_weights [T, top_k] float32 routing weights."""
+    name: str
+    seed: int
+    T: int
+    top_k: int
+    E: int
+    H: int
+    I: int
+    rank: int
+    L: int
+    scale: float
+    x: np.ndarray
+    y0: np.ndarray
+    topk_ids: np.ndarray
+    lora_ids: np.ndarray
+    topk_weights: np.ndarray
+    A_banks: list
+    B_banks: list
+
+
+def moe_w2_case(seed: int = 1240, T: int = 2048, top_k: int = 8, E: int = 64, H: int = 2048,
+                I: int = 768, rank: int = 16, L: int = 8, scale: float = 2.0,
+                p_none: float = 0.2) -> MoeDownCase:
+    """The FC1 workload's routing and shapes seen from the down projection:
+    top_k distinct experts of E per token (uniform), lora_ids uniform over L
+    with p_none of -1; x ~ N(0, 1) (reading: the activation has no fan-in),
+    A ~ N(0,1)/sqrt(I), B ~ N(0,1)/sqrt(rank); routing weights a softmax of
+    N(0, 1) logits over the token's top_k (reading: the pages fix no router)."""
+    rng = np.random.default_rng(seed + 40_000)
+    topk = np.stack([rng.permutation(E)[:top_k] for _ in range(T)]).astype(np.int32)
+    lora = rng.integers(0, L, size=T).astype(np.int32)
+    lora[rng.random(T) < p_none] = -1
+    logits = rng.standard_normal(size=(T, top_k))
+    w = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    x = _normal_bf16(rng, (T * top_k, I))
+    A = [_normal_bf16(rng, (E, L, rank, I), 1.0 / np.sqrt(I))]
+    B = [_normal_bf16(rng, (E, L, H, rank), 1.0 / np.sqrt(rank))]
+    y0 = _normal_bf16(rng, (T, top_k, H))
+    return MoeDownCase(name=f"MoE w2 T={T} top_k={top_k} E={E} H={H} I={I} rank={rank}",
+                       seed=seed, T=T, top_k=top_k, E=E, H=H, I=I, rank=rank, L=L,
+                       scale=scale, x=x, y0=y0, topk_ids=topk, lora_ids=lora, topk_weights=w,
+                       A_banks=A, B_banks=B)

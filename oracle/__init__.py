@@ -70,6 +70,16 @@ def lib() -> ctypes.CDLL:
     L.oracle_moe_fc1.argtypes = [_vpp, _vpp, _vpp, ctypes.c_int64, _vpp, ctypes.c_int64,
                                  ctypes.c_int, _vpp, _vpp] + [ctypes.c_int] * 7 + [
                                      ctypes.c_float, ctypes.c_int, _u32p]
+    L.oracle_moe_w13.restype = ctypes.c_int
+    L.oracle_moe_w13.argtypes = [_vpp, _vpp, _vpp, ctypes.c_int64, _vpp, ctypes.c_int64,
+                                 ctypes.c_int, _vpp, _vpp, _vpp, ctypes.c_int, _vpp] + [
+                                     ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int,
+                                                          ctypes.c_int, _u32p]
+    L.oracle_moe_w2.restype = ctypes.c_int
+    L.oracle_moe_w2.argtypes = [_vpp, _vpp, _vpp, ctypes.c_int64, _vpp, ctypes.c_int64,
+                                _vpp, _vpp, _vpp, ctypes.c_int, _vpp, _vpp] + [
+                                    ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int,
+                                                         ctypes.c_int, _u32p]
     _LIB = L
     return L
 
@@ -274,4 +284,74 @@ def moe_fc1(x: np.ndarray, banks_a: list, banks_b: list, topk_ids: np.ndarray,
                                 int(bool(shared_a)), _p(topk_ids), _p(lora_ids), T, top_k, E, H,
                                 I, rank, num_loras, float(scale), int(acc64), ctypes.byref(err)),
            "moe_fc1")
+    return out, int(err.value)
+
+
+# ------------------------------------------------- in-place MoE w13 / w2 ----
+
+def _bank_tables(banks_a: list, banks_b: list):
+    E = banks_a[0].shape[0]
+    wa = np.array([bank[e].ctypes.data for bank in banks_a for e in range(E)], dtype=np.uint64)
+    wb = np.array([bank[e].ctypes.data for bank in banks_b for e in range(E)], dtype=np.uint64)
+    return E, wa, wb, int(np.prod(banks_a[0].shape[2:])), int(np.prod(banks_b[0].shape[2:]))
+
+
+def _opt_i32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def moe_w13(y: np.ndarray, x: np.ndarray, banks_a: list, banks_b: list, topk_ids: np.ndarray,
+            lora_ids: np.ndarray, I: int, rank: int, scale: float, shared_a: bool,
+            num_loras: int, expert_map=None, adapter_enabled=None, add_inputs: bool = True,
+            acc64: bool = False):
+    """add_lora_w13 on a copy of ``y`` [T, top_k, 2I] (bf16 bits); returns (y, err).
+
+    Banks as for :func:`moe_fc1`, indexed by the local expert id.  ``expert_map``
+    [n_global] int32 maps global expert ids to local ones (-1: not local);
+    ``adapter_enabled`` [num_loras] int32 (0: the adapter adds nothing)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H = x.shape
+    topk_ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    lora_ids = np.ascontiguousarray(lora_ids, dtype=np.int32)
+    top_k = topk_ids.shape[1]
+    E, wa, wb, stride_a, stride_b = _bank_tables(banks_a, banks_b)
+    emap, en = _opt_i32(expert_map), _opt_i32(adapter_enabled)
+    out = np.array(y, dtype=np.uint16, copy=True, order="C")
+    assert out.shape == (T, top_k, 2 * I)
+    err = ctypes.c_uint32(0)
+    _check(lib().oracle_moe_w13(_p(out), _p(x), _p(wa), stride_a, _p(wb), stride_b,
+                                int(bool(shared_a)), _p(topk_ids), _p(lora_ids), _p(emap),
+                                0 if emap is None else int(emap.size), _p(en), T, top_k, E, H,
+                                I, rank, num_loras, float(scale), int(bool(add_inputs)),
+                                int(acc64), ctypes.byref(err)), "moe_w13")
+    return out, int(err.value)
+
+
+def moe_w2(y: np.ndarray, x: np.ndarray, banks_a: list, banks_b: list, topk_ids: np.ndarray,
+           lora_ids: np.ndarray, rank: int, scale: float, num_loras: int, expert_map=None,
+           adapter_enabled=None, topk_weights=None, add_inputs: bool = True,
+           acc64: bool = False):
+    """add_lora_w2 on a copy of ``y`` [T, top_k, H] (bf16 bits); returns (y, err).
+
+    ``x`` [T * top_k, I] holds one activation row per (token, slot);
+    ``banks_a = [A_down]`` [E, L, rank, I], ``banks_b = [B_down]`` [E, L, H, rank];
+    ``topk_weights`` [T, top_k] float32 or None."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    topk_ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    lora_ids = np.ascontiguousarray(lora_ids, dtype=np.int32)
+    T, top_k = topk_ids.shape
+    I = x.shape[1]
+    assert x.shape[0] == T * top_k
+    E, wa, wb, stride_a, stride_b = _bank_tables(banks_a, banks_b)
+    H = banks_b[0].shape[2]
+    emap, en = _opt_i32(expert_map), _opt_i32(adapter_enabled)
+    wts = None if topk_weights is None else np.ascontiguousarray(topk_weights, dtype=np.float32)
+    out = np.array(y, dtype=np.uint16, copy=True, order="C")
+    assert out.shape == (T, top_k, H)
+    err = ctypes.c_uint32(0)
+    _check(lib().oracle_moe_w2(_p(out), _p(x), _p(wa), stride_a, _p(wb), stride_b,
+                               _p(topk_ids), _p(lora_ids), _p(emap),
+                               0 if emap is None else int(emap.size), _p(en), _p(wts), T, top_k,
+                               E, H, I, rank, num_loras, float(scale), int(bool(add_inputs)),
+                               int(acc64), ctypes.byref(err)), "moe_w2")
     return out, int(err.value)

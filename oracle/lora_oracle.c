@@ -428,3 +428,165 @@ int oracle_moe_fc1(uint16_t *out, const uint16_t *x, const uint16_t *const *w_pt
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* In-place MoE LoRA around the two expert GEMMs.  [punica] add_lora_w13 */
+/* adds the gate/up delta to y = intermediate_cache1 [T, top_k, 2I] in   */
+/* place, before the activation; add_lora_w2 adds the down delta to      */
+/* y = intermediate_cache3 [T, top_k, H] in place, before moe_sum, from  */
+/* x = intermediate_cache2 [T * top_k, I], one input row per (token,     */
+/* slot).  Per pair the delta is the [flashinfer] one:                   */
+/*   w13: scale * concat(B_gate @ (A_gate @ x[t]), B_up @ (A_up @ x[t])) */
+/*        or scale * B_fused @ (A_shared @ x[t]);                        */
+/*   w2:  scale * B_down @ (A_down @ x[t * top_k + j]), A_down [rank, I], */
+/*        B_down [H, rank].                                              */
+/* Readings (the page gives signatures and docstrings only):             */
+/*   - the pair's adapter is lora_ids[t] (the token-to-adapter mapping); */
+/*     l < 0, or adapter_enabled[l] == 0 when that table is given, means */
+/*     no delta; l >= num_loras is an error (no delta, bit 4);           */
+/*   - expert_map, when given, maps a global expert id in [0, n_global)  */
+/*     to this rank's local id, -1 = not on this rank (no delta); a      */
+/*     global id outside the map or a local id outside [0, E) is an      */
+/*     error (no delta, bit 2);                                          */
+/*   - y is the caller's buffer: a pair with no delta is left untouched; */
+/*   - add_inputs: y = RN(f32(y) + v), else y = RN(v), on pairs with a   */
+/*     delta;                                                            */
+/*   - w2 with topk_weights: v = w[t, j] * (scale * d), the routing       */
+/*     weight that the down GEMM applied before moe_sum; without them    */
+/*     v = scale * d.                                                    */
+/* ------------------------------------------------------------------ */
+
+/* The (adapter, local expert) of pair p; 0 when the pair gets no delta. */
+static int moe_pair_key(int64_t p, int top_k, const int32_t *topk_ids, const int32_t *lora_ids,
+                        const int32_t *expert_map, int n_global, const int32_t *adapter_enabled,
+                        int E, int num_loras, int *l_out, int *e_out, uint32_t *err)
+{
+    int l = lora_ids[p / top_k];
+    int e = topk_ids[p];
+    uint32_t bit = 0;
+    if (l < 0)
+        return 0;
+    if (l >= num_loras) {
+        bit = ORACLE_ERR_LORA;
+    } else if (adapter_enabled && adapter_enabled[l] == 0) {
+        return 0;
+    } else if (expert_map) {
+        if (e < 0 || e >= n_global)
+            bit = ORACLE_ERR_EXPERT;
+        else if (expert_map[e] < 0)
+            return 0;
+        else if (expert_map[e] >= E)
+            bit = ORACLE_ERR_EXPERT;
+        else
+            e = expert_map[e];
+    } else if (e < 0 || e >= E) {
+        bit = ORACLE_ERR_EXPERT;
+    }
+    if (bit) {
+        if (err) {
+#pragma omp atomic
+            *err |= bit;
+        }
+        return 0;
+    }
+    *l_out = l;
+    *e_out = e;
+    return 1;
+}
+
+/* y[c] (c < width) gets the delta scale * B @ (A @ x) of one pair, with
+ * A [rank, k_in] and B [width, rank] row-major; `w` multiplies the folded
+ * value when has_w. */
+static void moe_pair_fold(uint16_t *y, const uint16_t *xrow, int k_in, const uint16_t *A,
+                          const uint16_t *B, int width, int rank, float scale, int has_w,
+                          float w, int add_inputs, int acc64)
+{
+    float hf[512];
+    double hd[512];
+    for (int q = 0; q < rank; ++q) {
+        const uint16_t *arow = A + (size_t)q * k_in;
+        if (acc64) {
+            double acc = 0.0;
+            for (int k = 0; k < k_in; ++k)
+                acc += (double)oracle_bf16_to_f32(xrow[k]) * (double)oracle_bf16_to_f32(arow[k]);
+            hd[q] = acc;
+        } else {
+            float acc = 0.0f;
+            for (int k = 0; k < k_in; ++k)
+                acc += oracle_bf16_to_f32(xrow[k]) * oracle_bf16_to_f32(arow[k]);
+            hf[q] = acc;
+        }
+    }
+    for (int c = 0; c < width; ++c) {
+        const uint16_t *brow = B + (size_t)c * rank;
+        if (acc64) {
+            double d = 0.0;
+            for (int q = 0; q < rank; ++q)
+                d += hd[q] * (double)oracle_bf16_to_f32(brow[q]);
+            double v = (double)scale * d;
+            if (has_w)
+                v = (double)w * v;
+            y[c] = oracle_f64_to_bf16(add_inputs ? (double)oracle_bf16_to_f32(y[c]) + v : v);
+        } else {
+            float d = 0.0f;
+            for (int q = 0; q < rank; ++q)
+                d += hf[q] * oracle_bf16_to_f32(brow[q]);
+            float v = scale * d;
+            if (has_w)
+                v = w * v;
+            y[c] = oracle_f32_to_bf16(add_inputs ? oracle_bf16_to_f32(y[c]) + v : v);
+        }
+    }
+}
+
+int oracle_moe_w13(uint16_t *y, const uint16_t *x, const uint16_t *const *w_ptr_a,
+                   int64_t stride_a, const uint16_t *const *w_ptr_b, int64_t stride_b,
+                   int shared_a, const int32_t *topk_ids, const int32_t *lora_ids,
+                   const int32_t *expert_map, int n_global, const int32_t *adapter_enabled,
+                   int T, int top_k, int E, int H, int I, int rank, int num_loras, float scale,
+                   int add_inputs, int acc64, uint32_t *err)
+{
+    if (T < 0 || top_k < 0 || E <= 0 || H < 0 || I < 0 || rank < 0 || rank > 512 ||
+        (expert_map && n_global <= 0))
+        return 1;
+    const int n_slices = shared_a ? 1 : 2;
+    const int width = shared_a ? 2 * I : I;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (int64_t p = 0; p < (int64_t)T * top_k; ++p) {
+        int l, e;
+        if (!moe_pair_key(p, top_k, topk_ids, lora_ids, expert_map, n_global, adapter_enabled, E,
+                          num_loras, &l, &e, err))
+            continue;
+        const uint16_t *xrow = x + (size_t)(p / top_k) * H;
+        for (int j = 0; j < n_slices; ++j)
+            moe_pair_fold(y + (size_t)p * 2 * I + (size_t)j * I, xrow, H,
+                          w_ptr_a[(size_t)j * E + e] + (size_t)l * stride_a,
+                          w_ptr_b[(size_t)j * E + e] + (size_t)l * stride_b, width, rank, scale,
+                          0, 1.0f, add_inputs, acc64);
+    }
+    return 0;
+}
+
+int oracle_moe_w2(uint16_t *y, const uint16_t *x, const uint16_t *const *w_ptr_a,
+                  int64_t stride_a, const uint16_t *const *w_ptr_b, int64_t stride_b,
+                  const int32_t *topk_ids, const int32_t *lora_ids, const int32_t *expert_map,
+                  int n_global, const int32_t *adapter_enabled, const float *topk_weights,
+                  int T, int top_k, int E, int H, int I, int rank, int num_loras, float scale,
+                  int add_inputs, int acc64, uint32_t *err)
+{
+    if (T < 0 || top_k < 0 || E <= 0 || H < 0 || I < 0 || rank < 0 || rank > 512 ||
+        (expert_map && n_global <= 0))
+        return 1;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (int64_t p = 0; p < (int64_t)T * top_k; ++p) {
+        int l, e;
+        if (!moe_pair_key(p, top_k, topk_ids, lora_ids, expert_map, n_global, adapter_enabled, E,
+                          num_loras, &l, &e, err))
+            continue;
+        moe_pair_fold(y + (size_t)p * H, x + (size_t)p * I, I,
+                      w_ptr_a[e] + (size_t)l * stride_a, w_ptr_b[e] + (size_t)l * stride_b, H,
+                      rank, scale, topk_weights != NULL,
+                      topk_weights ? topk_weights[p] : 1.0f, add_inputs, acc64);
+    }
+    return 0;
+}

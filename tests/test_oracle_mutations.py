@@ -3,7 +3,8 @@
 Each case copies ``oracle/lora_oracle.c``, plants one plausible mistake (a
 dropped term, a transposed operand, a wrong index or offset, a missing scale, a
 wrong tie rule, an unstable sort, non-zero padding, swapped MoE slices, a wrong
-adapter stride), compiles the copy into a temporary library and runs the pin
+adapter stride, a per-token input row for the down projection, a dropped routing
+weight, a non-local expert treated as local, a disabled adapter applied), compiles the copy into a temporary library and runs the pin
 suite against it in a subprocess.  The pins must fail for every mutant.
 """
 import os
@@ -43,6 +44,18 @@ MUTANTS = {
     "moe_wrong_adapter_stride": (
         "            const uint16_t *B = w_ptr_b[(size_t)j * E + e] + (size_t)l * stride_b;",
         "            const uint16_t *B = w_ptr_b[(size_t)j * E + e] + (size_t)l * (stride_b / 2);"),
+    "moe_w2_x_per_token": (
+        "        moe_pair_fold(y + (size_t)p * H, x + (size_t)p * I, I,",
+        "        moe_pair_fold(y + (size_t)p * H, x + (size_t)(p / top_k) * I, I,"),
+    "moe_w2_weight_dropped": (
+        "            if (has_w)\n                v = w * v;",
+        "            if (has_w)\n                v = 1.0f * v;"),
+    "moe_nonlocal_expert_as_zero": (
+        "        else if (expert_map[e] < 0)\n            return 0;",
+        "        else if (expert_map[e] < 0)\n            e = 0;"),
+    "moe_disabled_adapter_applied": (
+        "adapter_enabled && adapter_enabled[l] == 0)",
+        "adapter_enabled && adapter_enabled[l] == 2)"),
 }
 
 

@@ -430,3 +430,167 @@ def test_moe_skipped_pairs_are_zero_and_flag_errors(oracle):
     assert not o[0].any() and not o[1].any() and not o[2, 1].any()
     assert o[2, 0].any() and o[3].any()
     assert err == (4 | 2)
+
+
+# ----------------------------------------------------- in-place MoE w13 / w2 --
+
+def _pair_delta64(A, B, xrow, scale):
+    """scale * B @ (A @ x) in fp64 numpy (A [rank, k], B [w, rank] bf16 bits)."""
+    h = f32(A).astype(np.float64) @ f32(xrow).astype(np.float64)
+    return scale * (f32(B).astype(np.float64) @ h)
+
+
+def _rne_row(vals):
+    return [rne_bf16(Fraction(float(v))) for v in vals]
+
+
+def test_moe_w13_in_place_matches_fp64_formula(oracle):
+    """'punica_base.py' add_lora_w13: the gate/up delta of 'bgmv_moe_gemm1_lora_delta'
+    added to intermediate_cache1 in place, y = RN(y + delta); pairs with no adapter
+    keep y bit for bit.  fp64 oracle == correctly rounded fp64 numpy."""
+    for shared in (False, True):
+        c = _moe_small(shared, seed=21)
+        y0 = inputs.moe_y0(21, (c.T, c.top_k, 2 * c.I))
+        y, err = oracle.moe_w13(y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I,
+                                c.rank, c.scale, shared, c.L, acc64=True)
+        assert err == 0
+        want = y0.copy()
+        for t in range(c.T):
+            l = int(c.lora_ids[t])
+            if l < 0:
+                continue
+            for j in range(c.top_k):
+                e = int(c.topk_ids[t, j])
+                if shared:
+                    d = _pair_delta64(c.A_banks[0][e, l], c.B_banks[0][e, l], c.x[t], c.scale)
+                else:
+                    d = np.concatenate([
+                        _pair_delta64(c.A_banks[0][e, l], c.B_banks[0][e, l], c.x[t], c.scale),
+                        _pair_delta64(c.A_banks[1][e, l], c.B_banks[1][e, l], c.x[t], c.scale)])
+                want[t, j] = _rne_row(f32(y0[t, j]).astype(np.float64) + d)
+        assert np.array_equal(y, want)
+        assert np.array_equal(y[c.lora_ids < 0], y0[c.lora_ids < 0])
+        y32, _ = oracle.moe_w13(y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I,
+                                c.rank, c.scale, shared, c.L)
+        assert bf16_ulp_distance(y32, want).max() <= 1
+
+
+def test_moe_w13_overwrite_writes_only_adapted_pairs(oracle):
+    """add_inputs=False writes RN(delta) on the pairs that have an adapter (the FC1
+    values of 'bgmv_moe_gemm1_lora_delta'); the other pairs keep the caller's y."""
+    c = _moe_small(False, seed=23)
+    poison = np.full((c.T, c.top_k, 2 * c.I), 0x7FC1, dtype=np.uint16)
+    y, _ = oracle.moe_w13(poison, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I,
+                          c.rank, c.scale, False, c.L, add_inputs=False, acc64=True)
+    fc1, _ = oracle.moe_fc1(c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I, c.rank,
+                            c.scale, False, c.L, acc64=True)
+    ad = c.lora_ids >= 0
+    assert np.array_equal(y[ad], fc1[ad])
+    assert (y[~ad] == 0x7FC1).all()
+
+
+def test_moe_expert_map_selects_local_experts(oracle):
+    """'punica_base.py' add_lora_w13 expert_map: global expert ids map to this rank's
+    local ids, -1 = not local.  Eight global experts, four local (global 1, 3, 6, 7 in
+    a shuffled local order): pairs on a local expert get that expert's adapter, the
+    others keep y; an id past the map or a map entry >= E flags bit 2."""
+    c = _moe_small(False, seed=25, E=8, p_none=0.0)
+    local_of = {1: 2, 3: 0, 6: 3, 7: 1}
+    emap = np.full(8, -1, dtype=np.int32)
+    for g, loc in local_of.items():
+        emap[g] = loc
+    inv = {loc: g for g, loc in local_of.items()}
+    banks_a = [np.ascontiguousarray(b[[inv[i] for i in range(4)]]) for b in c.A_banks]
+    banks_b = [np.ascontiguousarray(b[[inv[i] for i in range(4)]]) for b in c.B_banks]
+    y0 = inputs.moe_y0(25, (c.T, c.top_k, 2 * c.I))
+    y, err = oracle.moe_w13(y0, c.x, banks_a, banks_b, c.topk_ids, c.lora_ids, c.I, c.rank,
+                            c.scale, False, c.L, expert_map=emap, acc64=True)
+    assert err == 0
+    want = y0.copy()
+    for t in range(c.T):
+        l = int(c.lora_ids[t])
+        for j in range(c.top_k):
+            g = int(c.topk_ids[t, j])
+            if g not in local_of:
+                continue
+            d = np.concatenate([
+                _pair_delta64(c.A_banks[0][g, l], c.B_banks[0][g, l], c.x[t], c.scale),
+                _pair_delta64(c.A_banks[1][g, l], c.B_banks[1][g, l], c.x[t], c.scale)])
+            want[t, j] = _rne_row(f32(y0[t, j]).astype(np.float64) + d)
+    assert np.array_equal(y, want)
+    assert any(int(g) not in local_of for g in c.topk_ids.ravel())
+    bad_map = emap.copy()
+    bad_map[3] = 4  # local id past E
+    topk = c.topk_ids.copy()
+    topk[0, 0] = 8  # global id past the map
+    yb, err = oracle.moe_w13(y0, c.x, banks_a, banks_b, topk, c.lora_ids, c.I, c.rank,
+                             c.scale, False, c.L, expert_map=bad_map)
+    assert err == 2
+    assert np.array_equal(yb[0, 0], y0[0, 0])
+
+
+def test_moe_adapter_enabled_switches_adapters_off(oracle):
+    """adapter_enabled: an adapter marked 0 adds nothing (its pairs keep y bit for
+    bit); all ones is the same as no table."""
+    c = _moe_small(False, seed=27)
+    y0 = inputs.moe_y0(27, (c.T, c.top_k, 2 * c.I))
+    args = (c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I, c.rank, c.scale, False, c.L)
+    base, _ = oracle.moe_w13(y0, *args)
+    ones, _ = oracle.moe_w13(y0, *args, adapter_enabled=np.ones(c.L, np.int32))
+    assert np.array_equal(base, ones)
+    en = np.ones(c.L, np.int32)
+    en[1] = 0
+    part, _ = oracle.moe_w13(y0, *args, adapter_enabled=en)
+    off = c.lora_ids == 1
+    assert off.any()
+    assert np.array_equal(part[off], y0[off])
+    assert np.array_equal(part[~off], base[~off])
+
+
+def _w2_small(seed=31, **kw):
+    args = dict(T=20, top_k=3, E=5, H=40, I=24, rank=4, L=3, scale=2.0, p_none=0.25)
+    args.update(kw)
+    return inputs.moe_w2_case(seed=seed, **args)
+
+
+def test_moe_w2_matches_fp64_formula_per_pair_row(oracle):
+    """'punica_base.py' add_lora_w2: intermediate_cache3 [T, top_k, H] gets, in place,
+    w[t, j] * scale * B_down[l,e] @ (A_down[l,e] @ x[t*top_k + j]), x being the
+    activation row of that (token, slot); fp64 oracle == correctly rounded numpy,
+    with and without routing weights."""
+    c = _w2_small()
+    for weights in (None, c.topk_weights):
+        y, err = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.rank,
+                               c.scale, c.L, topk_weights=weights, acc64=True)
+        assert err == 0
+        want = c.y0.copy()
+        for t in range(c.T):
+            l = int(c.lora_ids[t])
+            if l < 0:
+                continue
+            for j in range(c.top_k):
+                e = int(c.topk_ids[t, j])
+                d = _pair_delta64(c.A_banks[0][e, l], c.B_banks[0][e, l], c.x[t * c.top_k + j],
+                                  c.scale)
+                if weights is not None:
+                    d = float(weights[t, j]) * d
+                want[t, j] = _rne_row(f32(c.y0[t, j]).astype(np.float64) + d)
+        assert np.array_equal(y, want)
+        y32, _ = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.rank,
+                               c.scale, c.L, topk_weights=weights)
+        assert bf16_ulp_distance(y32, want).max() <= 1
+
+
+def test_moe_w2_weight_two_is_double_scale(oracle):
+    """Multiplying by two is exact in binary floating point, so a routing weight of 2
+    on every pair gives bit for bit the result of twice the scale and no weights."""
+    c = _w2_small(seed=33)
+    w2x = np.full((c.T, c.top_k), 2.0, np.float32)
+    a, _ = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.rank,
+                         c.scale, c.L, topk_weights=w2x)
+    b, _ = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.rank,
+                         2 * c.scale, c.L)
+    assert np.array_equal(a, b)
+    plain, _ = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.rank,
+                             c.scale, c.L)
+    assert not np.array_equal(a, plain)
