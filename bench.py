@@ -419,6 +419,8 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src, only=
         _fold(ld, di, inputs, device, hbm_peak, timed, res)
     if only in (None, "moe"):
         _moe(ld, di, inputs, device, hbm_peak, timed, res)
+    if only in (None, "moe_inplace"):
+        _moe_inplace(ld, di, inputs, device, hbm_peak, timed, res)
     res["peak_source"] = peak_src
     return res
 
@@ -505,8 +507,53 @@ def _moe(ld, di, inputs, device, hbm_peak, timed, res):
         res["moe_fc1_" + ("shared" if shared else "regular")] = {
             "pairs_per_s": round(mc.T * mc.top_k / (ms / 1e3), 1), "ms": round(ms, 4),
             "routed_pairs": pairs, "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
-            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 3}
+            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 4}
         del dm, out, ws
+        torch.cuda.empty_cache()
+
+
+def _moe_inplace(ld, di, inputs, device, hbm_peak, timed, res):
+    import numpy as np
+    import torch
+    # in-place MoE deltas on either side of the activation, FC1's routing:
+    # w13 (gate/up, regular banks) into intermediate_cache1, w2 (down, with
+    # routing weights) into intermediate_cache3 from per-pair activations
+    mc = inputs.moe_case()
+    c2 = inputs.moe_w2_case()
+    for name, case in (("moe_w13_inplace", mc), ("moe_w2_inplace_weighted", c2)):
+        dm = di.moe_to_device(case, device)
+        valid = case.lora_ids >= 0
+        pairs = int(valid.sum()) * case.top_k
+        keys = {(int(l), int(e)) for t in np.flatnonzero(valid) for l, e in
+                zip([case.lora_ids[t]] * case.top_k, case.topk_ids[t])}
+        if name == "moe_w13_inplace":
+            y = di.bf16(inputs.moe_y0(mc.seed, (mc.T, mc.top_k, 2 * mc.I)), device)
+            ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L, mc.rank,
+                                                        False), dtype=torch.uint8, device=device)
+            fn = lambda: ld.lora_moe_w13_delta(y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b,
+                                               dm.stride_b, False, dm.topk_ids, dm.lora_ids,
+                                               mc.E, mc.I, mc.rank, mc.L, mc.scale, workspace=ws)
+            bank = len(keys) * (2 * mc.rank * mc.H * 2 + 2 * mc.I * mc.rank * 2)
+            ab = bank + pairs * 2 * mc.I * 2 * 2 + int(valid.sum()) * mc.H * 2
+        else:
+            y = di.bf16(case.y0, device)
+            wts = torch.from_numpy(case.topk_weights).to(device)
+            ws = torch.empty(ld.lora_moe_workspace_size(case.T, case.top_k, case.E, case.L,
+                                                        case.rank, True),
+                             dtype=torch.uint8, device=device)
+            fn = lambda: ld.lora_moe_w2_delta(y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b,
+                                              dm.stride_b, dm.topk_ids, dm.lora_ids, case.E,
+                                              case.H, case.rank, case.L, case.scale,
+                                              topk_weights=wts, workspace=ws)
+            bank = len(keys) * (case.rank * case.I * 2 + case.H * case.rank * 2)
+            ab = bank + pairs * case.H * 2 * 2 + pairs * case.I * 2
+        ms = timed(fn)
+        res[name] = {"pairs_per_s": round(case.T * case.top_k / (ms / 1e3), 1),
+                     "ms": round(ms, 4), "routed_pairs": pairs,
+                     "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
+                     "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                     "launches_per_call": 3}
+        del dm, y, ws
         torch.cuda.empty_cache()
 
 
@@ -560,7 +607,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads (prefill, skewed, MoE)")
-    ap.add_argument("--only", choices=["prefill", "skewed", "moe", "fold"], default=None,
+    ap.add_argument("--only", choices=["prefill", "skewed", "moe", "fold", "moe_inplace"], default=None,
                     help="time one of the other workloads alone and print its numbers "
                          "(for profiling captures; not the benchmark line)")
     args = ap.parse_args()

@@ -25,7 +25,8 @@
  *
  * Pages the calls follow (cited per call below):
  *  [punica]     "vllm/lora/punica_wrapper/punica_base.py": add_shrink,
- *               add_expand, add_lora_linear "Semantics"; prefill_metadata.
+ *               add_expand, add_lora_linear "Semantics"; prefill_metadata;
+ *               add_lora_w13 / add_lora_w2 (in-place MoE deltas).
  *  [sharded]    "vllm.lora.fully_sharded_layers": the float32 shrink buffer
  *               and the shrink-with-scale-1.0 then expand sequence.
  *  [metrale]    "Module lora_delta": LoraPair / LoraRoute layouts, the
@@ -238,6 +239,62 @@ int lora_moe_fc1_delta(void *out, const void *x, const int64_t *w_ptr_a, int64_t
                        const int32_t *topk_ids, const int32_t *lora_ids, int T, int top_k, int E,
                        int H, int I, int rank, int num_loras, float scale, void *workspace,
                        size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_moe_w13_delta -- [punica] add_lora_w13: the gate/up delta of
+ * lora_moe_fc1_delta added IN PLACE to y = intermediate_cache1
+ * [T, top_k, 2I] bf16 (the expert gate/up GEMM's output, before the
+ * activation):
+ *   y[t, j, :] = RN_bf16(y[t, j, :] + delta[t, j, :])     (add_inputs != 0)
+ *   y[t, j, :] = RN_bf16(delta[t, j, :])                   (add_inputs == 0)
+ * with delta and the bank tables, strides and layouts exactly as
+ * lora_moe_fc1_delta (regular or shared-A / fused-B mode).  Routing, per pair
+ * (t, j): l = lora_ids[t] (the token-to-adapter mapping), e = topk_ids[t, j];
+ *   - expert_map [n_global_experts] int32 (device, or NULL = identity):
+ *     global expert id -> this rank's local id in [0, E), -1 = the expert
+ *     is not on this rank (no delta).  A global id outside the map or a
+ *     local id >= E sets LORA_DEV_ERR_EXPERT (no delta);
+ *   - adapter_enabled [num_loras] int32 (device, or NULL): an adapter with
+ *     entry 0 adds nothing;
+ *   - l < 0: no delta; l >= num_loras: no delta + LORA_DEV_ERR_LORA.
+ * A pair without a delta is left untouched (y belongs to the caller).
+ * Requirements as lora_moe_fc1_delta, with E the local expert count; the
+ * workspace is lora_moe_workspace_size(T, top_k, E, num_loras, rank,
+ * shared_a) bytes.  Readings: the page gives the signature and docstring
+ * only; routing weights are not applied before the activation.
+ */
+int lora_moe_w13_delta(void *y, const void *x, const int64_t *w_ptr_a, int64_t stride_a,
+                       const int64_t *w_ptr_b, int64_t stride_b, int shared_a,
+                       const int32_t *topk_ids, const int32_t *lora_ids,
+                       const int32_t *expert_map, int n_global_experts,
+                       const int32_t *adapter_enabled, int T, int top_k, int E, int H, int I,
+                       int rank, int num_loras, float scale, int add_inputs, void *workspace,
+                       size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
+ * lora_moe_w2_delta -- [punica] add_lora_w2: the down-projection delta added
+ * IN PLACE to y = intermediate_cache3 [T, top_k, H] bf16 (the expert down
+ * GEMM's per-pair output, before moe_sum), from x = intermediate_cache2
+ * [T * top_k, I] bf16, one activation row per (token, slot) pair p = t *
+ * top_k + j:
+ *   v[c] = w_p * scale * sum_r B[l,e][c, r] * (A[l,e] x[p])[r]      (fp32)
+ *   y[t, j, c] = RN_bf16(y[t, j, c] + v[c])  (add_inputs != 0), else RN_bf16(v[c])
+ * w_ptr_a / w_ptr_b: [E] int64 tables of bank base addresses; adapter l of a
+ * bank starts l * stride elements after its base; A[l,e] [rank, I] and
+ * B[l,e] [H, rank] row-major bf16.  topk_weights [T, top_k] fp32 (device, or
+ * NULL: w_p = 1) are the routing weights the down GEMM applied before
+ * moe_sum.  Routing (expert_map, adapter_enabled, lora_ids, errors) and the
+ * untouched pairs as lora_moe_w13_delta.  Requires H, I, rank multiples of 8,
+ * rank <= 128, E * num_loras <= 3071 and a workspace of
+ * lora_moe_workspace_size(T, top_k, E, num_loras, rank, 1) bytes (one slice).
+ */
+int lora_moe_w2_delta(void *y, const void *x, const int64_t *w_ptr_a, int64_t stride_a,
+                      const int64_t *w_ptr_b, int64_t stride_b, const int32_t *topk_ids,
+                      const int32_t *lora_ids, const int32_t *expert_map, int n_global_experts,
+                      const int32_t *adapter_enabled, const float *topk_weights, int T,
+                      int top_k, int E, int H, int I, int rank, int num_loras, float scale,
+                      int add_inputs, void *workspace, size_t ws_bytes, uint32_t *err_word,
+                      lora_stream_t stream);
 
 /*
  * lora_delta_fused_noalloc -- lora_delta_fused for callers that cannot

@@ -25,7 +25,8 @@ __all__ = [
     "lora_workspace_size", "lora_workspace_min_size", "lora_route", "lora_route_scratch_size",
     "lora_route_with_scratch", "lora_shrink", "lora_expand", "lora_delta_fused",
     "lora_delta_segmented",
-    "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_get_error", "new_error_word",
+    "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_moe_w13_delta",
+    "lora_moe_w2_delta", "lora_get_error", "new_error_word",
     "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes",
 ]
 
@@ -324,6 +325,67 @@ def lora_moe_fc1_delta(out, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, s
         _ptr(out), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
         int(bool(shared_a)), _ptr(topk_ids), _ptr(lora_ids), T, top_k, int(E), H, int(I),
         int(rank), int(num_loras), float(scale), _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def _opt_dev(t, name, dtype):
+    if t is None:
+        return None
+    _dev(t, name, dtype)
+    return t
+
+
+def lora_moe_w13_delta(y, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, shared_a: bool,
+                       topk_ids, lora_ids, E: int, I: int, rank: int, num_loras: int,
+                       scale: float, expert_map=None, adapter_enabled=None,
+                       add_inputs: bool = True, workspace=None, err=None, stream=None):
+    """add_lora_w13: the gate/up delta added in place to ``y`` [T, top_k, 2I] bf16."""
+    _dev(y, "y", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(topk_ids, "topk_ids", torch.int32)
+    _dev(lora_ids, "lora_ids", torch.int32)
+    _dev(w_ptr_a, "w_ptr_a", torch.int64)
+    _dev(w_ptr_b, "w_ptr_b", torch.int64)
+    _opt_dev(expert_map, "expert_map", torch.int32)
+    _opt_dev(adapter_enabled, "adapter_enabled", torch.int32)
+    T, H = x.shape
+    top_k = topk_ids.shape[1]
+    ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras, rank, shared_a),
+                         workspace, x.device)
+    _check("lora_moe_w13_delta", lib().lora_moe_w13_delta(
+        _ptr(y), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
+        int(bool(shared_a)), _ptr(topk_ids), _ptr(lora_ids), _ptr(expert_map),
+        0 if expert_map is None else expert_map.numel(), _ptr(adapter_enabled), T, top_k,
+        int(E), H, int(I), int(rank), int(num_loras), float(scale), int(bool(add_inputs)),
+        _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_moe_w2_delta(y, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, topk_ids,
+                      lora_ids, E: int, H: int, rank: int, num_loras: int, scale: float,
+                      expert_map=None, adapter_enabled=None, topk_weights=None,
+                      add_inputs: bool = True, workspace=None, err=None, stream=None):
+    """add_lora_w2: the down delta added in place to ``y`` [T, top_k, H] bf16 from the
+    per-pair activations ``x`` [T * top_k, I]."""
+    _dev(y, "y", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(topk_ids, "topk_ids", torch.int32)
+    _dev(lora_ids, "lora_ids", torch.int32)
+    _dev(w_ptr_a, "w_ptr_a", torch.int64)
+    _dev(w_ptr_b, "w_ptr_b", torch.int64)
+    _opt_dev(expert_map, "expert_map", torch.int32)
+    _opt_dev(adapter_enabled, "adapter_enabled", torch.int32)
+    _opt_dev(topk_weights, "topk_weights", torch.float32)
+    T, top_k = topk_ids.shape
+    I = x.shape[1]
+    if x.shape[0] != T * top_k:
+        raise ValueError("x must hold one row per (token, slot) pair")
+    ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras, rank, True),
+                         workspace, x.device)
+    _check("lora_moe_w2_delta", lib().lora_moe_w2_delta(
+        _ptr(y), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
+        _ptr(topk_ids), _ptr(lora_ids), _ptr(expert_map),
+        0 if expert_map is None else expert_map.numel(), _ptr(adapter_enabled),
+        _ptr(topk_weights), T, top_k, int(E), int(H), I, int(rank), int(num_loras),
+        float(scale), int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
 
 
 def lora_get_error(err: torch.Tensor, clear: bool = True, stream=None) -> int:

@@ -38,6 +38,10 @@ SIGNATURES = {
     "lora_moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "lora_moe_fc1_delta": (_i, [_vp, _vp, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i, _i, _i, _i, _i,
                                 _i, _i, _f, _vp, _sz, _vp, _vp]),
+    "lora_moe_w13_delta": (_i, [_vp, _vp, _vp, _i64, _vp, _i64, _i, _vp, _vp, _vp, _i, _vp,
+                                _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp, _vp]),
+    "lora_moe_w2_delta": (_i, [_vp, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i, _vp, _vp,
+                               _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp, _vp]),
     "lora_get_error": (_i, [_vp, _vp, _i, _vp]),
     "lora_noalloc_scratch_bytes": (_sz, []),
     "lora_delta_fused_noalloc": (_i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i,

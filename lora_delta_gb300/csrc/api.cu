@@ -802,62 +802,83 @@ size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras, int rank,
   return ws_bytes_for(T * top_k, E * num_loras, hs, kMaxKSplit);
 }
 
-int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t stride_a,
-                       const int64_t* w_ptr_b, int64_t stride_b, int shared_a,
-                       const int32_t* topk_ids, const int32_t* lora_ids, int T, int top_k, int E,
-                       int H, int I, int rank, int num_loras, float scale, void* workspace,
-                       size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
-  if (T < 0 || top_k < 0 || E < 1 || H < 0 || I < 0 || num_loras < 1 || stride_a < 0 ||
-      stride_b < 0)
-    return LORA_ERR_ARG;
-  const int64_t n64 = (int64_t)T * top_k;
-  if (n64 == 0 || I == 0) return LORA_OK;
+}  // extern "C"
+
+namespace {
+
+// One routed-MoE delta over the T * top_k (token, slot) pairs, keyed by
+// (adapter, local expert): FC1 (fresh output), w13 and w2 (in place).
+struct MoeCall {
+  void* out;
+  int64_t ld_out;
+  const void* x;
+  int64_t ld_x;
+  int k_in, x_div, n_slices;
+  int32_t widths[2];
+  const int64_t *w_ptr_a, *w_ptr_b;
+  int64_t stride_a, stride_b;
+  const int32_t *topk_ids, *lora_ids, *expert_map, *adapter_enabled;
+  const float* pair_weight;
+  int n_global, T, top_k, E, H, I, rank, num_loras;
+  float scale;
+  int add_inputs;
+  int zero_skipped;  // write zeros on the pairs with no delta (fresh output)
+};
+
+int moe_delta(const MoeCall& c, void* workspace, size_t ws_bytes, uint32_t* err_word,
+              cudaStream_t s) {
+  const int64_t n64 = (int64_t)c.T * c.top_k;
+  const int n_cols = c.widths[0] + (c.n_slices > 1 ? c.widths[1] : 0);
+  if (n64 == 0 || n_cols == 0) return LORA_OK;
   if (n64 > (1 << 30)) return LORA_ERR_UNSUPPORTED;
-  if (!out || !x || !w_ptr_a || !w_ptr_b || !topk_ids || !lora_ids) return LORA_ERR_ARG;
-  if ((int64_t)E * num_loras > kMaxKeys) return LORA_ERR_UNSUPPORTED;
-  const int n_slices = shared_a ? 1 : 2;
-  int rc = check_rank(n_slices, rank);
+  if (!c.out || !c.x || !c.w_ptr_a || !c.w_ptr_b || !c.topk_ids || !c.lora_ids)
+    return LORA_ERR_ARG;
+  if (c.expert_map && c.n_global < 1) return LORA_ERR_ARG;
+  if ((int64_t)c.E * c.num_loras > kMaxKeys) return LORA_ERR_UNSUPPORTED;
+  int rc = check_rank(c.n_slices, c.rank);
   if (rc) return rc;
-  if (H % 8 || I % 8 || stride_a % 8 || stride_b % 8 || !aligned16(out) || !aligned16(x))
+  if (c.H % 8 || c.I % 8 || c.k_in % 8 || n_cols % 8 || c.ld_x % 8 || c.ld_out % 8 || c.stride_a % 8 ||
+      c.stride_b % 8 || !aligned16(c.out) || !aligned16(c.x))
     return LORA_ERR_ALIGN;
-  const int n = (int)n64, n_keys = E * num_loras;
-  const int hs = (n_slices * rank + 15) / 16 * 16;
+  const int n = (int)n64, n_keys = c.E * c.num_loras;
+  const int hs = (c.n_slices * c.rank + 15) / 16 * 16;
   if (!workspace || ws_bytes < ws_bytes_for(n, n_keys, hs)) return LORA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
-  cudaStream_t s = (cudaStream_t)stream;
   const Workspace w = carve(workspace, n, n_keys);
   int32_t* perm = w.perm;
   int32_t* seg = w.seg;
-  rc = launch_route_scratch(MoeKey{topk_ids, lora_ids, top_k, E, num_loras}, n, n_keys, perm,
-                            seg, w.rcounts, err_word, s);
+  rc = launch_route_scratch(MoeKey{c.topk_ids, c.lora_ids, c.expert_map, c.adapter_enabled,
+                                   c.top_k, c.E, c.num_loras, c.n_global},
+                            n, n_keys, perm, seg, w.rcounts, err_word, s);
   if (rc) return rc;
 
   DeltaArgs a = {};
-  int32_t widths[2] = {shared_a ? 2 * I : I, I};
-  if ((rc = make_slices(widths, n_slices, 0, a.sl, a.rel))) return rc;
-  a.out = (__nv_bfloat16*)out;
-  a.ld_out = 2 * (int64_t)I;
-  a.x = (const __nv_bfloat16*)x;
-  a.ld_x = H;
-  a.k_in = H;
-  a.R = rank;
-  a.add_inputs = 0;
-  a.sr_max = n_slices * rank;
+  if ((rc = make_slices(c.widths, c.n_slices, 0, a.sl, a.rel))) return rc;
+  a.out = (__nv_bfloat16*)c.out;
+  a.ld_out = c.ld_out;
+  a.x = (const __nv_bfloat16*)c.x;
+  a.ld_x = c.ld_x;
+  a.k_in = c.k_in;
+  a.R = c.rank;
+  a.add_inputs = c.add_inputs;
+  a.sr_max = c.n_slices * c.rank;
   a.n = n;
   a.n_keys = n_keys;
   a.perm = perm;
   a.seg_start = seg;
   a.row_cap = 0;
   a.err = err_word;
-  plan_tiles(a, H, a.sl.n_cols, a.sr_max, kModeFused);
-  MoeTables tb{w_ptr_a, w_ptr_b, stride_a, stride_b, E, top_k, n_slices, scale};
+  plan_tiles(a, c.k_in, a.sl.n_cols, a.sr_max, kModeFused);
+  MoeTables tb{c.w_ptr_a, c.w_ptr_b, c.stride_a, c.stride_b, c.E, c.x_div, c.n_slices,
+               c.scale, c.pair_weight};
   // With LORA_MOE_SGMV_MIN_ROWS set, keys with at least that many pairs go to
   // the tensor-core path.  Off by default: at the ~26 pairs per key of a
   // top-8-of-64 routing the cluster kernel is faster (0.139 against 0.187 ms
   // on GB300), and the tensor-core kernels cost ~10 us of launches per call
-  // even when no key qualifies.
+  // even when no key qualifies.  Its epilogue folds one scale per key, so
+  // calls with routing weights stay on the cluster kernel.
   static const int moe_thr = env_int("LORA_MOE_SGMV_MIN_ROWS", 0);
-  const bool sgmv = moe_thr >= 1 && a.sr_max <= kSgmvMaxSR;
+  const bool sgmv = moe_thr >= 1 && a.sr_max <= kSgmvMaxSR && !c.pair_weight;
   if (sgmv) a.max_rows = moe_thr;
   rc = launch_delta<kModeFused>(a, tb, n_keys, s);
   if (rc) return rc;
@@ -866,9 +887,132 @@ int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t
     wb.bytes = ws_bytes;
     if ((rc = launch_sgmv(a, tb, wb, n_keys, moe_thr, s))) return rc;
   }
+  if (!c.zero_skipped) return LORA_OK;
   // the pairs with no adapter (the no-key bucket) are written as zeros
-  zero_rows_kernel<<<1024, 256, 0, s>>>(a.out, a.ld_out, 2 * I, perm, seg, n_keys);
+  zero_rows_kernel<<<1024, 256, 0, s>>>(a.out, a.ld_out, n_cols, perm, seg, n_keys);
   return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_moe_fc1_delta(void* out, const void* x, const int64_t* w_ptr_a, int64_t stride_a,
+                       const int64_t* w_ptr_b, int64_t stride_b, int shared_a,
+                       const int32_t* topk_ids, const int32_t* lora_ids, int T, int top_k, int E,
+                       int H, int I, int rank, int num_loras, float scale, void* workspace,
+                       size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (T < 0 || top_k < 0 || E < 1 || H < 0 || I < 0 || num_loras < 1 || stride_a < 0 ||
+      stride_b < 0)
+    return LORA_ERR_ARG;
+  MoeCall c = {};
+  c.out = out;
+  c.ld_out = 2 * (int64_t)I;
+  c.x = x;
+  c.ld_x = H;
+  c.k_in = H;
+  c.x_div = top_k > 0 ? top_k : 1;
+  c.n_slices = shared_a ? 1 : 2;
+  c.widths[0] = shared_a ? 2 * I : I;
+  c.widths[1] = I;
+  c.w_ptr_a = w_ptr_a;
+  c.w_ptr_b = w_ptr_b;
+  c.stride_a = stride_a;
+  c.stride_b = stride_b;
+  c.topk_ids = topk_ids;
+  c.lora_ids = lora_ids;
+  c.T = T;
+  c.top_k = top_k;
+  c.E = E;
+  c.H = H;
+  c.I = I;
+  c.rank = rank;
+  c.num_loras = num_loras;
+  c.scale = scale;
+  c.zero_skipped = 1;
+  return moe_delta(c, workspace, ws_bytes, err_word, (cudaStream_t)stream);
+}
+
+int lora_moe_w13_delta(void* y, const void* x, const int64_t* w_ptr_a, int64_t stride_a,
+                       const int64_t* w_ptr_b, int64_t stride_b, int shared_a,
+                       const int32_t* topk_ids, const int32_t* lora_ids,
+                       const int32_t* expert_map, int n_global_experts,
+                       const int32_t* adapter_enabled, int T, int top_k, int E, int H, int I,
+                       int rank, int num_loras, float scale, int add_inputs, void* workspace,
+                       size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (T < 0 || top_k < 0 || E < 1 || H < 0 || I < 0 || num_loras < 1 || stride_a < 0 ||
+      stride_b < 0)
+    return LORA_ERR_ARG;
+  MoeCall c = {};
+  c.out = y;
+  c.ld_out = 2 * (int64_t)I;
+  c.x = x;
+  c.ld_x = H;
+  c.k_in = H;
+  c.x_div = top_k > 0 ? top_k : 1;
+  c.n_slices = shared_a ? 1 : 2;
+  c.widths[0] = shared_a ? 2 * I : I;
+  c.widths[1] = I;
+  c.w_ptr_a = w_ptr_a;
+  c.w_ptr_b = w_ptr_b;
+  c.stride_a = stride_a;
+  c.stride_b = stride_b;
+  c.topk_ids = topk_ids;
+  c.lora_ids = lora_ids;
+  c.expert_map = expert_map;
+  c.n_global = n_global_experts;
+  c.adapter_enabled = adapter_enabled;
+  c.T = T;
+  c.top_k = top_k;
+  c.E = E;
+  c.H = H;
+  c.I = I;
+  c.rank = rank;
+  c.num_loras = num_loras;
+  c.scale = scale;
+  c.add_inputs = add_inputs ? 1 : 0;
+  return moe_delta(c, workspace, ws_bytes, err_word, (cudaStream_t)stream);
+}
+
+int lora_moe_w2_delta(void* y, const void* x, const int64_t* w_ptr_a, int64_t stride_a,
+                      const int64_t* w_ptr_b, int64_t stride_b, const int32_t* topk_ids,
+                      const int32_t* lora_ids, const int32_t* expert_map, int n_global_experts,
+                      const int32_t* adapter_enabled, const float* topk_weights, int T,
+                      int top_k, int E, int H, int I, int rank, int num_loras, float scale,
+                      int add_inputs, void* workspace, size_t ws_bytes, uint32_t* err_word,
+                      lora_stream_t stream) {
+  if (T < 0 || top_k < 0 || E < 1 || H < 0 || I < 0 || num_loras < 1 || stride_a < 0 ||
+      stride_b < 0)
+    return LORA_ERR_ARG;
+  MoeCall c = {};
+  c.out = y;
+  c.ld_out = H;
+  c.x = x;
+  c.ld_x = I;
+  c.k_in = I;
+  c.x_div = 1;
+  c.n_slices = 1;
+  c.widths[0] = H;
+  c.w_ptr_a = w_ptr_a;
+  c.w_ptr_b = w_ptr_b;
+  c.stride_a = stride_a;
+  c.stride_b = stride_b;
+  c.topk_ids = topk_ids;
+  c.lora_ids = lora_ids;
+  c.expert_map = expert_map;
+  c.n_global = n_global_experts;
+  c.adapter_enabled = adapter_enabled;
+  c.pair_weight = topk_weights;
+  c.T = T;
+  c.top_k = top_k;
+  c.E = E;
+  c.H = H;
+  c.I = I;
+  c.rank = rank;
+  c.num_loras = num_loras;
+  c.scale = scale;
+  c.add_inputs = add_inputs ? 1 : 0;
+  return moe_delta(c, workspace, ws_bytes, err_word, (cudaStream_t)stream);
 }
 
 int lora_get_error(uint32_t* err_word, uint32_t* host_out, int clear, lora_stream_t stream) {

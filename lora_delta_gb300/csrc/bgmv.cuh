@@ -83,15 +83,20 @@ struct LinearTables {
   }
   __device__ int64_t x_row(int item) const { return item; }
   __device__ int64_t out_row(int item) const { return item; }
+  __device__ float row_weight(int) const { return 1.0f; }
 };
 
-// MoE FC1: key = l * E + e; slices = (gate, up) or one fused slice.
+// MoE: key = l * E + e (local expert e); slices = (gate, up) or one fused
+// slice for FC1 / w13, one down slice for w2.  Items are (token, slot)
+// pairs; the input row is the token's (x_div = top_k) or the pair's own
+// (x_div = 1, the down projection).
 struct MoeTables {
   const int64_t* w_ptr_a;
   const int64_t* w_ptr_b;
   int64_t stride_a, stride_b;
-  int E, top_k, n_slices;
+  int E, x_div, n_slices;
   float scale;
+  const float* pair_weight;  // [T * top_k] routing weights folded with scale, or null
   __device__ void resolve(int key, int S, int mode, SlotView& v, uint32_t& bad) const {
     const int l = key / E, e = key - (key / E) * E;
     v.scale = scale;
@@ -111,8 +116,9 @@ struct MoeTables {
       v.ja[j] = v.nact++;
     }
   }
-  __device__ int64_t x_row(int item) const { return item / top_k; }
+  __device__ int64_t x_row(int item) const { return item / x_div; }
   __device__ int64_t out_row(int item) const { return item; }
+  __device__ float row_weight(int item) const { return pair_weight ? pair_weight[item] : 1.0f; }
 };
 
 struct DeltaArgs {
@@ -665,7 +671,8 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       const bool ok0 = row0 < nr, ok1 = row1 < nr;
       const int64_t orow0 = ok0 ? tb.out_row(prow[row0]) : 0;
       const int64_t orow1 = ok1 ? tb.out_row(prow[row1]) : 0;
-      const float sc = v.scale;
+      const float sc0 = ok0 ? v.scale * tb.row_weight(prow[row0]) : 0.f;
+      const float sc1 = ok1 ? v.scale * tb.row_weight(prow[row1]) : 0.f;
       for (int j = 0; j < a.sl.S; ++j) {
         const int ja = v.ja[j];
         if (ja < 0) continue;
@@ -730,10 +737,10 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
                 }
                 if (ok0)
                   *reinterpret_cast<uint32_t*>(o0base + t * 8) =
-                      pack_bf16x2(bf16lo(ov[b][0]) + sc * d[0], bf16hi(ov[b][0]) + sc * d[1]);
+                      pack_bf16x2(bf16lo(ov[b][0]) + sc0 * d[0], bf16hi(ov[b][0]) + sc0 * d[1]);
                 if (ok1)
                   *reinterpret_cast<uint32_t*>(o1base + t * 8) =
-                      pack_bf16x2(bf16lo(ov[b][1]) + sc * d[2], bf16hi(ov[b][1]) + sc * d[3]);
+                      pack_bf16x2(bf16lo(ov[b][1]) + sc1 * d[2], bf16hi(ov[b][1]) + sc1 * d[3]);
               }
             }
           }
@@ -770,10 +777,10 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
               }
               if (ok0)
                 *reinterpret_cast<uint32_t*>(o0base + t * 8) =
-                    pack_bf16x2(bf16lo(ov[b][0]) + sc * d[0], bf16hi(ov[b][0]) + sc * d[1]);
+                    pack_bf16x2(bf16lo(ov[b][0]) + sc0 * d[0], bf16hi(ov[b][0]) + sc0 * d[1]);
               if (ok1)
                 *reinterpret_cast<uint32_t*>(o1base + t * 8) =
-                    pack_bf16x2(bf16lo(ov[b][1]) + sc * d[2], bf16hi(ov[b][1]) + sc * d[3]);
+                    pack_bf16x2(bf16lo(ov[b][1]) + sc1 * d[2], bf16hi(ov[b][1]) + sc1 * d[3]);
             }
           }
         }

@@ -42,15 +42,26 @@ struct SlotKey {
 struct MoeKey {
   const int32_t* topk_ids;
   const int32_t* lora_ids;
-  int top_k, E, num_loras;
+  const int32_t* expert_map;       // [n_global] global -> local expert id (-1: not local), or null
+  const int32_t* adapter_enabled;  // [num_loras], 0: the adapter adds nothing; or null
+  int top_k, E, num_loras, n_global;
   __device__ int operator()(int p, uint32_t& err) const {
     const int l = lora_ids[p / top_k];
-    const int e = topk_ids[p];
+    int e = topk_ids[p];
     const int none = num_loras * E;
     if (l < 0) return none;
     if (l >= num_loras) {
       err |= LORA_DEV_ERR_LORA;
       return none;
+    }
+    if (adapter_enabled && adapter_enabled[l] == 0) return none;
+    if (expert_map) {
+      if (e < 0 || e >= n_global) {
+        err |= LORA_DEV_ERR_EXPERT;
+        return none;
+      }
+      e = expert_map[e];
+      if (e < 0) return none;  // the expert lives on another rank
     }
     if (e < 0 || e >= E) {
       err |= LORA_DEV_ERR_EXPERT;

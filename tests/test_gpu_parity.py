@@ -441,6 +441,131 @@ def test_moe_bad_ids(ld, di, oracle):
     assert not got[0].any() and not got[1].any() and not got[2, 1].any()
 
 
+# ------------------------------------------- in-place MoE w13 / w2 deltas --
+
+def _opt_cuda(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_w13(ld, di, mc, y0, expert_map=None, adapter_enabled=None, add_inputs=True, topk=None,
+            lora=None):
+    dm = di.moe_to_device(mc)
+    if topk is not None:
+        dm.topk_ids = torch.from_numpy(topk).cuda()
+    if lora is not None:
+        dm.lora_ids = torch.from_numpy(lora).cuda()
+    y = di.bf16(y0, "cuda")
+    err = ld.new_error_word()
+    ld.lora_moe_w13_delta(y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b,
+                          mc.shared_a, dm.topk_ids, dm.lora_ids, dm.A_banks[0].shape[0], mc.I,
+                          mc.rank, mc.L, mc.scale, expert_map=_opt_cuda(expert_map),
+                          adapter_enabled=_opt_cuda(adapter_enabled), add_inputs=add_inputs,
+                          err=err)
+    return di.bits(y), ld.lora_get_error(err)
+
+
+def run_w2(ld, di, c, expert_map=None, adapter_enabled=None, weights=None, add_inputs=True):
+    dm = di.moe_to_device(c)
+    y = di.bf16(c.y0, "cuda")
+    err = ld.new_error_word()
+    ld.lora_moe_w2_delta(y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b,
+                         dm.topk_ids, dm.lora_ids, dm.A_banks[0].shape[0], c.H, c.rank, c.L,
+                         c.scale, expert_map=_opt_cuda(expert_map),
+                         adapter_enabled=_opt_cuda(adapter_enabled),
+                         topk_weights=_opt_cuda(weights), add_inputs=add_inputs, err=err)
+    return di.bits(y), ld.lora_get_error(err)
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_moe_w13_in_place_workload(ld, di, oracle, shared):
+    """add_lora_w13 at the FC1 workload's size: 2048 tokens x top-8 of 64 experts."""
+    mc = inputs.moe_case(shared_a=shared)
+    y0 = inputs.moe_y0(mc.seed, (mc.T, mc.top_k, 2 * mc.I))
+    got, err = run_w13(ld, di, mc, y0)
+    ref, ref_err = oracle.moe_w13(y0, mc.x, mc.A_banks, mc.B_banks, mc.topk_ids, mc.lora_ids,
+                                  mc.I, mc.rank, mc.scale, shared, mc.L)
+    assert err == ref_err == 0
+    assert_close(got, ref, "w13 " + mc.name)
+    skipped = mc.lora_ids < 0
+    assert np.array_equal(got[skipped], y0[skipped])
+
+
+@pytest.mark.parametrize("add_inputs", [True, False])
+def test_moe_w13_expert_map_switch_and_bad_ids(ld, di, oracle, add_inputs):
+    """Expert parallel view: 12 global experts, 5 local (shuffled); adapter 1 switched
+    off; an adapter id past the table, a global id past the map, a map entry past E."""
+    mc = inputs.moe_case(seed=41, T=150, top_k=4, E=12, H=136, I=40, rank=8, L=3,
+                         p_none=0.1)
+    local = {2: 3, 5: 0, 7: 4, 8: 1, 11: 2}
+    emap = np.full(12, -1, np.int32)
+    for g, loc in local.items():
+        emap[g] = loc
+    emap[9] = 5  # past the 5 local experts
+    inv = {loc: g for g, loc in local.items()}
+    lc = inputs.MoeCase(**{**mc.__dict__, "E": 5,
+                           "A_banks": [np.ascontiguousarray(b[[inv[i] for i in range(5)]])
+                                       for b in mc.A_banks],
+                           "B_banks": [np.ascontiguousarray(b[[inv[i] for i in range(5)]])
+                                       for b in mc.B_banks]})
+    en = np.array([1, 0, 1], np.int32)
+    topk = mc.topk_ids.copy()
+    lora = mc.lora_ids.copy()
+    lora[3] = 3
+    lora[4] = 0
+    topk[4, 2] = 12
+    y0 = inputs.moe_y0(41, (mc.T, mc.top_k, 2 * mc.I))
+    got, err = run_w13(ld, di, lc, y0, expert_map=emap, adapter_enabled=en,
+                       add_inputs=add_inputs, topk=topk, lora=lora)
+    ref, ref_err = oracle.moe_w13(y0, lc.x, lc.A_banks, lc.B_banks, topk, lora, mc.I, mc.rank,
+                                  mc.scale, False, mc.L, expert_map=emap, adapter_enabled=en,
+                                  add_inputs=add_inputs)
+    assert ref_err == (2 | 4)
+    assert err == ref_err
+    assert_close(got, ref, "w13 expert map")
+    keep = np.all(ref == y0, axis=2)
+    assert np.array_equal(got[keep], y0[keep])
+
+
+@pytest.mark.parametrize("weighted", [False, True])
+def test_moe_w2_in_place_workload(ld, di, oracle, weighted):
+    """add_lora_w2 at the FC1 workload's routing: 2048 tokens x top-8 of 64 experts,
+    per-pair activations [16384, 768] into intermediate_cache3 [2048, 8, 2048]."""
+    c = inputs.moe_w2_case()
+    w = c.topk_weights if weighted else None
+    got, err = run_w2(ld, di, c, weights=w)
+    ref, ref_err = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids,
+                                 c.rank, c.scale, c.L, topk_weights=w)
+    assert err == ref_err == 0
+    assert_close(got, ref, c.name)
+    skipped = c.lora_ids < 0
+    assert np.array_equal(got[skipped], c.y0[skipped])
+
+
+@pytest.mark.parametrize("add_inputs", [True, False])
+def test_moe_w2_ragged_with_map_and_weights(ld, di, oracle, add_inputs):
+    """Small ragged shapes: H 264 (a 64-column tail), I 40, rank 24 (a half MMA
+    k-step), 7 global experts of which 4 local, routing weights, a switched-off adapter."""
+    c = inputs.moe_w2_case(seed=43, T=70, top_k=3, E=7, H=264, I=40, rank=24, L=4, p_none=0.15)
+    local = {0: 1, 3: 0, 4: 3, 6: 2}
+    emap = np.full(7, -1, np.int32)
+    for g, loc in local.items():
+        emap[g] = loc
+    inv = {loc: g for g, loc in local.items()}
+    lc = inputs.MoeDownCase(**{**c.__dict__, "E": 4,
+                               "A_banks": [np.ascontiguousarray(c.A_banks[0][[inv[i] for i in range(4)]])],
+                               "B_banks": [np.ascontiguousarray(c.B_banks[0][[inv[i] for i in range(4)]])]})
+    en = np.array([1, 1, 0, 1], np.int32)
+    got, err = run_w2(ld, di, lc, expert_map=emap, adapter_enabled=en, weights=c.topk_weights,
+                      add_inputs=add_inputs)
+    ref, ref_err = oracle.moe_w2(c.y0, c.x, lc.A_banks, lc.B_banks, c.topk_ids, c.lora_ids,
+                                 c.rank, c.scale, c.L, expert_map=emap, adapter_enabled=en,
+                                 topk_weights=c.topk_weights, add_inputs=add_inputs)
+    assert err == ref_err == 0
+    assert_close(got, ref, "w2 ragged")
+    keep = np.all(ref == c.y0, axis=2)
+    assert keep.any() and np.array_equal(got[keep], c.y0[keep])
+
+
 # ------------------------------------------------- tensor-core (SGMV) path --
 
 def _hot_slots_case(seed, n, k_in, widths, R, ranks, hot=(0, 1), **kw):
