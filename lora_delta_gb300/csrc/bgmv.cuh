@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
           }
         }
       }
-      cluster_arrive();  // partials in place
+      cluster_arrive_release_smem();  // partials in place
       cluster_wait();
       {
         // 4 lanes per 4-entry group; lane qq reads peers qq, qq + 4, qq + 8,

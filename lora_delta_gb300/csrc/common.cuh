@@ -198,6 +198,15 @@ __device__ __forceinline__ uint32_t cluster_index_x() {
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// Arrival that publishes this CTA's earlier shared-memory writes to the
+// cluster: a release fence restricted to shared::cta accesses, then a
+// relaxed arrive.  A full release also orders the CTA's global traffic and
+// cost ~0.5 us more per exchange on GB300.
+__device__ __forceinline__ void cluster_arrive_release_smem() {
+  asm volatile(
+      "fence.release.sync_restrict::shared::cta.cluster;\n\t"
+      "barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 // Arrival without memory ordering: for a CTA that only signals that it has
 // finished reading its peers' shared memory (the values already consumed).
 __device__ __forceinline__ void cluster_arrive_relaxed() {
