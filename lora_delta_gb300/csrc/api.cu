@@ -10,6 +10,7 @@
 
 #include "bgmv.cuh"
 #include "common.cuh"
+#include "keyed.cuh"
 #include "lora_delta.h"
 #include "route.cuh"
 #include "sgmv.cuh"
@@ -33,11 +34,11 @@ int env_int(const char* name, int dflt) {
 
 // Cluster size of the small-segment kernel: 16 CTAs per key when there are few
 // keys (decode: spread each adapter's bytes over many SMs), fewer when there
-// are many keys (MoE); LORA_CLUSTER_SIZE (2..16) overrides, read once.
+// are many keys (MoE); LORA_CLUSTER_SIZE (1..16) overrides, read once.
 int cluster_size_for(int n_keys) {
   static const int forced = [] {
     const int v = env_int("LORA_CLUSTER_SIZE", 0);
-    return (v >= 2 && v <= 16) ? v : 0;
+    return (v >= 1 && v <= 16) ? v : 0;
   }();
   if (forced) return forced;
   // measured on GB300 (152 SMs): 16 slots run best at 12 CTAs per cluster
@@ -249,6 +250,34 @@ int launch_delta(const DeltaArgs& a, const Tables& tb, int n_keys, cudaStream_t 
   if (a.R <= 32) return launch_delta_r<32, MODE>(a, tb, n_keys, smem, s);
   if (a.R <= 64) return launch_delta_r<64, MODE>(a, tb, n_keys, smem, s);
   return launch_delta_r<128, MODE>(a, tb, n_keys, smem, s);
+}
+
+// One CTA per key (the routed-MoE deltas): S * R up to kKeyMaxSR, R <= 32.
+template <class Tables>
+int launch_key(const DeltaArgs& a, const Tables& tb, int n_keys, cudaStream_t stream) {
+  const int sr16 = (a.sr_max + 15) / 16 * 16;
+  if (sr16 > kKeyMaxSR || a.R > 32) return LORA_ERR_UNSUPPORTED;
+  const int smem = key_smem(sr16).total;
+  auto kernel = a.R <= 16 ? delta_key_kernel<16, Tables> : delta_key_kernel<32, Tables>;
+  if (prepare_kernel(kernel, smem, false) != cudaSuccess) return LORA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_keys, 1, 1);
+  cfg.blockDim = dim3(kKeyThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, a, tb));
+}
+
+// The one-CTA-per-key kernel for the routed-MoE deltas (LORA_MOE_KEYED=0
+// falls back to the cluster kernel).
+bool moe_keyed() {
+  static const bool on = env_int("LORA_MOE_KEYED", 1) != 0;
+  return on;
 }
 
 template <class KeyFn>
@@ -880,7 +909,14 @@ int moe_delta(const MoeCall& c, void* workspace, size_t ws_bytes, uint32_t* err_
   static const int moe_thr = env_int("LORA_MOE_SGMV_MIN_ROWS", 0);
   const bool sgmv = moe_thr >= 1 && a.sr_max <= kSgmvMaxSR && !c.pair_weight;
   if (sgmv) a.max_rows = moe_thr;
-  rc = launch_delta<kModeFused>(a, tb, n_keys, s);
+  // One CTA per key streams the key's whole A but also expands all of its
+  // columns alone, so it is taken where the contraction is at least as long
+  // as the output row (FC1, w13: 0.122 against 0.135 ms on GB300); the down
+  // projection (k_in = I < H) stays on the cluster kernel (0.116 against
+  // 0.125 ms).
+  const bool keyed = moe_keyed() && (a.sr_max + 15) / 16 * 16 <= kKeyMaxSR && c.rank <= 32 &&
+                     c.k_in >= n_cols;
+  rc = keyed ? launch_key(a, tb, n_keys, s) : launch_delta<kModeFused>(a, tb, n_keys, s);
   if (rc) return rc;
   if (sgmv) {
     Workspace wb = w;

@@ -1,0 +1,332 @@
+// The routed delta for many keys with a few dozen rows each (the routed-MoE
+// deltas: "flashinfer.fused_moe.bgmv_moe_gemm1_lora_delta" and the in-place
+// w13 / w2 deltas of "punica_base.py"): one CTA per key, which streams the
+// key's whole A through a deep cp.async ring and expands straight from
+// registers.  There are hundreds of keys, so the grid fills the GPU without
+// splitting a key over a cluster, and no partial sums cross CTAs.
+//
+// Per key (rows from the routing sort, in passes of 32):
+//   * shrink: k_in in chunks of 64 columns; stage s of a kKeyStages ring holds
+//     the chunk of the key's active (slice, rank) A rows and of the pass's x
+//     rows.  Every thread copies one fixed 16-byte column of one A row and of
+//     one x row per stage (its source pointers are set once per key), so the
+//     copy issue costs a few instructions per stage, and kKeyStages - 1
+//     stages stay in flight.  The A rows of the first stages are requested
+//     before the grid dependency wait: adapter weights are never written by
+//     the preceding kernel.  Warps own (16 pairs x 16 rows) tiles of the
+//     product and split the k-steps of a chunk when there are fewer tiles
+//     than warps; mma.sync m16n8k16, fp32 accumulate.
+//   * the k-group partials meet in shared memory as the fp32 h [rows][pairs];
+//   * expand + fold: every warp takes 8-column tiles of the key's slices; h
+//     as a bf16 (hi, lo) pair on the A side (rows), B fragments and the out
+//     values loaded from L2 (prefetched at the start of the pass) in batches
+//     of four tiles (one at rank 32), then RN_bf16(out + scale * w_row * d) stored in place
+//     (or RN_bf16(scale * w_row * d) without add_inputs).
+#pragma once
+
+#include "bgmv.cuh"
+#include "common.cuh"
+
+namespace lora {
+
+constexpr int kKeyThreads = 256;
+constexpr int kKeyWarps = kKeyThreads / 32;
+constexpr int kKeyRows = 32;              // rows per pass
+constexpr int kKeyKC = 64;                // k columns per stage
+constexpr int kKeyStages = 6;             // ring depth
+constexpr int kKeyStride = kKeyKC + 8;    // padded row (elements): ldmatrix conflict-free
+constexpr int kKeyMaxSR = 64;             // largest S * R (rounded to 16) this kernel takes
+
+// Shared-memory plan (bytes), identical on host and device.
+struct KeySmem {
+  int stage_bytes, ring_off, p_off, h_off, total;
+};
+__host__ __device__ inline KeySmem key_smem(int sr16) {
+  KeySmem p;
+  p.stage_bytes = (sr16 + kKeyRows) * kKeyStride * 2;
+  p.ring_off = 0;
+  int o = kKeyStages * p.stage_bytes;
+  o = (o + 127) / 128 * 128;
+  p.p_off = o;  // k-group partials [G - 1][rows][sr16] (group 0 writes h directly)
+  const int mt = sr16 / 16;
+  const int units = mt * 2;
+  const int G = units >= kKeyWarps ? 1 : kKeyWarps / units;
+  o += (G - 1) * kKeyRows * sr16 * 4;
+  p.h_off = o;
+  o += kKeyRows * sr16 * 4 + 128;  // (+ slack: no guarded read of h can leave the plan)
+  p.total = o;
+  return p;
+}
+
+template <int RMAX, class Tables>
+__global__ void __launch_bounds__(kKeyThreads, 3)
+    delta_key_kernel(const DeltaArgs a, const Tables tb) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ SlotView v;
+  __shared__ int prow[kKeyRows];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int key = blockIdx.x;
+
+  if (tid == 0) {
+    uint32_t bad = 0;
+    tb.resolve(key, a.sl.S, kModeFused, v, bad);
+    if (bad) set_error(a.err, bad);
+  }
+  __syncthreads();
+  const int R = a.R;
+  const int SRa = v.nact * R;
+  const int SR16 = (a.sr_max + 15) / 16 * 16;
+  const KeySmem plan = key_smem(SR16);
+  uint8_t* ring = smem + plan.ring_off;
+  float* P = reinterpret_cast<float*>(smem + plan.p_off);
+  float* H = reinterpret_cast<float*>(smem + plan.h_off);
+  const int nchunks = (a.k_in + kKeyKC - 1) / kKeyKC;
+
+  // this thread's copy slots: 16-byte column `cq` of A rows ar0 (and ar0 + 32)
+  // and of x row `ar0` of every stage
+  const int cq = tid & 7, ar0 = tid >> 3;
+  const __nv_bfloat16* asrc[2] = {nullptr, nullptr};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = ar0 + 32 * h;
+    if (t < SRa) {
+      const int jj = t / R, q = t - jj * R;
+      asrc[h] = v.A[v.act_slice[jj]] + (size_t)q * a.k_in + cq * 8;
+    }
+  }
+  auto stage_a = [&](int s) {
+    return reinterpret_cast<__nv_bfloat16*>(ring + (size_t)s * plan.stage_bytes);
+  };
+  auto stage_x = [&](int s) { return stage_a(s) + (size_t)SR16 * kKeyStride; };
+  // copies of chunk c's A rows (the x rows follow separately)
+  auto copy_a = [&](int c, int s) {
+    const int k0 = c * kKeyKC, kw = min(kKeyKC, a.k_in - k0);
+    __nv_bfloat16* dst = stage_a(s) + cq * 8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (asrc[h] && cq * 8 < kw)
+        cp_async16(dst + (size_t)(ar0 + 32 * h) * kKeyStride, asrc[h] + k0);
+  };
+
+  const bool early = a.early && v.nact > 0;
+  if (early) {  // A rows of the first stages, before the dependency wait
+    for (int c = 0; c < kKeyStages - 1 && c < nchunks; ++c) copy_a(c, c);
+    cp_async_commit();
+  }
+  cudaTriggerProgrammaticLaunchCompletion();
+  cudaGridDependencySynchronize();
+  const int s0 = a.seg_start[key];
+  const int nrows = v.nact > 0 ? a.seg_start[key + 1] - s0 : 0;
+  if (nrows <= 0 || nrows < a.min_rows || nrows >= a.max_rows) {
+    if (early) cp_async_wait<0>();  // no copy may land in a CTA that has exited
+    return;
+  }
+  const int* rows = a.perm + s0;
+
+  // shrink work split: units of (16 pairs x 16 rows), k-groups over the warps
+  const int mt = SR16 / 16, units = mt * 2;
+  const int G = units >= kKeyWarps ? 1 : kKeyWarps / units;
+  const int my_u = warp % units, my_g = warp / units;
+  const bool mma_warp = warp < G * units;
+  const int my_m = my_u >> 1, my_rg = my_u & 1;
+  constexpr int KS = RMAX / 16;
+  constexpr int NB = KS == 1 ? 4 : 1;  // expand tiles per load batch (registers)
+  bool first_pass = true;
+
+  for (int p0 = 0; p0 < nrows; p0 += kKeyRows) {
+    const int nr = min(kKeyRows, nrows - p0);
+    if (!first_pass) __syncthreads();  // the previous pass is done with prow, H and the ring
+    if (tid < nr) prow[tid] = rows[p0 + tid];
+    __syncthreads();
+    // L2 prefetch of the pass's expand operands (B of the key; out rows)
+    if (warp == kKeyWarps - 1) {
+      if (first_pass)
+        for (int j = lane; j < a.sl.S; j += 32)
+          if (v.ja[j] >= 0)
+            bulk_prefetch_l2(v.B[j], (uint32_t)(a.sl.width[j] * R * 2));
+      if (a.add_inputs)
+        for (int r = lane; r < nr; r += 32)
+          for (int j = 0; j < a.sl.S; ++j)
+            if (v.ja[j] >= 0 && a.sl.width[j] > 0)
+              bulk_prefetch_l2(a.out + tb.out_row(prow[r]) * a.ld_out + a.sl.off[j],
+                               (uint32_t)(a.sl.width[j] * 2));
+    }
+    const __nv_bfloat16* xsrc =
+        ar0 < nr ? a.x + tb.x_row(prow[ar0]) * a.ld_x + cq * 8 : nullptr;
+    auto copy_x = [&](int c, int s) {
+      const int k0 = c * kKeyKC, kw = min(kKeyKC, a.k_in - k0);
+      if (xsrc && cq * 8 < kw) cp_async16(stage_x(s) + (size_t)ar0 * kKeyStride + cq * 8, xsrc + k0);
+    };
+    // k tail: zero the columns [kw, round16(kw)) of the last chunk's rows
+    auto zero_tail = [&](int c, int s) {
+      const int k0 = c * kKeyKC, kw = min(kKeyKC, a.k_in - k0);
+      if ((kw & 15) == 0) return;
+      for (int i = tid; i < SR16 + kKeyRows; i += kKeyThreads)
+        *reinterpret_cast<uint4*>(stage_a(s) + (size_t)i * kKeyStride + kw) = make_uint4(0, 0, 0, 0);
+    };
+
+    // ---- ring prologue: stages 0 .. kKeyStages - 2 ----------------------
+    const bool a_done = early && first_pass;
+    for (int c = 0; c < kKeyStages - 1; ++c) {
+      if (c < nchunks) {
+        if (!a_done) copy_a(c, c);
+        copy_x(c, c);
+        if (c == nchunks - 1) zero_tail(c, c);
+      }
+      cp_async_commit();  // (empty groups keep the count uniform)
+    }
+    first_pass = false;
+
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    const bool rg_live = my_rg * 16 < nr;  // (warp-uniform)
+    for (int c = 0; c < nchunks; ++c) {
+      cp_async_wait<kKeyStages - 2>();  // chunk c landed
+      __syncthreads();                  // ... for every thread; slot (c - 1) is free
+      {
+        const int cn = c + kKeyStages - 1, sn = cn % kKeyStages;
+        if (cn < nchunks) {
+          copy_a(cn, sn);
+          copy_x(cn, sn);
+          if (cn == nchunks - 1) zero_tail(cn, sn);
+        }
+        cp_async_commit();
+      }
+      const int s = c % kKeyStages;
+      const int kw = min(kKeyKC, a.k_in - c * kKeyKC);
+      const int ksteps = (kw + 15) / 16;
+      if (mma_warp && rg_live) {
+        const __nv_bfloat16* Ab = stage_a(s);
+        const __nv_bfloat16* Xb = stage_x(s);
+        const uint32_t aaddr = smem_addr(Ab + (size_t)(my_m * 16 + (((lane >> 3) & 1) << 3) +
+                                                       (lane & 7)) * kKeyStride +
+                                         ((lane >> 4) << 3));
+        const uint32_t xaddr = smem_addr(Xb + (size_t)(my_rg * 16 + ((lane >> 4) << 3) +
+                                                       (lane & 7)) * kKeyStride +
+                                         ((lane >> 3) & 1) * 8);
+        for (int ks = my_g; ks < ksteps; ks += G) {
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
+          ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+          mma_16816(&acc[0], a0, a1, a2, a3, b0, b1);
+          mma_16816(&acc[4], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+    cp_async_wait<0>();  // (only empty groups remain)
+
+    // ---- k-group partials -> h [rows][pairs] -----------------------------
+    if (mma_warp && rg_live) {
+      float* dst = my_g == 0 ? H : P + (size_t)(my_g - 1) * kKeyRows * SR16;
+      const int pr = my_m * 16 + gq;       // pair of acc[0], acc[1]
+      const int xr = my_rg * 16 + 2 * tq;  // x row of acc[0]
+      dst[(xr) * SR16 + pr] = acc[0];
+      dst[(xr + 1) * SR16 + pr] = acc[1];
+      dst[(xr) * SR16 + pr + 8] = acc[2];
+      dst[(xr + 1) * SR16 + pr + 8] = acc[3];
+      dst[(xr + 8) * SR16 + pr] = acc[4];
+      dst[(xr + 9) * SR16 + pr] = acc[5];
+      dst[(xr + 8) * SR16 + pr + 8] = acc[6];
+      dst[(xr + 9) * SR16 + pr + 8] = acc[7];
+    }
+    __syncthreads();
+    if (G > 1) {
+      for (int i = tid; i < nr * SR16; i += kKeyThreads) {
+        float s = H[i];
+        for (int g = 1; g < G; ++g) s += P[(size_t)(g - 1) * kKeyRows * SR16 + i];
+        H[i] = s;
+      }
+      __syncthreads();
+    }
+
+    // ---- expand + fold ------------------------------------------------------
+    const int nm = nr > 16 ? 2 : 1;  // 16-row m-tiles of the pass
+    int64_t orow[2][2];
+    float sc[2][2];
+    bool ok[2][2];
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = mi * 16 + gq + 8 * h;
+        ok[mi][h] = r < nr;
+        orow[mi][h] = ok[mi][h] ? tb.out_row(prow[r]) : 0;
+        sc[mi][h] = ok[mi][h] ? v.scale * tb.row_weight(prow[r]) : 0.f;
+      }
+    for (int j = 0; j < a.sl.S; ++j) {
+      const int ja = v.ja[j];
+      if (ja < 0) continue;
+      const int ntl = a.sl.width[j] / 8;
+      if (warp >= ntl) continue;
+      uint32_t ahi[2][KS][4], alo[2][KS][4];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const float* hb = H + ja * R + 2 * tq + (mi * 16 + gq) * SR16;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const bool lo_ok = mi < nm && kk * 16 < R, hi_ok = mi < nm && kk * 16 + 8 < R;
+          const float* h0 = hb + kk * 16;
+          const float* h1 = h0 + 8 * SR16;
+          split_bf16x2(lo_ok ? h0[0] : 0.f, lo_ok ? h0[1] : 0.f, ahi[mi][kk][0], alo[mi][kk][0]);
+          split_bf16x2(lo_ok ? h1[0] : 0.f, lo_ok ? h1[1] : 0.f, ahi[mi][kk][1], alo[mi][kk][1]);
+          split_bf16x2(hi_ok ? h0[8] : 0.f, hi_ok ? h0[9] : 0.f, ahi[mi][kk][2], alo[mi][kk][2]);
+          split_bf16x2(hi_ok ? h1[8] : 0.f, hi_ok ? h1[9] : 0.f, ahi[mi][kk][3], alo[mi][kk][3]);
+        }
+      }
+      const __nv_bfloat16* bbase = v.B[j] + (size_t)gq * R + 2 * tq;
+      const int64_t cbase = a.sl.off[j] + 2 * tq;
+      for (int t0 = warp; t0 < ntl; t0 += kKeyWarps * NB) {
+        uint32_t bf[NB][KS][2], ov[NB][2][2];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {  // every load of the batch first
+          const int t = t0 + b * kKeyWarps;
+          if (t < ntl) {
+            const __nv_bfloat16* brow = bbase + (size_t)t * 8 * R;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              bf[b][kk][0] = (kk * 16 < R) ? ldg_nc_u32(brow + kk * 16) : 0u;
+              bf[b][kk][1] = (kk * 16 + 8 < R) ? ldg_nc_u32(brow + kk * 16 + 8) : 0u;
+            }
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                ov[b][mi][h] = (a.add_inputs && ok[mi][h])
+                                   ? *reinterpret_cast<const uint32_t*>(
+                                         a.out + orow[mi][h] * a.ld_out + cbase + t * 8)
+                                   : 0u;
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const int t = t0 + b * kKeyWarps;
+          if (t >= ntl) continue;
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) {
+            if (mi >= nm) continue;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              if (kk * 16 < R) {
+                mma_16816(d, ahi[mi][kk][0], ahi[mi][kk][1], ahi[mi][kk][2], ahi[mi][kk][3],
+                          bf[b][kk][0], bf[b][kk][1]);
+                mma_16816(d, alo[mi][kk][0], alo[mi][kk][1], alo[mi][kk][2], alo[mi][kk][3],
+                          bf[b][kk][0], bf[b][kk][1]);
+              }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (ok[mi][h])
+                *reinterpret_cast<uint32_t*>(a.out + orow[mi][h] * a.ld_out + cbase + t * 8) =
+                    pack_bf16x2(bf16lo(ov[b][mi][h]) + sc[mi][h] * d[2 * h],
+                                bf16hi(ov[b][mi][h]) + sc[mi][h] * d[2 * h + 1]);
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace lora

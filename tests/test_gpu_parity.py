@@ -566,6 +566,39 @@ def test_moe_w2_ragged_with_map_and_weights(ld, di, oracle, add_inputs):
     assert keep.any() and np.array_equal(got[keep], c.y0[keep])
 
 
+@pytest.mark.parametrize("shared", [False, True])
+def test_moe_many_rows_per_key_rank_32(ld, di, oracle, shared):
+    """Few keys with ~50 pairs each (two 32-row passes of the per-key kernel),
+    rank 32 (two MMA k-steps), H 520 (a k tail of 8 after eight 64-column chunks)."""
+    mc = inputs.moe_case(shared_a=shared, seed=47, T=150, top_k=2, E=3, H=520, I=48, rank=32,
+                         L=2, p_none=0.05)
+    got, err = run_moe(ld, di, mc)
+    ref, ref_err = oracle.moe_fc1(mc.x, mc.A_banks, mc.B_banks, mc.topk_ids, mc.lora_ids, mc.I,
+                                  mc.rank, mc.scale, shared, mc.L)
+    assert err == ref_err == 0
+    assert_close(got, ref, "moe many rows rank 32")
+    y0 = inputs.moe_y0(47, (mc.T, mc.top_k, 2 * mc.I))
+    got, err = run_w13(ld, di, mc, y0)
+    ref, _ = oracle.moe_w13(y0, mc.x, mc.A_banks, mc.B_banks, mc.topk_ids, mc.lora_ids, mc.I,
+                            mc.rank, mc.scale, shared, mc.L)
+    assert err == 0
+    assert_close(got, ref, "w13 many rows rank 32")
+
+
+def test_moe_w2_contraction_longer_than_output(ld, di, oracle):
+    """A down projection with I > H takes the per-key kernel: per-pair input rows and
+    routing weights there, ~40 pairs per key."""
+    c = inputs.moe_w2_case(seed=49, T=120, top_k=2, E=3, H=64, I=136, rank=16, L=2,
+                           p_none=0.1)
+    got, err = run_w2(ld, di, c, weights=c.topk_weights)
+    ref, ref_err = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids,
+                                 c.rank, c.scale, c.L, topk_weights=c.topk_weights)
+    assert err == ref_err == 0
+    assert_close(got, ref, "w2 I > H")
+    keep = np.all(ref == c.y0, axis=2)
+    assert np.array_equal(got[keep], c.y0[keep])
+
+
 # ------------------------------------------------- tensor-core (SGMV) path --
 
 def _hot_slots_case(seed, n, k_in, widths, R, ranks, hot=(0, 1), **kw):
