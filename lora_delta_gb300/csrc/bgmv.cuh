@@ -352,9 +352,13 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
 
   // ---- the key's rows, in ascending row order (warp 0) -----------------
   // Warp 0 also starts the first pass's x / out copies when they are few
-  // (decode-sized: at most 8 per lane); larger ones are left to every warp.
-  const bool warp0_copies =
-      early && kRowsPerPass * (min(a.kst, k_hi - k_lo) / 8 + (o_staged ? a.cpc / 8 : 0)) <= 256;
+  // (decode-sized: at most 16 per lane); larger ones are left to every warp.
+  // The choice depends only on the key's row count, which warp 0 knows first
+  // and every thread reads after the barrier below.
+  const int w0_chunks = min(a.kst, k_hi - k_lo) / 8 + (o_staged ? a.cpc / 8 : 0);
+  auto warp0_copies_for = [&](int total) {
+    return early && min(kRowsPerPass, total) * w0_chunks <= 512;
+  };
   if (warp == 0) {
     int total = 0, s0 = 0;
     if (a.perm) {
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       rows_base_s = s0;
     }
     __syncwarp();
-    if (warp0_copies && total > 0 && total >= a.min_rows && total < a.max_rows) {
+    if (warp0_copies_for(total) && total > 0 && total >= a.min_rows && total < a.max_rows) {
       const int* rows0 = a.perm ? a.perm + s0 : rows_s;
       const int nr0 = min(kRowsPerPass, total);
       copy_x_rows(a, tb, rows0, nr0, k_lo, min(a.kst, k_hi - k_lo), Xs, stride, lane, 1);
@@ -397,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
   __syncthreads();
   if (v.nact == 0) return;
   const int nrows = nrows_s;
+  const bool warp0_copies = warp0_copies_for(nrows);
   const int* rows = a.perm ? a.perm + rows_base_s : rows_s;
   if (nrows == 0 || nrows < a.min_rows || nrows >= a.max_rows) {  // uniform
     if (early) cp_async_wait<0>();  // no copy may land in a CTA that has exited
