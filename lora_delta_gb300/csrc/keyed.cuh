@@ -33,9 +33,14 @@ constexpr int kKeyThreads = 256;
 constexpr int kKeyWarps = kKeyThreads / 32;
 constexpr int kKeyRows = 32;              // rows per pass
 constexpr int kKeyKC = 64;                // k columns per stage
-constexpr int kKeyStages = 6;             // ring depth
+constexpr int kKeyStages = 5;             // ring depth
 constexpr int kKeyStride = kKeyKC + 8;    // padded row (elements): ldmatrix conflict-free
 constexpr int kKeyMaxSR = 64;             // largest S * R (rounded to 16) this kernel takes
+
+// 16-byte asynchronous global -> shared copy to a shared-window address.
+__device__ __forceinline__ void cp_async16_s(uint32_t saddr, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gsrc) : "memory");
+}
 
 // Shared-memory plan (bytes), identical on host and device.
 struct KeySmem {
@@ -59,7 +64,7 @@ __host__ __device__ inline KeySmem key_smem(int sr16) {
 }
 
 template <int RMAX, class Tables>
-__global__ void __launch_bounds__(kKeyThreads, 3)
+__global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
     delta_key_kernel(const DeltaArgs a, const Tables tb) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ SlotView v;
@@ -95,23 +100,33 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
       asrc[h] = v.A[v.act_slice[jj]] + (size_t)q * a.k_in + cq * 8;
     }
   }
-  auto stage_a = [&](int s) {
-    return reinterpret_cast<__nv_bfloat16*>(ring + (size_t)s * plan.stage_bytes);
-  };
-  auto stage_x = [&](int s) { return stage_a(s) + (size_t)SR16 * kKeyStride; };
-  // copies of chunk c's A rows (the x rows follow separately)
-  auto copy_a = [&](int c, int s) {
-    const int k0 = c * kKeyKC, kw = min(kKeyKC, a.k_in - k0);
-    __nv_bfloat16* dst = stage_a(s) + cq * 8;
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      if (asrc[h] && cq * 8 < kw)
-        cp_async16(dst + (size_t)(ar0 + 32 * h) * kKeyStride, asrc[h] + k0);
+  // Stage layout: A rows [SR16][kKeyStride], then x rows [kKeyRows][kKeyStride].
+  // Addresses are 32-bit shared-window offsets, advanced per stage without
+  // divisions: the copy issue and the fragment loads cost a few integer
+  // instructions per chunk.
+  const uint32_t ring_s = smem_addr(ring);
+  const uint32_t sbytes = (uint32_t)plan.stage_bytes;
+  const uint32_t ring_end = ring_s + kKeyStages * sbytes;
+  const uint32_t a_off = (uint32_t)(ar0 * kKeyStride + cq * 8) * 2u;
+  const uint32_t a_off2 = a_off + 32u * kKeyStride * 2u;
+  const uint32_t x_off = (uint32_t)((SR16 + ar0) * kKeyStride + cq * 8) * 2u;
+  const int full = a.k_in / kKeyKC;  // chunks with all 64 columns
+  const int tail_kw = a.k_in - full * kKeyKC;
+  const bool tail_col = cq * 8 < tail_kw;  // this thread's column exists in the last chunk
+  auto next_slot = [&](uint32_t sb) { sb += sbytes; return sb == ring_end ? ring_s : sb; };
+  // copies of chunk c's A rows into the slot at sb (the x rows follow separately)
+  auto copy_a = [&](int c, uint32_t sb) {
+    if (c < full || tail_col) {
+      const size_t k0 = (size_t)c * kKeyKC;
+      if (asrc[0]) cp_async16_s(sb + a_off, asrc[0] + k0);
+      if (asrc[1]) cp_async16_s(sb + a_off2, asrc[1] + k0);
+    }
   };
 
   const bool early = a.early && v.nact > 0;
   if (early) {  // A rows of the first stages, before the dependency wait
-    for (int c = 0; c < kKeyStages - 1 && c < nchunks; ++c) copy_a(c, c);
+    uint32_t sb = ring_s;
+    for (int c = 0; c < kKeyStages - 1 && c < nchunks; ++c, sb += sbytes) copy_a(c, sb);
     cp_async_commit();
   }
   cudaTriggerProgrammaticLaunchCompletion();
@@ -130,8 +145,15 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
   const int my_u = warp % units, my_g = warp / units;
   const bool mma_warp = warp < G * units;
   const int my_m = my_u >> 1, my_rg = my_u & 1;
+  // ldmatrix row addresses of this lane inside a stage (bytes)
+  const uint32_t a_frag =
+      (uint32_t)((my_m * 16 + (((lane >> 3) & 1) << 3) + (lane & 7)) * kKeyStride +
+                 ((lane >> 4) << 3)) * 2u;
+  const uint32_t x_frag =
+      (uint32_t)((SR16 + my_rg * 16 + ((lane >> 4) << 3) + (lane & 7)) * kKeyStride +
+                 ((lane >> 3) & 1) * 8) * 2u;
   constexpr int KS = RMAX / 16;
-  constexpr int NB = KS == 1 ? 4 : 1;  // expand tiles per load batch (registers)
+  constexpr int NB = KS == 1 ? 2 : 1;  // expand tiles per load batch (registers)
   bool first_pass = true;
 
   for (int p0 = 0; p0 < nrows; p0 += kKeyRows) {
@@ -154,27 +176,25 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
     }
     const __nv_bfloat16* xsrc =
         ar0 < nr ? a.x + tb.x_row(prow[ar0]) * a.ld_x + cq * 8 : nullptr;
-    auto copy_x = [&](int c, int s) {
-      const int k0 = c * kKeyKC, kw = min(kKeyKC, a.k_in - k0);
-      if (xsrc && cq * 8 < kw) cp_async16(stage_x(s) + (size_t)ar0 * kKeyStride + cq * 8, xsrc + k0);
-    };
-    // k tail: zero the columns [kw, round16(kw)) of the last chunk's rows
-    auto zero_tail = [&](int c, int s) {
-      const int k0 = c * kKeyKC, kw = min(kKeyKC, a.k_in - k0);
-      if ((kw & 15) == 0) return;
-      for (int i = tid; i < SR16 + kKeyRows; i += kKeyThreads)
-        *reinterpret_cast<uint4*>(stage_a(s) + (size_t)i * kKeyStride + kw) = make_uint4(0, 0, 0, 0);
+    // chunk c's A (unless already requested) and x rows into the slot at sb;
+    // the partial last chunk also zeroes its columns [kw, round16(kw))
+    auto issue = [&](int c, uint32_t sb, bool with_a) {
+      if (with_a) copy_a(c, sb);
+      if (xsrc && (c < full || tail_col)) cp_async16_s(sb + x_off, xsrc + (size_t)c * kKeyKC);
+      if (c == full && (tail_kw & 15)) {
+        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(ring + (sb - ring_s));
+        for (int i = tid; i < SR16 + kKeyRows; i += kKeyThreads)
+          *reinterpret_cast<uint4*>(st + (size_t)i * kKeyStride + tail_kw) = make_uint4(0, 0, 0, 0);
+      }
     };
 
-    // ---- ring prologue: stages 0 .. kKeyStages - 2 ----------------------
+    // ---- ring prologue: chunks 0 .. kKeyStages - 2 ----------------------
     const bool a_done = early && first_pass;
+    uint32_t sb_issue = ring_s;
     for (int c = 0; c < kKeyStages - 1; ++c) {
-      if (c < nchunks) {
-        if (!a_done) copy_a(c, c);
-        copy_x(c, c);
-        if (c == nchunks - 1) zero_tail(c, c);
-      }
+      if (c < nchunks) issue(c, sb_issue, !a_done);
       cp_async_commit();  // (empty groups keep the count uniform)
+      sb_issue = next_slot(sb_issue);
     }
     first_pass = false;
 
@@ -182,30 +202,16 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     const bool rg_live = my_rg * 16 < nr;  // (warp-uniform)
+    uint32_t sb = ring_s;
     for (int c = 0; c < nchunks; ++c) {
       cp_async_wait<kKeyStages - 2>();  // chunk c landed
-      __syncthreads();                  // ... for every thread; slot (c - 1) is free
-      {
-        const int cn = c + kKeyStages - 1, sn = cn % kKeyStages;
-        if (cn < nchunks) {
-          copy_a(cn, sn);
-          copy_x(cn, sn);
-          if (cn == nchunks - 1) zero_tail(cn, sn);
-        }
-        cp_async_commit();
-      }
-      const int s = c % kKeyStages;
-      const int kw = min(kKeyKC, a.k_in - c * kKeyKC);
-      const int ksteps = (kw + 15) / 16;
+      __syncthreads();                  // ... for every thread; the slot of c - 1 is free
+      if (c + kKeyStages - 1 < nchunks) issue(c + kKeyStages - 1, sb_issue, true);
+      cp_async_commit();
+      sb_issue = next_slot(sb_issue);
       if (mma_warp && rg_live) {
-        const __nv_bfloat16* Ab = stage_a(s);
-        const __nv_bfloat16* Xb = stage_x(s);
-        const uint32_t aaddr = smem_addr(Ab + (size_t)(my_m * 16 + (((lane >> 3) & 1) << 3) +
-                                                       (lane & 7)) * kKeyStride +
-                                         ((lane >> 4) << 3));
-        const uint32_t xaddr = smem_addr(Xb + (size_t)(my_rg * 16 + ((lane >> 4) << 3) +
-                                                       (lane & 7)) * kKeyStride +
-                                         ((lane >> 3) & 1) * 8);
+        const uint32_t aaddr = sb + a_frag, xaddr = sb + x_frag;
+        const int ksteps = c < full ? kKeyKC / 16 : (tail_kw + 15) / 16;
         for (int ks = my_g; ks < ksteps; ks += G) {
           uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
           ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
@@ -214,6 +220,7 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
           mma_16816(&acc[4], a0, a1, a2, a3, b2, b3);
         }
       }
+      sb = next_slot(sb);
     }
     cp_async_wait<0>();  // (only empty groups remain)
 
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
 
     // ---- expand + fold ------------------------------------------------------
     const int nm = nr > 16 ? 2 : 1;  // 16-row m-tiles of the pass
-    int64_t orow[2][2];
+    int orow[2][2];  // (row < n <= 2^30)
     float sc[2][2];
     bool ok[2][2];
 #pragma unroll
@@ -252,7 +259,7 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
       for (int h = 0; h < 2; ++h) {
         const int r = mi * 16 + gq + 8 * h;
         ok[mi][h] = r < nr;
-        orow[mi][h] = ok[mi][h] ? tb.out_row(prow[r]) : 0;
+        orow[mi][h] = ok[mi][h] ? (int)tb.out_row(prow[r]) : 0;
         sc[mi][h] = ok[mi][h] ? v.scale * tb.row_weight(prow[r]) : 0.f;
       }
     for (int j = 0; j < a.sl.S; ++j) {
@@ -295,7 +302,7 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
               for (int h = 0; h < 2; ++h)
                 ov[b][mi][h] = (a.add_inputs && ok[mi][h])
                                    ? *reinterpret_cast<const uint32_t*>(
-                                         a.out + orow[mi][h] * a.ld_out + cbase + t * 8)
+                                         a.out + (int64_t)orow[mi][h] * a.ld_out + cbase + t * 8)
                                    : 0u;
           }
         }
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(kKeyThreads, 3)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               if (ok[mi][h])
-                *reinterpret_cast<uint32_t*>(a.out + orow[mi][h] * a.ld_out + cbase + t * 8) =
+                *reinterpret_cast<uint32_t*>(a.out + (int64_t)orow[mi][h] * a.ld_out + cbase + t * 8) =
                     pack_bf16x2(bf16lo(ov[b][mi][h]) + sc[mi][h] * d[2 * h],
                                 bf16hi(ov[b][mi][h]) + sc[mi][h] * d[2 * h + 1]);
           }
