@@ -556,7 +556,7 @@ def _moe(ld, di, inputs, device, hbm_peak, timed, res):
         res["moe_fc1_" + ("shared" if shared else "regular")] = {
             "pairs_per_s": round(mc.T * mc.top_k / (ms / 1e3), 1), "ms": round(ms, 4),
             "routed_pairs": pairs, "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
-            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 4}
+            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 3}
         del dm, out, ws
         torch.cuda.empty_cache()
 

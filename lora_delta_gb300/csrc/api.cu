@@ -253,15 +253,17 @@ int launch_delta(const DeltaArgs& a, const Tables& tb, int n_keys, cudaStream_t 
 }
 
 // One CTA per key (the routed-MoE deltas): S * R up to kKeyMaxSR, R <= 32.
+// zero_ctas extra CTAs write zeros on the no-key bucket's rows.
 template <class Tables>
-int launch_key(const DeltaArgs& a, const Tables& tb, int n_keys, cudaStream_t stream) {
+int launch_key(const DeltaArgs& a, const Tables& tb, int n_keys, int zero_ctas,
+               cudaStream_t stream) {
   const int sr16 = (a.sr_max + 15) / 16 * 16;
   if (sr16 > kKeyMaxSR || a.R > 32) return LORA_ERR_UNSUPPORTED;
   const int smem = key_smem(sr16).total;
   auto kernel = a.R <= 16 ? delta_key_kernel<16, Tables> : delta_key_kernel<32, Tables>;
   if (prepare_kernel(kernel, smem, false) != cudaSuccess) return LORA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)n_keys, 1, 1);
+  cfg.gridDim = dim3((unsigned)(n_keys + zero_ctas), 1, 1);
   cfg.blockDim = dim3(kKeyThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
@@ -270,7 +272,7 @@ int launch_key(const DeltaArgs& a, const Tables& tb, int n_keys, cudaStream_t st
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = use_pdl() ? 1 : 0;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, a, tb));
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, a, tb, zero_ctas));
 }
 
 // The one-CTA-per-key kernel for the routed-MoE deltas (LORA_MOE_KEYED=0
@@ -916,14 +918,17 @@ int moe_delta(const MoeCall& c, void* workspace, size_t ws_bytes, uint32_t* err_
   // 0.125 ms).
   const bool keyed = moe_keyed() && (a.sr_max + 15) / 16 * 16 <= kKeyMaxSR && c.rank <= 32 &&
                      c.k_in >= n_cols;
-  rc = keyed ? launch_key(a, tb, n_keys, s) : launch_delta<kModeFused>(a, tb, n_keys, s);
+  // the per-key kernel also zeroes the pairs without an adapter (fresh output)
+  const int zero_ctas = keyed && c.zero_skipped && !sgmv ? 64 : 0;
+  rc = keyed ? launch_key(a, tb, n_keys, zero_ctas, s)
+             : launch_delta<kModeFused>(a, tb, n_keys, s);
   if (rc) return rc;
   if (sgmv) {
     Workspace wb = w;
     wb.bytes = ws_bytes;
     if ((rc = launch_sgmv(a, tb, wb, n_keys, moe_thr, s))) return rc;
   }
-  if (!c.zero_skipped) return LORA_OK;
+  if (!c.zero_skipped || zero_ctas) return LORA_OK;
   // the pairs with no adapter (the no-key bucket) are written as zeros
   zero_rows_kernel<<<1024, 256, 0, s>>>(a.out, a.ld_out, n_cols, perm, seg, n_keys);
   return cuda_status(cudaGetLastError());

@@ -65,13 +65,30 @@ __host__ __device__ inline KeySmem key_smem(int sr16) {
 
 template <int RMAX, class Tables>
 __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
-    delta_key_kernel(const DeltaArgs a, const Tables tb) {
+    delta_key_kernel(const DeltaArgs a, const Tables tb, int zero_ctas) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ SlotView v;
   __shared__ int prow[kKeyRows];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, tq = lane & 3;
   const int key = blockIdx.x;
+
+  if (key >= a.n_keys) {
+    // The last zero_ctas CTAs write zeros on the rows of the no-key bucket
+    // (MoE pairs without an adapter, when the output is written fresh).
+    cudaTriggerProgrammaticLaunchCompletion();
+    cudaGridDependencySynchronize();
+    const int z0 = a.seg_start[a.n_keys], z1 = a.seg_start[a.n_keys + 1];
+    const int vpr = a.sl.n_cols / 8;
+    const int64_t total = (int64_t)(z1 - z0) * vpr;
+    for (int64_t i = (int64_t)(key - a.n_keys) * kKeyThreads + tid; i < total;
+         i += (int64_t)zero_ctas * kKeyThreads) {
+      const int r = (int)(i / vpr), c = (int)(i - (int64_t)r * vpr);
+      *reinterpret_cast<uint4*>(a.out + tb.out_row(a.perm[z0 + r]) * a.ld_out + c * 8) =
+          make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
 
   if (tid == 0) {
     uint32_t bad = 0;
