@@ -911,13 +911,10 @@ int moe_delta(const MoeCall& c, void* workspace, size_t ws_bytes, uint32_t* err_
   static const int moe_thr = env_int("LORA_MOE_SGMV_MIN_ROWS", 0);
   const bool sgmv = moe_thr >= 1 && a.sr_max <= kSgmvMaxSR && !c.pair_weight;
   if (sgmv) a.max_rows = moe_thr;
-  // One CTA per key streams the key's whole A but also expands all of its
-  // columns alone, so it is taken where the contraction is at least as long
-  // as the output row (FC1, w13: 0.122 against 0.135 ms on GB300); the down
-  // projection (k_in = I < H) stays on the cluster kernel (0.116 against
-  // 0.125 ms).
-  const bool keyed = moe_keyed() && (a.sr_max + 15) / 16 * 16 <= kKeyMaxSR && c.rank <= 32 &&
-                     c.k_in >= n_cols;
+  // One CTA per key (S * R <= 64, rank <= 32): FC1 regular 0.107 against
+  // 0.135 ms on the cluster kernel (GB300), w13 0.126 against 0.154, w2
+  // 0.115 against 0.117.
+  const bool keyed = moe_keyed() && (a.sr_max + 15) / 16 * 16 <= kKeyMaxSR && c.rank <= 32;
   // the per-key kernel also zeroes the pairs without an adapter (fresh output)
   const int zero_ctas = keyed && c.zero_skipped && !sgmv ? 64 : 0;
   rc = keyed ? launch_key(a, tb, n_keys, zero_ctas, s)

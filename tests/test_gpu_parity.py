@@ -586,8 +586,8 @@ def test_moe_many_rows_per_key_rank_32(ld, di, oracle, shared):
 
 
 def test_moe_w2_contraction_longer_than_output(ld, di, oracle):
-    """A down projection with I > H takes the per-key kernel: per-pair input rows and
-    routing weights there, ~40 pairs per key."""
+    """A down projection with I > H: per-pair input rows, routing weights, ~40 pairs per
+    key, a k tail of 8."""
     c = inputs.moe_w2_case(seed=49, T=120, top_k=2, E=3, H=64, I=136, rank=16, L=2,
                            p_none=0.1)
     got, err = run_w2(ld, di, c, weights=c.topk_weights)
@@ -597,6 +597,29 @@ def test_moe_w2_contraction_longer_than_output(ld, di, oracle):
     assert_close(got, ref, "w2 I > H")
     keep = np.all(ref == c.y0, axis=2)
     assert np.array_equal(got[keep], c.y0[keep])
+
+
+def test_moe_rank_64_takes_the_cluster_kernel(ld, di, oracle):
+    """Rank 64 (S * R = 128 for the regular banks; rank above the per-key kernel's 32):
+    FC1, w13 and w2 with routing weights on the cluster kernel."""
+    mc = inputs.moe_case(seed=51, T=60, top_k=3, E=4, H=128, I=40, rank=64, L=2, p_none=0.1)
+    got, err = run_moe(ld, di, mc)
+    ref, ref_err = oracle.moe_fc1(mc.x, mc.A_banks, mc.B_banks, mc.topk_ids, mc.lora_ids, mc.I,
+                                  mc.rank, mc.scale, False, mc.L)
+    assert err == ref_err == 0
+    assert_close(got, ref, "moe fc1 rank 64")
+    y0 = inputs.moe_y0(51, (mc.T, mc.top_k, 2 * mc.I))
+    got, err = run_w13(ld, di, mc, y0)
+    ref, _ = oracle.moe_w13(y0, mc.x, mc.A_banks, mc.B_banks, mc.topk_ids, mc.lora_ids, mc.I,
+                            mc.rank, mc.scale, False, mc.L)
+    assert err == 0
+    assert_close(got, ref, "w13 rank 64")
+    c = inputs.moe_w2_case(seed=53, T=60, top_k=3, E=4, H=96, I=48, rank=64, L=2, p_none=0.1)
+    got, err = run_w2(ld, di, c, weights=c.topk_weights)
+    ref, ref_err = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids,
+                                 c.rank, c.scale, c.L, topk_weights=c.topk_weights)
+    assert err == ref_err == 0
+    assert_close(got, ref, "w2 rank 64")
 
 
 # ------------------------------------------------- tensor-core (SGMV) path --
