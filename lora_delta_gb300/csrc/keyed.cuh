@@ -17,11 +17,12 @@
 //     product and split the k-steps of a chunk when there are fewer tiles
 //     than warps; mma.sync m16n8k16, fp32 accumulate.
 //   * the k-group partials meet in shared memory as the fp32 h [rows][pairs];
-//   * expand + fold: every warp takes 8-column tiles of the key's slices; h
-//     as a bf16 (hi, lo) pair on the A side (rows), B fragments and the out
-//     values loaded from L2 (prefetched at the start of the pass) in batches
-//     of four tiles (one at rank 32), then RN_bf16(out + scale * w_row * d) stored in place
-//     (or RN_bf16(scale * w_row * d) without add_inputs).
+//   * expand + fold: the key's B rows (and, in place, the pass's out
+//     segments) go through the idle ring in (slice, column chunk) items,
+//     double-buffered in its two halves; every warp takes 8-column tiles of
+//     the chunk, h as a bf16 (hi, lo) pair on the A side (rows), B fragments
+//     by ldmatrix, then RN_bf16(out + scale * w_row * d) stored in place (or
+//     RN_bf16(scale * w_row * d) without add_inputs).
 #pragma once
 
 #include "bgmv.cuh"
@@ -37,6 +38,13 @@ constexpr int kKeyStages = 5;             // ring depth
 constexpr int kKeyStride = kKeyKC + 8;    // padded row (elements): ldmatrix conflict-free
 constexpr int kKeyMaxSR = 64;             // largest S * R (rounded to 16) this kernel takes
 
+// ldmatrix of two 8x8 b16 matrices (lanes 0-15 give the row addresses).
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
 // 16-byte asynchronous global -> shared copy to a shared-window address.
 __device__ __forceinline__ void cp_async16_s(uint32_t saddr, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gsrc) : "memory");
@@ -44,13 +52,18 @@ __device__ __forceinline__ void cp_async16_s(uint32_t saddr, const void* gsrc) {
 
 // Shared-memory plan (bytes), identical on host and device.
 struct KeySmem {
-  int stage_bytes, ring_off, p_off, h_off, total;
+  int stage_bytes, ring_off, ring_bytes, p_off, h_off, total;
 };
 __host__ __device__ inline KeySmem key_smem(int sr16) {
   KeySmem p;
   p.stage_bytes = (sr16 + kKeyRows) * kKeyStride * 2;
   p.ring_off = 0;
-  int o = kKeyStages * p.stage_bytes;
+  // at least the ring of S * R = 32: the expand stages its B / out chunks in
+  // the two halves of this region, and a small S * R has a long expand
+  p.ring_bytes = kKeyStages * p.stage_bytes;
+  const int min_ring = kKeyStages * (32 + kKeyRows) * kKeyStride * 2;
+  if (p.ring_bytes < min_ring) p.ring_bytes = min_ring;
+  int o = p.ring_bytes;
   o = (o + 127) / 128 * 128;
   p.p_off = o;  // k-group partials [G - 1][rows][sr16] (group 0 writes h directly)
   const int mt = sr16 / 16;
@@ -170,7 +183,6 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
       (uint32_t)((SR16 + my_rg * 16 + ((lane >> 4) << 3) + (lane & 7)) * kKeyStride +
                  ((lane >> 3) & 1) * 8) * 2u;
   constexpr int KS = RMAX / 16;
-  constexpr int NB = KS == 1 ? 2 : 1;  // expand tiles per load batch (registers)
   bool first_pass = true;
 
   for (int p0 = 0; p0 < nrows; p0 += kKeyRows) {
@@ -266,6 +278,10 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
     }
 
     // ---- expand + fold ------------------------------------------------------
+    // The key's B goes through the idle ring in (slice, column chunk) items,
+    // double-buffered in its two halves; fragments come from shared memory
+    // by ldmatrix (B rows padded to R + 8 elements: conflict-free), so a
+    // chunk costs one copy round trip instead of one per batch of tiles.
     const int nm = nr > 16 ? 2 : 1;  // 16-row m-tiles of the pass
     int orow[2][2];  // (row < n <= 2^30)
     float sc[2][2];
@@ -279,77 +295,122 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
         orow[mi][h] = ok[mi][h] ? (int)tb.out_row(prow[r]) : 0;
         sc[mi][h] = ok[mi][h] ? v.scale * tb.row_weight(prow[r]) : 0.f;
       }
-    for (int j = 0; j < a.sl.S; ++j) {
+    // A half holds the chunk's B rows [cc][bstride] and, with add_inputs, its
+    // out segments [kKeyRows][ostride] (a stride of 4 words mod 8: the
+    // fragment reads are conflict-free); cc is chosen so that both fit.
+    const int bstride = R + 8;
+    const uint32_t half_bytes = ((uint32_t)plan.ring_bytes / 2u) & ~15u;
+    const int per_col = bstride * 2 + (a.add_inputs ? kKeyRows * 2 : 0);
+    const int cc = (int)((half_bytes - (a.add_inputs ? kKeyRows * 32u : 0u)) / (uint32_t)per_col) / 8 * 8;
+    const int ostride = cc + (cc % 16 == 0 ? 8 : 16);  // elements, 8 mod 16: <= cc + 16
+    const uint32_t o_off = (uint32_t)(cc * bstride * 2);
+    const int vpc = R / 8;  // 16-byte pieces per B column
+    auto first_slice = [&](int j) {
+      while (j < a.sl.S && v.ja[j] < 0) ++j;
+      return j;
+    };
+    auto issue_b = [&](int j, int c0, uint32_t hb) {
+      const int cw = min(cc, a.sl.width[j] - c0);
+      const __nv_bfloat16* src = v.B[j] + (size_t)c0 * R;
+      for (int i = tid; i < cw * vpc; i += kKeyThreads) {
+        const int col = i / vpc, part = i - col * vpc;
+        cp_async16_s(hb + (uint32_t)(col * bstride + part * 8) * 2u, src + (size_t)col * R + part * 8);
+      }
+      if (a.add_inputs) {
+        const int ppr = cw / 8;  // pieces per out row
+        for (int i = tid; i < nr * ppr; i += kKeyThreads) {
+          const int r = i / ppr, q = i - r * ppr;
+          cp_async16_s(hb + o_off + (uint32_t)(r * ostride + q * 8) * 2u,
+                       a.out + tb.out_row(prow[r]) * a.ld_out + a.sl.off[j] + c0 + q * 8);
+        }
+      }
+    };
+    // ldmatrix row address of this lane inside a chunk (matrix lane / 8 is k
+    // block lane / 8 of the tile's 8 columns)
+    const uint32_t b_frag = (uint32_t)((lane & 7) * bstride + ((lane >> 3) & (KS * 2 - 1)) * 8) * 2u;
+    int j = first_slice(0), c0 = 0, hsel = 0;
+    if (j < a.sl.S) issue_b(j, c0, ring_s);
+    cp_async_commit();
+    int ja_split = -1;  // slice whose h fragments are in registers
+    uint32_t ahi[2][KS][4], alo[2][KS][4];
+    while (j < a.sl.S) {
+      // the next item into the other half
+      int jn = j, cn = c0 + cc;
+      if (cn >= a.sl.width[j]) {
+        cn = 0;
+        jn = first_slice(j + 1);
+      }
+      if (jn < a.sl.S) issue_b(jn, cn, ring_s + (hsel ^ 1) * half_bytes);
+      cp_async_commit();
+      cp_async_wait<1>();  // this item's chunk landed
+      __syncthreads();
       const int ja = v.ja[j];
-      if (ja < 0) continue;
-      const int ntl = a.sl.width[j] / 8;
-      if (warp >= ntl) continue;
-      uint32_t ahi[2][KS][4], alo[2][KS][4];
+      if (ja != ja_split) {  // h of the slice as bf16 (hi, lo) A fragments
+        ja_split = ja;
 #pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        const float* hb = H + ja * R + 2 * tq + (mi * 16 + gq) * SR16;
+        for (int mi = 0; mi < 2; ++mi) {
+          const float* hb = H + ja * R + 2 * tq + (mi * 16 + gq) * SR16;
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            const bool lo_ok = mi < nm && kk * 16 < R, hi_ok = mi < nm && kk * 16 + 8 < R;
+            const float* h0 = hb + kk * 16;
+            const float* h1 = h0 + 8 * SR16;
+            split_bf16x2(lo_ok ? h0[0] : 0.f, lo_ok ? h0[1] : 0.f, ahi[mi][kk][0], alo[mi][kk][0]);
+            split_bf16x2(lo_ok ? h1[0] : 0.f, lo_ok ? h1[1] : 0.f, ahi[mi][kk][1], alo[mi][kk][1]);
+            split_bf16x2(hi_ok ? h0[8] : 0.f, hi_ok ? h0[9] : 0.f, ahi[mi][kk][2], alo[mi][kk][2]);
+            split_bf16x2(hi_ok ? h1[8] : 0.f, hi_ok ? h1[9] : 0.f, ahi[mi][kk][3], alo[mi][kk][3]);
+          }
+        }
+      }
+      const int cw = min(cc, a.sl.width[j] - c0);
+      const uint32_t hbase = ring_s + hsel * half_bytes + b_frag;
+      const int64_t cbase = a.sl.off[j] + c0 + 2 * tq;
+      const __nv_bfloat16* os = reinterpret_cast<const __nv_bfloat16*>(
+          ring + (size_t)hsel * half_bytes + o_off) + 2 * tq;
+      for (int t = warp; t < cw / 8; t += kKeyWarps) {
+        uint32_t bf[KS][2];
+        const uint32_t ba = hbase + (uint32_t)(t * 8 * bstride) * 2u;
+        if (KS == 1) {
+          ldsm_x2(ba, bf[0][0], bf[0][1]);
+        } else {
+          ldsm_x4(ba, bf[0][0], bf[0][1], bf[KS - 1][0], bf[KS - 1][1]);
+        }
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
-          const bool lo_ok = mi < nm && kk * 16 < R, hi_ok = mi < nm && kk * 16 + 8 < R;
-          const float* h0 = hb + kk * 16;
-          const float* h1 = h0 + 8 * SR16;
-          split_bf16x2(lo_ok ? h0[0] : 0.f, lo_ok ? h0[1] : 0.f, ahi[mi][kk][0], alo[mi][kk][0]);
-          split_bf16x2(lo_ok ? h1[0] : 0.f, lo_ok ? h1[1] : 0.f, ahi[mi][kk][1], alo[mi][kk][1]);
-          split_bf16x2(hi_ok ? h0[8] : 0.f, hi_ok ? h0[9] : 0.f, ahi[mi][kk][2], alo[mi][kk][2]);
-          split_bf16x2(hi_ok ? h1[8] : 0.f, hi_ok ? h1[9] : 0.f, ahi[mi][kk][3], alo[mi][kk][3]);
+          if (kk * 16 + 8 >= R) bf[kk][1] = 0u;  // k past the rank: padding
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+          if (mi >= nm) continue;
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            if (kk * 16 < R) {
+              mma_16816(d, ahi[mi][kk][0], ahi[mi][kk][1], ahi[mi][kk][2], ahi[mi][kk][3],
+                        bf[kk][0], bf[kk][1]);
+              mma_16816(d, alo[mi][kk][0], alo[mi][kk][1], alo[mi][kk][2], alo[mi][kk][3],
+                        bf[kk][0], bf[kk][1]);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            if (ok[mi][h]) {
+              const uint32_t o =
+                  a.add_inputs ? *reinterpret_cast<const uint32_t*>(
+                                     os + (mi * 16 + gq + 8 * h) * ostride + t * 8)
+                               : 0u;
+              *reinterpret_cast<uint32_t*>(a.out + (int64_t)orow[mi][h] * a.ld_out + cbase +
+                                           t * 8) =
+                  pack_bf16x2(bf16lo(o) + sc[mi][h] * d[2 * h], bf16hi(o) + sc[mi][h] * d[2 * h + 1]);
+            }
         }
       }
-      const __nv_bfloat16* bbase = v.B[j] + (size_t)gq * R + 2 * tq;
-      const int64_t cbase = a.sl.off[j] + 2 * tq;
-      for (int t0 = warp; t0 < ntl; t0 += kKeyWarps * NB) {
-        uint32_t bf[NB][KS][2], ov[NB][2][2];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {  // every load of the batch first
-          const int t = t0 + b * kKeyWarps;
-          if (t < ntl) {
-            const __nv_bfloat16* brow = bbase + (size_t)t * 8 * R;
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-              bf[b][kk][0] = (kk * 16 < R) ? ldg_nc_u32(brow + kk * 16) : 0u;
-              bf[b][kk][1] = (kk * 16 + 8 < R) ? ldg_nc_u32(brow + kk * 16 + 8) : 0u;
-            }
-#pragma unroll
-            for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                ov[b][mi][h] = (a.add_inputs && ok[mi][h])
-                                   ? *reinterpret_cast<const uint32_t*>(
-                                         a.out + (int64_t)orow[mi][h] * a.ld_out + cbase + t * 8)
-                                   : 0u;
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const int t = t0 + b * kKeyWarps;
-          if (t >= ntl) continue;
-#pragma unroll
-          for (int mi = 0; mi < 2; ++mi) {
-            if (mi >= nm) continue;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-              if (kk * 16 < R) {
-                mma_16816(d, ahi[mi][kk][0], ahi[mi][kk][1], ahi[mi][kk][2], ahi[mi][kk][3],
-                          bf[b][kk][0], bf[b][kk][1]);
-                mma_16816(d, alo[mi][kk][0], alo[mi][kk][1], alo[mi][kk][2], alo[mi][kk][3],
-                          bf[b][kk][0], bf[b][kk][1]);
-              }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              if (ok[mi][h])
-                *reinterpret_cast<uint32_t*>(a.out + (int64_t)orow[mi][h] * a.ld_out + cbase + t * 8) =
-                    pack_bf16x2(bf16lo(ov[b][mi][h]) + sc[mi][h] * d[2 * h],
-                                bf16hi(ov[b][mi][h]) + sc[mi][h] * d[2 * h + 1]);
-          }
-        }
-      }
+      __syncthreads();  // this half is free for the item after next
+      j = jn;
+      c0 = cn;
+      hsel ^= 1;
     }
+    cp_async_wait<0>();  // (an empty group)
   }
 }
 
