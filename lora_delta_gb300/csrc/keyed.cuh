@@ -1,8 +1,8 @@
 // The routed delta for many keys with a few dozen rows each (the routed-MoE
 // deltas: "flashinfer.fused_moe.bgmv_moe_gemm1_lora_delta" and the in-place
 // w13 / w2 deltas of "punica_base.py"): one CTA per key, which streams the
-// key's whole A through a deep cp.async ring and expands straight from
-// registers.  There are hundreds of keys, so the grid fills the GPU without
+// key's whole A through a deep cp.async ring, then its B through the same
+// ring for the expand.  There are hundreds of keys, so the grid fills the GPU without
 // splitting a key over a cluster, and no partial sums cross CTAs.
 //
 // Per key (rows from the routing sort, in passes of 32):
