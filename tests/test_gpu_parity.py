@@ -622,6 +622,40 @@ def test_moe_rank_64_takes_the_cluster_kernel(ld, di, oracle):
     assert_close(got, ref, "w2 rank 64")
 
 
+def test_moe_edge_cases_on_the_per_key_kernel(ld, di, oracle):
+    """Pass boundaries (keys with exactly 32 and 33 pairs at top-1), no local expert at all
+    (an expert map of -1: y untouched, no error), every adapter switched off (w2: y
+    untouched), and an empty batch (T = 0: nothing launched, status OK)."""
+    import torch
+    # top-1, two experts, one adapter: expert 0 gets 32 tokens, expert 1 gets 33
+    mc = inputs.moe_case(seed=55, T=65, top_k=1, E=2, H=64, I=16, rank=16, L=1, p_none=0.0)
+    topk = np.array([[0]] * 32 + [[1]] * 33, dtype=np.int32)
+    got, err = run_moe(ld, di, mc, topk=topk)
+    ref, ref_err = oracle.moe_fc1(mc.x, mc.A_banks, mc.B_banks, topk, mc.lora_ids, mc.I,
+                                  mc.rank, mc.scale, False, mc.L)
+    assert err == ref_err == 0
+    assert_close(got, ref, "moe 32 / 33 pairs per key")
+
+    y0 = inputs.moe_y0(55, (mc.T, mc.top_k, 2 * mc.I))
+    none_local = np.full(4, -1, np.int32)
+    got, err = run_w13(ld, di, mc, y0, expert_map=none_local, topk=topk)
+    assert err == 0 and np.array_equal(got, y0)
+
+    c = inputs.moe_w2_case(seed=57, T=40, top_k=2, E=3, H=64, I=32, rank=16, L=2, p_none=0.0)
+    got, err = run_w2(ld, di, c, adapter_enabled=np.zeros(2, np.int32), weights=c.topk_weights)
+    assert err == 0 and np.array_equal(got, c.y0)
+
+    dm = di.moe_to_device(mc)
+    empty_x = torch.empty(0, mc.H, dtype=torch.bfloat16, device="cuda")
+    empty_ids = torch.empty(0, 1, dtype=torch.int32, device="cuda")
+    empty_l = torch.empty(0, dtype=torch.int32, device="cuda")
+    out = torch.empty(0, 1, 2 * mc.I, dtype=torch.bfloat16, device="cuda")
+    e = ld.new_error_word()
+    ld.lora_moe_fc1_delta(out, empty_x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b, False,
+                          empty_ids, empty_l, mc.E, mc.I, mc.rank, mc.L, mc.scale, err=e)
+    assert ld.lora_get_error(e) == 0
+
+
 # ------------------------------------------------- tensor-core (SGMV) path --
 
 def _hot_slots_case(seed, n, k_in, widths, R, ranks, hot=(0, 1), **kw):
