@@ -393,13 +393,17 @@ Workspace carve(void* ws, int n, int n_keys) {
 }
 
 // Rows per key from which the tensor-core (SGMV) path takes a key over from
-// the small-segment kernel; LORA_SGMV_MIN_ROWS overrides, read once.
-int sgmv_min_rows() {
-  static const int v = [] {
-    const int x = env_int("LORA_SGMV_MIN_ROWS", 64);
-    return x < 1 ? 1 : x;
-  }();
-  return v;
+// the small-segment kernel, by the size of a slot's weights;
+// LORA_SGMV_MIN_ROWS overrides, read once.
+int sgmv_min_rows(int S, int R, int k_in) {
+  static const int forced = env_int("LORA_SGMV_MIN_ROWS", 0);
+  if (forced >= 1) return forced;
+  // Measured on GB300: a slot whose weights are large (the skewed workload,
+  // R 64 over k_in 5120 / 13824: 0.64 / 1.7 MiB) streams them faster on the
+  // tensor-core path from 16 rows on (0.288 against 0.331 ms at 64); a small
+  // one (the expert fold, 64 KiB) keeps the cluster kernel below 64 rows.
+  const int64_t slot_bytes = (int64_t)S * R * k_in * 2;
+  return slot_bytes >= (512 << 10) ? 16 : 64;
 }
 
 // Batches of at least this many rows are clustered by the routing kernel when
@@ -778,7 +782,7 @@ int lora_delta_segmented(void* out, int64_t ld_out, const void* x, int n, int k_
   plan_tiles(a, k_in, a.sl.n_cols, a.sr_max, kModeFused);
   LinearTables tb{a_table, b_table, scale_table, n_segs};
   const bool sgmv = a.sr_max <= kSgmvMaxSR;
-  const int thr = sgmv_min_rows();
+  const int thr = sgmv_min_rows(S, R, k_in);
   if (sgmv) a.max_rows = thr;
   rc = launch_delta<kModeFused>(a, tb, n_segs, st);
   if (rc || !sgmv) return rc;
@@ -817,7 +821,7 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
   LinearTables tb{a_table, b_table, scale_table, max_loras};
   // keys with many rows go to the tensor-core path, the others stay here
   const bool sgmv = a.perm != nullptr && a.sr_max <= kSgmvMaxSR;
-  const int thr = sgmv_min_rows();
+  const int thr = sgmv_min_rows(S, R, k_in);
   if (sgmv) a.max_rows = thr;
   // when the average slot has enough rows for the tensor-core path, most
   // slots will leave the cluster kernel at once: no early weight copies
