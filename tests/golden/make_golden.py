@@ -34,6 +34,23 @@ def tiny_moe(shared):
     return c, out, err
 
 
+def tiny_w13():
+    c = inputs.moe_case(shared_a=False, T=6, top_k=2, E=4, H=32, I=8, rank=4, L=2)
+    y0 = inputs.moe_y0(c.seed, (c.T, c.top_k, 2 * c.I))
+    emap = np.array([1, -1, 0, 3, 2, -1], dtype=np.int32)  # 6 global experts, 4 local
+    topk = np.minimum(c.topk_ids * 2, 5).astype(np.int32)  # global ids
+    y, err = oracle.moe_w13(y0, c.x, c.A_banks, c.B_banks, topk, c.lora_ids, c.I, c.rank,
+                            c.scale, False, c.L, expert_map=emap)
+    return c, y, err
+
+
+def tiny_w2():
+    c = inputs.moe_w2_case(T=6, top_k=2, E=4, H=16, I=24, rank=8, L=2)
+    y, err = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.rank,
+                           c.scale, c.L, topk_weights=c.topk_weights)
+    return c, y, err
+
+
 def write(path, header, arr):
     with open(path, "w") as f:
         for line in header:
@@ -63,6 +80,23 @@ def main():
             f"lora_ids {' '.join(str(int(v)) for v in c.lora_ids)}; error word {err}",
             "Written by tests/golden/make_golden.py (oracle only).",
         ], out)
+    c, y, err = tiny_w13()
+    write(os.path.join(HERE, "tiny_moe_w13_oracle.txt"), [
+        "oracle output (bf16 bits, hex) of a tiny in-place w13 delta with an expert map",
+        "(6 global experts, 4 local): T=6, top_k=2, H=32, I=8, rank=4, L=2, scale 2, seed 1238.",
+        "Semantics: 'punica_base.py', add_lora_w13 (the delta of",
+        "'flashinfer.fused_moe.bgmv_moe_gemm1_lora_delta', added in place).",
+        f"error word {err}",
+        "Written by tests/golden/make_golden.py (oracle only).",
+    ], y)
+    c, y, err = tiny_w2()
+    write(os.path.join(HERE, "tiny_moe_w2_oracle.txt"), [
+        "oracle output (bf16 bits, hex) of a tiny in-place w2 delta with routing weights:",
+        "T=6, top_k=2, E=4, H=16, I=24, rank=8, L=2, scale 2, seed 1240.",
+        "Semantics: 'punica_base.py', add_lora_w2.",
+        f"error word {err}",
+        "Written by tests/golden/make_golden.py (oracle only).",
+    ], y)
 
 
 if __name__ == "__main__":

@@ -36,3 +36,12 @@ def test_tiny_moe_golden(oracle):
     for mode, shared in (("regular", False), ("shared", True)):
         _, out, err = make_golden.tiny_moe(shared)
         assert np.array_equal(out, read(f"tiny_moe_{mode}_oracle.txt"))
+
+
+def test_tiny_moe_in_place_golden(oracle):
+    _, y, err = make_golden.tiny_w13()
+    assert err == 0
+    assert np.array_equal(y, read("tiny_moe_w13_oracle.txt"))
+    _, y, err = make_golden.tiny_w2()
+    assert err == 0
+    assert np.array_equal(y, read("tiny_moe_w2_oracle.txt"))
