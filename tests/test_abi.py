@@ -81,3 +81,30 @@ def test_host_validation_without_a_gpu(library):
     # MoE: too many keys
     assert L.lora_moe_fc1_delta(fake, fake, fake, 256, fake, 256, 0, fake, fake, 4, 2, 1024, 64,
                                 16, 16, 8, 1.0, None, 0, None, None) == 6
+
+
+def test_moe_in_place_host_validation_without_a_gpu(library):
+    """The in-place MoE calls check their arguments on the host, before any launch."""
+    import lora_delta_gb300 as ld
+    L = ld.lib()
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    # w13: T = 0 is a no-op
+    assert L.lora_moe_w13_delta(None, None, None, 0, None, 0, 0, None, None, None, 0, None, 0,
+                                2, 4, 64, 16, 16, 2, 1.0, 1, None, 0, None, None) == 0
+    # w13: an expert map without its size -> LORA_ERR_ARG
+    assert L.lora_moe_w13_delta(fake, fake, fake, 256, fake, 256, 0, fake, fake, fake, 0, None,
+                                4, 2, 4, 64, 16, 16, 2, 1.0, 1, None, 0, None, None) == 1
+    # w13: I not a multiple of 8 -> LORA_ERR_ALIGN
+    assert L.lora_moe_w13_delta(fake, fake, fake, 256, fake, 256, 0, fake, fake, None, 0, None,
+                                4, 2, 4, 64, 12, 16, 2, 1.0, 1, None, 0, None, None) == 3
+    # w2: NULL y -> LORA_ERR_ARG
+    assert L.lora_moe_w2_delta(None, fake, fake, 256, fake, 256, fake, fake, None, 0, None, None,
+                               4, 2, 4, 64, 16, 16, 2, 1.0, 1, None, 0, None, None) == 1
+    # w2: H not a multiple of 8 -> LORA_ERR_ALIGN
+    assert L.lora_moe_w2_delta(fake, fake, fake, 256, fake, 256, fake, fake, None, 0, None, None,
+                               4, 2, 4, 60, 16, 16, 2, 1.0, 1, None, 0, None, None) == 3
+    # w2: rank past 128 -> LORA_ERR_UNSUPPORTED; no workspace -> LORA_ERR_WORKSPACE
+    assert L.lora_moe_w2_delta(fake, fake, fake, 256, fake, 256, fake, fake, None, 0, None, None,
+                               4, 2, 4, 64, 16, 256, 2, 1.0, 1, None, 0, None, None) == 6
+    assert L.lora_moe_w2_delta(fake, fake, fake, 256, fake, 256, fake, fake, None, 0, None, None,
+                               4, 2, 4, 64, 16, 16, 2, 1.0, 1, None, 0, None, None) == 5

@@ -189,6 +189,19 @@ def test_single_slot_many_rows_and_rank8(ld, di, oracle):
     check_linear(oracle, case, got, err)
 
 
+def test_single_row_and_true_rank_one(ld, di, oracle):
+    """One row (on a rank-1 adapter padded to 16), and a batch over adapters of true
+    ranks 1, 2, 5 and 16 with rsLoRA scales."""
+    case = inputs.linear_case(7, n=1, k_in=264, widths=(136,), max_loras=2, max_rank=16,
+                              ranks=[1, 16], alpha=4.0, seq_slot=np.array([0], np.int32))
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+    case = inputs.linear_case(8, n=37, k_in=264, widths=(136, 40), max_loras=4, max_rank=16,
+                              ranks=[1, 2, 5, 16], alpha=4.0, p_none=0.1, use_rslora=True)
+    got, err, _ = run_fused(ld, di, case)
+    check_linear(oracle, case, got, err)
+
+
 def test_table_zero_scale_zero_and_offsets(ld, di, oracle):
     adapted = [[True, False, True], [False, False, False], [True, True, True],
                [False, True, False]]
