@@ -1,8 +1,9 @@
 """The data-parallel split, on two CPU processes over gloo.
 
-Rows of the linear delta and tokens of the MoE FC1 delta are independent
+Rows of the linear delta and tokens of the MoE deltas are independent
 ("Module lora_delta": one adapter per row through LoraRoute;
-"bgmv_moe_gemm1_lora_delta": the delta stays per (token, slot)).  Ranks that
+"bgmv_moe_gemm1_lora_delta": the delta stays per (token, slot); the in-place w2
+delta of "punica_base.py" reads each pair's own activation row).  Ranks that
 each apply the delta to their own contiguous shard, with the adapter pool
 replicated, therefore reproduce the whole batch bit for bit, with no
 collective on the data path.  The test also checks the host reductions the
@@ -69,6 +70,19 @@ def _worker(rank: int, world: int, port: int, q):
         mshards = [None] * w
         dist.all_gather_object(mshards, (tlo, thi, mo, merr))
 
+        # in-place w2 on token shards: the shard's pairs are rows tlo*top_k .. thi*top_k
+        # of the activations, its y rows are tokens tlo .. thi
+        dc = inputs.moe_w2_case(T=37, top_k=4, E=8, H=64, I=32, rank=16, L=4)
+        dlo, dhi = ldist.shard_rows(dc.T, r, w)
+        dy, derr = oracle.moe_w2(np.ascontiguousarray(dc.y0[dlo:dhi]),
+                                 np.ascontiguousarray(dc.x[dlo * dc.top_k:dhi * dc.top_k]),
+                                 dc.A_banks, dc.B_banks,
+                                 np.ascontiguousarray(dc.topk_ids[dlo:dhi]),
+                                 np.ascontiguousarray(dc.lora_ids[dlo:dhi]), dc.rank, dc.scale,
+                                 dc.L, topk_weights=np.ascontiguousarray(dc.topk_weights[dlo:dhi]))
+        dshards = [None] * w
+        dist.all_gather_object(dshards, (dlo, dhi, dy, derr))
+
         ldist.barrier()
         res["max"] = ldist.max_over_ranks(1.5 + rank)
         res["sum"] = ldist.sum_over_ranks(10 * (rank + 1))
@@ -85,6 +99,11 @@ def _worker(rank: int, world: int, port: int, q):
             mgot = np.concatenate([s[2] for s in sorted(mshards, key=lambda s: s[0])])
             res["moe_equal"] = bool(np.array_equal(mgot, mwhole))
             res["moe_cover"] = sorted((s[0], s[1]) for s in mshards)
+            dwhole, _ = oracle.moe_w2(dc.y0, dc.x, dc.A_banks, dc.B_banks, dc.topk_ids,
+                                      dc.lora_ids, dc.rank, dc.scale, dc.L,
+                                      topk_weights=dc.topk_weights)
+            dgot = np.concatenate([s[2] for s in sorted(dshards, key=lambda s: s[0])])
+            res["w2_equal"] = bool(np.array_equal(dgot, dwhole))
         dist.destroy_process_group()
         q.put((rank, res, None))
     except Exception as e:  # reported to the parent, which fails the test
@@ -130,3 +149,4 @@ def test_two_rank_shards_reproduce_the_whole_batch(oracle):
     assert werr == (shard_errs[0] | shard_errs[1])
     assert r0["moe_cover"] == [(0, 19), (19, 37)]
     assert r0["moe_equal"]
+    assert r0["w2_equal"]
