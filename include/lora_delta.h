@@ -72,6 +72,22 @@ const char *lora_status_string(int status);
 int lora_abi_version(void);
 
 /*
+ * lora_set_wait_limit_ns -- set the limit, in nanoseconds of the GPU's global
+ * timer, after which a bounded wait inside a kernel gives up; returns the
+ * previous limit.  None of the pages has this: it is a guard of this
+ * library's own kernels.  Every mbarrier wait of the tensor-core kernels is
+ * bounded; one that runs out sets LORA_DEV_ERR_TIMEOUT in the call's error
+ * word, and its CTA skips its stores, lets its issued MMAs finish, frees its
+ * tensor memory and returns, so the context stays usable.  The default is
+ * 2 s (2000000000), far above any legitimate wait.  0 makes a wait give up at
+ * its first poll that finds the awaited phase incomplete, which lets a test
+ * run the time-out path without a fault or a hang.  Process-wide; each
+ * launch copies the value current when it is enqueued (a captured CUDA
+ * graph keeps the value of its capture).  Thread-safe.
+ */
+uint64_t lora_set_wait_limit_ns(uint64_t ns);
+
+/*
  * lora_scale -- the adapter scale ([metrale] LoraPair): alpha / r, or
  * alpha / sqrt(r) when use_rslora is nonzero.  Computed on the host; the
  * caller stores it in its scale table.  Applied in the fold (after the
@@ -305,13 +321,18 @@ int lora_moe_w2_delta(void *y, const void *x, const int64_t *w_ptr_a, int64_t st
  * cannot provide lora_delta_fused's scratch workspace.
  * Same arguments and results as lora_delta_fused minus the workspace: the
  * scratch comes from a fixed buffer inside the library of
- * lora_noalloc_scratch_bytes() bytes (4 MiB), held on every GPU that loads
- * the library until the process exits.  A call whose smallest workspace
- * (lora_workspace_min_size(n, S, R, max_loras)) exceeds it returns LORA_ERR_TOO_LARGE
- * and enqueues nothing.  The call never allocates (no cudaMalloc, no
- * allocating library routine).  The first call on a device looks the buffer
- * up on that device (it must be the current device), so make that first
- * call before any stream capture.  All calls share the one buffer: calls that
+ * lora_noalloc_scratch_bytes() bytes (4 MiB).  The buffer sits in its own
+ * CUDA module, which the runtime loads lazily by default: the first call on a
+ * device (with that device current) looks the buffer up, and that is when the
+ * driver reserves its 4 MiB on the device, which then holds it until the
+ * process exits.  Make one warm-up call on every device before the memory
+ * budget is fixed and before any stream capture; later calls reserve
+ * nothing.  The looked-up address is cached per device and is stale after a
+ * cudaDeviceReset.  A call whose smallest workspace
+ * (lora_workspace_min_size(n, S, R, max_loras)) exceeds the buffer returns
+ * LORA_ERR_TOO_LARGE and enqueues nothing.  Apart from that first reservation
+ * the call never allocates (no cudaMalloc, no allocating library routine).
+ * All calls share the one buffer: calls that
  * may overlap on the GPU (different streams) race and must be serialized by
  * the caller.  The buffer keeps the last call's contents; nothing in it needs
  * to start at zero.

@@ -27,8 +27,12 @@ __all__ = [
     "lora_delta_segmented",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_moe_w13_delta",
     "lora_moe_w2_delta", "lora_get_error", "new_error_word",
-    "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes",
+    "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes", "lora_set_wait_limit_ns",
+    "WAIT_LIMIT_DEFAULT_NS",
 ]
+
+# Default limit of the kernels' bounded waits (2 s of the GPU's global timer).
+WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
 
 
 class LoraError(RuntimeError):
@@ -79,6 +83,13 @@ def lora_scale(alpha: float, r: int, use_rslora: bool = False) -> float:
     return float(lib().lora_scale(float(alpha), int(r), int(bool(use_rslora))))
 
 
+def lora_set_wait_limit_ns(ns: int) -> int:
+    """Set the limit of the kernels' bounded waits (ns of the GPU's global timer;
+    0: give up at the first incomplete poll, for tests of the time-out path);
+    returns the previous limit.  Process-wide, read by each launch."""
+    return int(lib().lora_set_wait_limit_ns(int(ns)))
+
+
 def lora_workspace_size(n: int, S: int, R: int, max_loras: int) -> int:
     return int(lib().lora_workspace_size(int(n), int(S), int(R), int(max_loras)))
 
@@ -93,13 +104,29 @@ def lora_moe_workspace_size(T: int, top_k: int, E: int, num_loras: int, rank: in
                                              int(rank), int(bool(shared_a))))
 
 
-def _workspace(nbytes: int, workspace, device):
+# Scratch workspaces the binding keeps for callers that pass none: one per
+# (device, stream), grown when a call needs more and otherwise reused, so a
+# steady stream of calls allocates nothing.  Calls on one stream run in
+# order, so they may share one; calls on different streams get different ones.
+_WS_CACHE: dict = {}
+
+
+def _workspace(nbytes: int, workspace, device, stream=None):
     if workspace is not None:
         return workspace, workspace.numel() * workspace.element_size()
     if nbytes == 0:
         return None, 0
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    return ws, nbytes
+    device = torch.device(device)
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           s.cuda_stream)
+    ws = _WS_CACHE.get(key)
+    if ws is None or ws.numel() < nbytes:
+        _WS_CACHE.pop(key, None)
+        with torch.cuda.stream(s):  # the allocator then reuses it on this stream only
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _WS_CACHE[key] = ws
+    return ws, ws.numel()
 
 
 # -------------------------------------------------------------------- pack --
@@ -195,13 +222,10 @@ def lora_route_with_scratch(seq_slot: torch.Tensor, max_loras: int, scratch=None
     perm = torch.empty(max(n, 1), dtype=torch.int32, device=dev) if perm is None else perm
     seg_start = (torch.empty(max_loras + 2, dtype=torch.int32, device=dev)
                  if seg_start is None else seg_start)
-    nbytes = lora_route_scratch_size(n, max_loras)
-    if scratch is None:
-        scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    scratch, sbytes = _workspace(lora_route_scratch_size(n, max_loras), scratch, dev, stream)
     _check("lora_route_with_scratch",
            lib().lora_route_with_scratch(_ptr(perm), _ptr(seg_start), _ptr(seq_slot), n,
-                                         int(max_loras), _ptr(scratch),
-                                         scratch.numel() * scratch.element_size(), _ptr(err),
+                                         int(max_loras), _ptr(scratch), sbytes, _ptr(err),
                                          _stream(stream)))
     return perm, seg_start
 
@@ -216,7 +240,7 @@ def lora_shrink(h, x, seq_slot, pool: LoraPool, scale_table=None, workspace=None
     _dev(seq_slot, "seq_slot", torch.int32)
     n, k_in = x.shape
     ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, pool.max_loras) if n > 1024
-                         else 0, workspace, x.device)
+                         else 0, workspace, x.device, stream)
     _check("lora_shrink", lib().lora_shrink(
         _ptr(h), _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table), _ptr(scale_table),
         pool.S, pool.R, pool.max_loras, _ptr(ws), wsb, _ptr(err), _stream(stream)))
@@ -230,7 +254,7 @@ def lora_expand(out, h, seq_slot, pool: LoraPool, scale_table=None, offset_start
     _dev(seq_slot, "seq_slot", torch.int32)
     n, ld_out = out.shape
     ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, pool.max_loras) if n > 1024
-                         else 0, workspace, out.device)
+                         else 0, workspace, out.device, stream)
     w = _widths_arg(pool.widths)
     _check("lora_expand", lib().lora_expand(
         _ptr(out), ld_out, _ptr(h), _ptr(seq_slot), _ptr(pool.b_table), _ptr(scale_table), w,
@@ -252,7 +276,7 @@ def lora_delta_fused(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,
     # batches of >= 256 rows get a workspace: they are clustered by slot, and
     # slots with many rows take the tensor-core path
     ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, pool.max_loras) if n >= 256
-                         else 0, workspace, x.device)
+                         else 0, workspace, x.device, stream)
     w = _widths_arg(pool.widths)
     _check("lora_delta_fused", lib().lora_delta_fused(
         _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
@@ -275,7 +299,8 @@ def lora_delta_segmented(out, x, seg_start, pool: LoraPool, offset_start: int = 
     if n_segs != pool.max_loras:
         raise ValueError("seg_start must have pool.max_loras + 1 entries")
     st = pool.scale_table if scale_table is None else scale_table
-    ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, n_segs), workspace, x.device)
+    ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, n_segs), workspace, x.device,
+                         stream)
     w = _widths_arg(pool.widths)
     _check("lora_delta_segmented", lib().lora_delta_segmented(
         _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seg_start), n_segs, _ptr(pool.a_table),
@@ -320,7 +345,7 @@ def lora_moe_fc1_delta(out, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, s
     T, H = x.shape
     top_k = topk_ids.shape[1]
     ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras, rank, shared_a),
-                         workspace, x.device)
+                         workspace, x.device, stream)
     _check("lora_moe_fc1_delta", lib().lora_moe_fc1_delta(
         _ptr(out), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
         int(bool(shared_a)), _ptr(topk_ids), _ptr(lora_ids), T, top_k, int(E), H, int(I),
@@ -350,7 +375,7 @@ def lora_moe_w13_delta(y, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, sha
     T, H = x.shape
     top_k = topk_ids.shape[1]
     ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras, rank, shared_a),
-                         workspace, x.device)
+                         workspace, x.device, stream)
     _check("lora_moe_w13_delta", lib().lora_moe_w13_delta(
         _ptr(y), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
         int(bool(shared_a)), _ptr(topk_ids), _ptr(lora_ids), _ptr(expert_map),
@@ -379,7 +404,7 @@ def lora_moe_w2_delta(y, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, topk
     if x.shape[0] != T * top_k:
         raise ValueError("x must hold one row per (token, slot) pair")
     ws, wsb = _workspace(lora_moe_workspace_size(T, top_k, E, num_loras, rank, True),
-                         workspace, x.device)
+                         workspace, x.device, stream)
     _check("lora_moe_w2_delta", lib().lora_moe_w2_delta(
         _ptr(y), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
         _ptr(topk_ids), _ptr(lora_ids), _ptr(expert_map),

@@ -21,6 +21,7 @@ _f = _c.c_float
 SIGNATURES = {
     "lora_status_string": (_c.c_char_p, [_i]),
     "lora_abi_version": (_i, []),
+    "lora_set_wait_limit_ns": (_c.c_uint64, [_c.c_uint64]),
     "lora_scale": (_f, [_f, _i, _i]),
     "lora_pool_pack": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "lora_workspace_size": (_sz, [_i, _i, _i, _i]),

@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -73,6 +74,9 @@ bool use_pdl() {
   static const bool on = env_int("LORA_PDL", 1) != 0;
   return on;
 }
+// Limit of the kernels' bounded waits, read at each launch
+// (lora_set_wait_limit_ns).
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 
 // Per-(kernel, device) function attributes, set once: the dynamic shared
 // memory opt-in (to the largest size requested so far) and the non-portable
@@ -494,6 +498,7 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   s.chunk0[kMaxSlices] = nch;
   s.add_inputs = d.add_inputs;
   s.err = d.err;
+  s.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -626,6 +631,10 @@ const char* lora_status_string(int status) {
 }
 
 int lora_abi_version(void) { return kAbiVersion; }
+
+uint64_t lora_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns, std::memory_order_relaxed);
+}
 
 float lora_scale(float alpha, int r, int use_rslora) {
   if (r <= 0) return 0.0f;

@@ -16,7 +16,9 @@ constexpr int kMaxRank = 128;
 constexpr int kMaxSR = 512;
 constexpr int kMaxKeys = 3071;
 constexpr int kInlineRowsMax = 1024;  // rows a kernel clusters on its own
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
+// A bounded wait gives up after this many nanoseconds of %globaltimer (the
+// default of the launch argument that carries the limit; 0 makes a wait give
+// up at its first poll that finds the phase incomplete).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kWaitSleepNs = 20000;  // longest sleep of one poll
 
@@ -136,13 +138,16 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Wait for the phase with the given parity to complete; gives up after
-// kWaitLimitNs and returns false (the caller records LORA_DEV_ERR_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// limit_ns nanoseconds (at the first incomplete poll when limit_ns is 0) and
+// returns false (the caller records LORA_DEV_ERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (limit_ns == 0) return false;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -9,11 +9,16 @@
 // such a caller cannot provide.  This entry point takes that scratch from a
 // fixed array that lives in the library itself.
 //
-// The array is a file-scope __device__ variable of kNoAllocScratchBytes bytes:
-// every GPU on which the library is loaded holds it until the process exits.
-// Its address is looked up once per device with cudaGetSymbolAddress, by the
-// first call on that device, with that device current; that first call should
-// therefore come before any stream capture.  Every call shares the one array,
+// The array is a file-scope __device__ variable of kNoAllocScratchBytes bytes.
+// This file is its own CUDA module, and the runtime loads modules lazily by
+// default (CUDA_MODULE_LOADING=LAZY): the driver reserves the array on a
+// device when the first call on that device looks its address up with
+// cudaGetSymbolAddress (with that device current), not when the library is
+// loaded.  From then on the device holds it until the process exits.  So a
+// caller makes one warm-up call on every device it uses before its memory
+// budget is fixed and before any stream capture; after that no call reserves
+// anything.  The address is cached per device; it is stale after a
+// cudaDeviceReset of that device.  Every call shares the one array,
 // so calls that overlap on the GPU (for example on two streams) race on it;
 // serialize them.  The array keeps whatever the last call left in it; the
 // kernels that use it overwrite every entry they read (the clustering writes
@@ -36,13 +41,19 @@ void* g_scratch_ptr[kMaxDevices] = {};
 // Device address of the scratch array on the current device (looked up once).
 int scratch_for_current_device(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
     return LORA_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      // (e.g. out of memory while the module loads): clear the runtime's last
+      // error, so that a later, unrelated launch check does not report it
+      cudaGetLastError();
       return LORA_ERR_CUDA;
+    }
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

@@ -18,8 +18,9 @@
 //     the chunk's B rows (both 128-byte swizzled tiles) and scale * d is folded
 //     into out in place, one rounding; the next item's B chunk and out
 //     segments stream into shared memory while the current one computes.
-// Every wait on an mbarrier is bounded; on a time-out the CTA records
-// LORA_DEV_ERR_TIMEOUT, skips its writes and still releases its TMEM.
+// Every wait on an mbarrier is bounded (the limit is a launch argument); on a
+// time-out the CTA records LORA_DEV_ERR_TIMEOUT, skips its writes, lets its
+// MMA thread's issued MMAs finish and still releases its TMEM.
 #pragma once
 
 #include "bgmv.cuh"
@@ -104,6 +105,7 @@ struct SgmvArgs {
   int chunk0[kMaxSlices + 1];  // first expand chunk of each slice; chunk0[S] = chunks total
   int add_inputs;
   uint32_t* err;
+  uint64_t wait_ns;  // limit of every bounded wait (kWaitLimitNs unless a test lowers it)
 };
 
 __device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gsrc, bool valid) {
@@ -131,7 +133,8 @@ __global__ void __launch_bounds__(kShrinkThreads)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ SlotView v;
   __shared__ uint32_t taddr_s;
-  __shared__ __align__(8) uint64_t full_bar[kShrinkStages], empty_bar[kShrinkStages], done_bar;
+  __shared__ __align__(8) uint64_t full_bar[kShrinkStages], empty_bar[kShrinkStages], done_bar,
+      drain_bar;
   __shared__ const __nv_bfloat16* xrow_s[kTileRows];
   __shared__ const __nv_bfloat16* arow_s[kSgmvMaxSR];
   cudaGridDependencySynchronize();
@@ -145,6 +148,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
       mbar_init(&empty_bar[s], 1);                // the MMA commit
     }
     mbar_init(&done_bar, 1);
+    mbar_init(&drain_bar, 1);  // the MMA thread's last commit after a time-out
     fence_barrier_init();
   }
   if (warp == 0) tc::tmem_alloc(&taddr_s, kSgmvMaxSR);  // room for any N
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
   int kbg = 0;  // k-blocks streamed through the stage ring so far
   int nd = 0;   // items committed to done_bar so far
   bool ok = true;
+  bool issued = false;  // (MMA thread) some MMA was issued
   // persistent: items (tile, split), tile-major
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int tile_id = item / ks, split = item - tile_id * ks;
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
       const int c = tid & 7;
       for (int kb = 0; kb < nkb; ++kb) {
         const int g = kbg + kb, s = g % kShrinkStages, k = g / kShrinkStages;
-        if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1)) {
+        if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
       const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, N);
       for (int kb = 0; kb < nkb; ++kb) {
         const int g = kbg + kb, s = g % kShrinkStages, k = g / kShrinkStages;
-        if (!mbar_wait_bounded(&full_bar[s], k & 1)) {
+        if (!mbar_wait_bounded(&full_bar[s], k & 1, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -229,6 +234,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
         for (int q = 0; q < 4; ++q)
           tc::mma_bf16(taddr, tc::sw128_desc(xa + q * 32), tc::sw128_desc(aa + q * 32), idesc,
                        (kb > 0 || q > 0) ? 1u : 0u);
+        issued = true;
         tc::mma_commit(&empty_bar[s]);  // the stage is free once these MMAs are done
       }
       tc::mma_commit(&done_bar);
@@ -238,7 +244,10 @@ __global__ void __launch_bounds__(kShrinkThreads)
     // warps 0-3: TMEM lane quarter q = tile rows 32q.., columns [0, SRa) ->
     // plane `split` of hbuf, row pos0 + r
     if (warp < 4) {
-      if (!mbar_wait_bounded(&done_bar, nd & 1)) ok = false;
+      // (uniform over the warp before the warp-collective TMEM loads: a lane
+      // may have given up in the producer loop, or see the phase later)
+      const bool done = ok && mbar_wait_bounded(&done_bar, nd & 1, a.wait_ns);
+      ok = __all_sync(0xffffffffu, done);
       tc::fence_after_sync();
       const int r = warp * 32 + lane;
       float* dst = a.hbuf + (size_t)split * a.plane + (size_t)(tile.pos0 + r) * a.hs;
@@ -260,6 +269,13 @@ __global__ void __launch_bounds__(kShrinkThreads)
   }
   if (warp < kShrinkMmaWarp) asm volatile("cp.async.wait_all;" ::: "memory");
   if (!ok) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
+  // After a time-out the MMAs issued last may still be running: one more
+  // commit tracks every earlier MMA of the thread, and TMEM is freed only
+  // after it has arrived.
+  if (!__syncthreads_and(ok) && warp == kShrinkMmaWarp && lane == 0 && issued) {
+    tc::mma_commit(&drain_bar);
+    mbar_wait_bounded(&drain_bar, 0, kWaitLimitNs);
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(taddr, kSgmvMaxSR);
@@ -311,7 +327,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   __shared__ SgmvTile tiles_s[kExpandMaxTiles];
   __shared__ int orow_map[kExpandMaxTiles][kTileRows];  // out row of each tile row
   __shared__ uint32_t taddr_s;
-  __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS], accf_bar[2], acce_bar[2], h_bar;
+  __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS], accf_bar[2], acce_bar[2], h_bar,
+      drain_bar;
   cudaGridDependencySynchronize();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int total = *a.n_tiles * n_chunks;
@@ -354,6 +371,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       mbar_init(&acce_bar[c], kExpandEpilogue / 32);  // the epilogue warps
     }
     mbar_init(&h_bar, kExpandEpilogue);  // every epilogue thread
+    mbar_init(&drain_bar, 1);            // the MMA thread's last commit after a time-out
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tc::tmem_alloc(&taddr_s, 2 * kExpandCols);  // two accumulators
@@ -382,6 +400,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     return it;
   };
   bool ok = true;
+  int na_issued = 0;  // (MMA thread) items whose MMAs were issued
 
   if (warp < kMmaWarp) {
     // ---------------------------------------------------------- producer --
@@ -390,7 +409,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       const int i = w - w0, s = i % NS, k = i / NS;
       const Item it = item_of(w);
       // the epilogue released this stage's previous use
-      if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1)) {
+      if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1, a.wait_ns)) {
         ok = false;
         break;
       }
@@ -433,14 +452,14 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
           ++hv;
           h_lt = it.lt;
           h_ja = it.ja;
-          if (!mbar_wait_bounded(&h_bar, hv & 1)) {
+          if (!mbar_wait_bounded(&h_bar, hv & 1, a.wait_ns)) {
             ok = false;
             break;
           }
         }
         const int acc = na & 1, u = na >> 1;
-        if (!mbar_wait_bounded(&full_bar[s], k & 1) ||
-            (u > 0 && !mbar_wait_bounded(&acce_bar[acc], (u - 1) & 1))) {
+        if (!mbar_wait_bounded(&full_bar[s], k & 1, a.wait_ns) ||
+            (u > 0 && !mbar_wait_bounded(&acce_bar[acc], (u - 1) & 1, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -461,6 +480,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         }
         tc::mma_commit(&accf_bar[acc]);
         ++na;
+        na_issued = na;
       }
     }
     __syncwarp();
@@ -476,7 +496,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       const Item it = item_of(w);
       if (it.ja < 0 || it.nc <= 0) {
         // nothing to compute: release the stage once its (empty) fill completed
-        if (!mbar_wait_bounded(&full_bar[s], k & 1)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], k & 1, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -518,7 +538,11 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         mbar_arrive(&h_bar);
       }
       const int acc = na & 1, u = na >> 1;
-      if (!mbar_wait_bounded(&accf_bar[acc], u & 1) || !mbar_wait_bounded(&full_bar[s], k & 1)) {
+      // (every lane of the warp takes the same branch: the TMEM loads below
+      // are warp-collective)
+      const bool ready = mbar_wait_bounded(&accf_bar[acc], u & 1, a.wait_ns) &&
+                         mbar_wait_bounded(&full_bar[s], k & 1, a.wait_ns);
+      if (!__all_sync(0xffffffffu, ready)) {
         ok = false;
         break;
       }
@@ -568,6 +592,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     __syncwarp();
   }
   if (!ok) set_error(a.err, LORA_DEV_ERR_TIMEOUT);
+  // After a time-out the MMAs issued last may still be running: one more
+  // commit tracks every earlier MMA of the thread, and TMEM is freed only
+  // after it has arrived.
+  if (!__syncthreads_and(ok) && warp == kMmaWarp && lane == 0 && na_issued > 0) {
+    tc::mma_commit(&drain_bar);
+    mbar_wait_bounded(&drain_bar, 0, kWaitLimitNs);
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) tc::tmem_dealloc(taddr, 2 * kExpandCols);

@@ -224,11 +224,35 @@ class MoeCase:
     B_banks: list = field(default_factory=list)
 
 
+def duplicate_experts(topk: np.ndarray, frac: float, seed: int) -> np.ndarray:
+    """A copy of ``topk`` [T, top_k] in which a fraction ``frac`` of the tokens
+    repeat experts: in each such token, between 1 and top_k - 1 of its slots
+    (chosen at random) take the id of another slot of the same token, so that
+    one token reaches one expert through two or more slots.  Nothing in the
+    pages makes a token's experts distinct, so the path has to accept this.
+    Drawn from its own generator: the default workloads do not change."""
+    out = np.array(topk, dtype=np.int32, copy=True)
+    T, k = out.shape
+    if k < 2 or frac <= 0:
+        return out
+    rng = np.random.default_rng(seed + 50_000)
+    for t in np.flatnonzero(rng.random(T) < frac):
+        n_dup = int(rng.integers(1, k))
+        slots = rng.permutation(k)
+        src = slots[n_dup:]
+        for j in slots[:n_dup]:
+            out[t, j] = out[t, int(rng.choice(src))]
+    return out
+
+
 def moe_case(shared_a: bool = False, seed: int = 1238, T: int = 2048, top_k: int = 8,
              E: int = 64, H: int = 2048, I: int = 768, rank: int = 16, L: int = 8,
-             scale: float = 2.0, p_none: float = 0.2, x_scaled: bool = False) -> MoeCase:
+             scale: float = 2.0, p_none: float = 0.2, x_scaled: bool = False,
+             dup_frac: float = 0.0) -> MoeCase:
     """MoE FC1 LoRA delta: T tokens, top_k distinct experts of E per token (uniform),
-    lora_ids uniform over L with p_none of -1, A ~ N(0,1)/sqrt(H), B ~ N(0,1)/sqrt(rank)."""
+    lora_ids uniform over L with p_none of -1, A ~ N(0,1)/sqrt(H), B ~ N(0,1)/sqrt(rank).
+    With ``dup_frac`` > 0, that fraction of the tokens repeat experts
+    (``duplicate_experts``)."""
     rng = np.random.default_rng(seed + (1 if shared_a else 0) * 7)
     topk = np.stack([rng.permutation(E)[:top_k] for _ in range(T)]).astype(np.int32)
     lora = rng.integers(0, L, size=T).astype(np.int32)
@@ -240,6 +264,8 @@ def moe_case(shared_a: bool = False, seed: int = 1238, T: int = 2048, top_k: int
         B = [_normal_bf16(rng, (E, L, 2 * I, rank), 1.0 / np.sqrt(rank))]
     else:
         B = [_normal_bf16(rng, (E, L, I, rank), 1.0 / np.sqrt(rank)) for _ in range(2)]
+    if dup_frac > 0:
+        topk = duplicate_experts(topk, dup_frac, seed)
     return MoeCase(name=("MoE FC1 shared-A/fused-B" if shared_a else "MoE FC1 regular")
                    + f" T={T} top_k={top_k} E={E} H={H} I={I} rank={rank}",
                    seed=seed, T=T, top_k=top_k, E=E, H=H, I=I, rank=rank, L=L, scale=scale,
@@ -306,12 +332,14 @@ class MoeDownCase:
 
 def moe_w2_case(seed: int = 1240, T: int = 2048, top_k: int = 8, E: int = 64, H: int = 2048,
                 I: int = 768, rank: int = 16, L: int = 8, scale: float = 2.0,
-                p_none: float = 0.2) -> MoeDownCase:
+                p_none: float = 0.2, dup_frac: float = 0.0) -> MoeDownCase:
     """The FC1 workload's routing and shapes seen from the down projection:
     top_k distinct experts of E per token (uniform), lora_ids uniform over L
     with p_none of -1; x ~ N(0, 1) (reading: the activation has no fan-in),
     A ~ N(0,1)/sqrt(I), B ~ N(0,1)/sqrt(rank); routing weights a softmax of
-    N(0, 1) logits over the token's top_k (reading: the pages fix no router)."""
+    N(0, 1) logits over the token's top_k (reading: the pages fix no router).
+    With ``dup_frac`` > 0, that fraction of the tokens repeat experts
+    (``duplicate_experts``)."""
     rng = np.random.default_rng(seed + 40_000)
     topk = np.stack([rng.permutation(E)[:top_k] for _ in range(T)]).astype(np.int32)
     lora = rng.integers(0, L, size=T).astype(np.int32)
@@ -323,6 +351,8 @@ def moe_w2_case(seed: int = 1240, T: int = 2048, top_k: int = 8, E: int = 64, H:
     A = [_normal_bf16(rng, (E, L, rank, I), 1.0 / np.sqrt(I))]
     B = [_normal_bf16(rng, (E, L, H, rank), 1.0 / np.sqrt(rank))]
     y0 = _normal_bf16(rng, (T, top_k, H))
+    if dup_frac > 0:
+        topk = duplicate_experts(topk, dup_frac, seed)
     return MoeDownCase(name=f"MoE w2 T={T} top_k={top_k} E={E} H={H} I={I} rank={rank}",
                        seed=seed, T=T, top_k=top_k, E=E, H=H, I=I, rank=rank, L=L,
                        scale=scale, x=x, y0=y0, topk_ids=topk, lora_ids=lora, topk_weights=w,

@@ -53,6 +53,18 @@ def test_host_only_calls(library):
     assert ld.lora_moe_workspace_size(2048, 8, 64, 8, 16, False) >= 2048 * 8 * 4
 
 
+def test_wait_limit_setter_is_process_wide_and_returns_the_previous_value(library):
+    """lora_set_wait_limit_ns: default 2 s; the setter returns the previous limit."""
+    import lora_delta_gb300 as ld
+    prev = ld.lora_set_wait_limit_ns(12345)
+    try:
+        assert prev == ld.WAIT_LIMIT_DEFAULT_NS
+        assert ld.lora_set_wait_limit_ns(0) == 12345
+    finally:
+        ld.lora_set_wait_limit_ns(prev)
+    assert ld.lora_set_wait_limit_ns(prev) == prev
+
+
 def test_host_validation_without_a_gpu(library):
     """Argument errors are caught on the host before anything is launched."""
     import lora_delta_gb300 as ld

@@ -2,7 +2,7 @@
 
 Each case copies ``oracle/lora_oracle.c``, plants one plausible mistake (a
 dropped term, a transposed operand, a wrong index or offset, a missing scale, a
-wrong tie rule, an unstable sort, non-zero padding, swapped MoE slices, a wrong
+wrong tie rule, an unstable sort, an overwrite that still adds or drops the scale, non-zero padding, swapped MoE slices, a wrong
 adapter stride, a per-token input row for the down projection, a dropped routing
 weight, a non-local expert treated as local, a disabled adapter applied), compiles the copy into a temporary library and runs the pin
 suite against it in a subprocess.  The pins must fail for every mutant.
@@ -31,6 +31,16 @@ MUTANTS = {
         "                    }\n                }\n            }\n            off += widths[j];",
         "                    }\n                }\n            }\n            off += widths[0];"),
     "missing_scale": ("                        float v = scale * d;", "                        float v = d;"),
+    "expand_overwrite_adds": (
+        "                    uint16_t *o = out + (size_t)i * ld_out + off + c;\n"
+        "                    *o = oracle_f32_to_bf16(add_inputs ? oracle_bf16_to_f32(*o) + v : v);",
+        "                    uint16_t *o = out + (size_t)i * ld_out + off + c;\n"
+        "                    *o = oracle_f32_to_bf16(oracle_bf16_to_f32(*o) + v);"),
+    "expand_overwrite_unscaled": (
+        "                    uint16_t *o = out + (size_t)i * ld_out + off + c;\n"
+        "                    *o = oracle_f32_to_bf16(add_inputs ? oracle_bf16_to_f32(*o) + v : v);",
+        "                    uint16_t *o = out + (size_t)i * ld_out + off + c;\n"
+        "                    *o = oracle_f32_to_bf16(add_inputs ? oracle_bf16_to_f32(*o) + v : d);"),
     "ties_away_from_zero": ("(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
     "unstable_segments": (
         "        for (int i = 0; i < n; ++i)\n            if (seq_slot[i] == s)",

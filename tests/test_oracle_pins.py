@@ -328,6 +328,41 @@ def test_add_inputs_false_overwrites_routed_rows(oracle):
     assert np.array_equal(o[~routed], case.out0[~routed])
 
 
+def test_expand_overwrite_from_poisoned_out_equals_add_from_zero(oracle):
+    """'punica_base.py', add_expand add_inputs flag, on the two-step form: with
+    add_inputs False the expand sets the routed columns to RN(scale * h.B), so a
+    poisoned starting out (huge values, infinities, NaN patterns) must give the
+    bits that add_inputs True gives from +0 (RN(+0 + v) = RN(v)); rows without a
+    slot keep their poison bit for bit, and columns outside the slices too."""
+    case = inputs.linear_case(103, n=41, k_in=96, widths=(40, 24), max_loras=3, max_rank=8,
+                              ranks=[8, 5, 8], alpha=8.0, p_none=0.25, offset_start=8,
+                              ld_out=80)
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, 3, 8)
+    h, _ = oracle.shrink(case.x, case.seq_slot, pool, None)
+    rng = np.random.default_rng(5)
+    poison = rng.choice(np.array([0x7F7F, 0xFF7F, 0x7F80, 0xFF80, 0x7FC0, 0x4480],
+                                 dtype=np.uint16), size=case.out0.shape)
+    o = poison.copy()
+    oracle.expand(o, h, case.seq_slot, pool, pool.scale_table, offset_start=8,
+                  add_inputs=False)
+    z = np.zeros_like(poison)
+    oracle.expand(z, h, case.seq_slot, pool, pool.scale_table, offset_start=8,
+                  add_inputs=True)
+    routed = case.seq_slot >= 0
+    cols = slice(8, 8 + 64)
+    assert np.array_equal(o[routed][:, cols], z[routed][:, cols])
+    assert np.array_equal(o[~routed], poison[~routed])
+    assert np.array_equal(o[:, :8], poison[:, :8]) and np.array_equal(o[:, 72:], poison[:, 72:])
+    # and the overwritten values are the correctly rounded fp64 expand within one
+    # bf16 step (fp32 accumulation of R = 8 terms)
+    B = [f32(b).astype(np.float64) for b in pool.B]
+    for i in np.flatnonzero(routed):
+        s = case.seq_slot[i]
+        ref = np.concatenate([float(pool.scale_table[s]) * (h[j, i].astype(np.float64) @ B[j][s].T)
+                              for j in range(2)])
+        assert bf16_ulp_distance(o[i, cols], oracle.f64_to_bf16(ref)).max() <= 1
+
+
 def test_bad_slot_sets_error_and_skips_row(oracle):
     """Reading (no page fixes it): a slot >= max_loras applies no delta and sets
     error bit 1 instead of trapping."""
@@ -388,6 +423,39 @@ def test_moe_matches_fp64_formula_per_pair(oracle):
         o32, _ = oracle.moe_fc1(c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I,
                                 c.rank, c.scale, shared, c.L)
         assert bf16_ulp_distance(o32, want).max() <= 1
+
+
+def test_moe_duplicate_experts_follow_the_formula_per_slot(oracle):
+    """'bgmv_moe_gemm1_lora_delta', topk_ids: a token may name one expert in two
+    or more slots.  Each slot is still its own (token, slot) row of the formula:
+    the rows of the repeated expert are equal bit for bit, and each equals the
+    correctly rounded fp64 formula (fp64 oracle) and a bf16 step of it (fp32)."""
+    for shared in (False, True):
+        c = _moe_small(shared, seed=23, dup_frac=0.6)
+        dup_rows = [(t, j1, j2) for t in range(c.T) for j1 in range(c.top_k)
+                    for j2 in range(j1 + 1, c.top_k)
+                    if c.topk_ids[t, j1] == c.topk_ids[t, j2] and c.lora_ids[t] >= 0]
+        assert dup_rows
+        o64, err = oracle.moe_fc1(c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I,
+                                  c.rank, c.scale, shared, c.L, acc64=True)
+        o32, err32 = oracle.moe_fc1(c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.I,
+                                    c.rank, c.scale, shared, c.L)
+        assert err == err32 == 0
+        for t, j1, j2 in dup_rows:
+            assert np.array_equal(o32[t, j1], o32[t, j2])
+            assert np.array_equal(o64[t, j1], o64[t, j2])
+        xf = f32(c.x).astype(np.float64)
+        for t, j1, _ in dup_rows:
+            e, l = int(c.topk_ids[t, j1]), int(c.lora_ids[t])
+            hs = [f32(a[e, l]).astype(np.float64) @ xf[t] for a in c.A_banks]
+            if shared:
+                d = c.scale * (f32(c.B_banks[0][e, l]).astype(np.float64) @ hs[0])
+            else:
+                d = c.scale * np.concatenate([f32(c.B_banks[i][e, l]).astype(np.float64) @ hs[i]
+                                              for i in range(2)])
+            want = np.array([rne_bf16(Fraction(float(v))) for v in d], dtype=np.uint16)
+            assert np.array_equal(o64[t, j1], want)
+            assert bf16_ulp_distance(o32[t, j1], want).max() <= 1
 
 
 def test_moe_shared_a_equals_regular_with_equal_a(oracle):
