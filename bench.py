@@ -45,9 +45,10 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-# DRAM bytes (read + write) of one launch of the decode step's kernel, from the
-# ncu capture summarised in profiles/delta_cluster_decode_qkv_n64.md, with the
-# hash of the sources it was taken on: reported only while they are unchanged.
+# DRAM bytes (read + write) of one launch of the decode step's kernel, from one
+# ncu capture of that launch (dram__bytes_read.sum + dram__bytes_write.sum),
+# with the hash of the sources it was taken on: reported only while they are
+# unchanged, null otherwise.
 DECODE_TRAFFIC = {"bytes": 10652160, "sources_sha256_16": "ac08fb373e1f02b3"}
 DECODE_SOURCES = ("lora_delta_gb300/csrc/bgmv.cuh", "lora_delta_gb300/csrc/common.cuh",
                   "lora_delta_gb300/csrc/api.cu")
@@ -198,6 +199,14 @@ def make_copies(ld, di, case, copies, device):
     return out
 
 
+def decode_config(case, world):
+    """The workload of one step (the same dict on both arms)."""
+    return {"workload": case.name, "rows_per_step": case.n, "k_in": case.k_in,
+            "output_slices": list(case.widths), "max_loras": case.max_loras,
+            "max_rank": case.max_rank, "unrouted_rows": int((case.seq_slot < 0).sum()),
+            "parallelism": f"dp{world} (rows sharded, pool replicated)"}
+
+
 def run_ours(args, rank, world):
     import numpy as np
     import torch
@@ -296,13 +305,10 @@ def run_ours(args, rank, world):
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init adapters)",
-        "config": {"workload": case.name, "rows_per_step": n, "k_in": case.k_in,
-                   "output_slices": list(case.widths), "max_loras": case.max_loras,
-                   "max_rank": case.max_rank, "unrouted_rows": int((case.seq_slot < 0).sum()),
-                   "l2": f"{copies} rotating copies of pool/x/out/seq_slot "
-                         f"({copies * per_copy / 2**20:.0f} MiB > 2x L2)",
-                   "timing": "one CUDA graph of K steps, CUDA events on the launching stream",
-                   "parallelism": f"dp{world} (rows sharded, pool replicated)"},
+        "config": decode_config(case, world),
+        "l2": f"{copies} rotating copies of pool/x/out/seq_slot "
+              f"({copies * per_copy / 2**20:.0f} MiB > 2x L2)",
+        "timing": "one CUDA graph of K steps, CUDA events on the launching stream",
         "roofline": roofline,
         "eager_ms_per_step": round(eager_ms, 6),
         "e2e": e2e,
@@ -437,24 +443,37 @@ def cpu_baseline(case, budget_s: float = 10.0):
                       f"({dt:.1f} s, OpenMP over rows, {cores} threads)"}
 
 
-def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src, only=None, reps=5,
-                    warm=2):
-    """The other workloads of the path, each timed on its own (not the headline)."""
+def rotation(set_bytes: int) -> int:
+    """Copies of a workload's buffers whose total passes twice the L2 (at least 1)."""
+    import math
+    return max(1, math.ceil(2.2 * l2_bytes() / max(1, set_bytes)))
+
+
+def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src, only=None, reps=20,
+                    warm=3):
+    """The other workloads of the path, each timed on its own (not the headline).
+
+    Each is timed with CUDA events over ``reps`` calls on one stream after
+    ``warm`` warm-up calls.  Where one call's buffers are smaller than twice the
+    L2, the calls rotate over enough independent copies of all of them (inputs,
+    adapters, outputs) that the total passes twice the L2, so the bytes come from
+    HBM; the copy count goes into each result."""
     import numpy as np
     import torch
     res = {}
     stream = torch.cuda.Stream(device)
-    rep_default, warm_default = reps, warm
+    rep_default, warm_default = max(20, reps), max(3, warm)
 
-    def timed(fn, reps=rep_default, warm=warm_default):
+    def timed(fns, reps=rep_default, warm=warm_default):
+        fns = fns if isinstance(fns, (list, tuple)) else [fns]
         with torch.cuda.stream(stream):
-            for _ in range(warm):
-                fn()
+            for i in range(max(warm, len(fns))):
+                fns[i % len(fns)]()
             torch.cuda.synchronize(device)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for _ in range(reps):
-                fn()
+            for i in range(reps):
+                fns[i % len(fns)]()
             e1.record(stream)
         torch.cuda.synchronize(device)
         return e0.elapsed_time(e1) / reps
@@ -477,11 +496,12 @@ def other_workloads(ld, di, inputs, device, hbm_peak, bf16_peak, peak_src, only=
 def _prefill(ld, di, inputs, device, hbm_peak, bf16_peak, timed, res):
     import torch
     case = inputs.prefill_gate_up_case()
-    d = di.linear_to_device(case, device)
+    ab, fl = algorithmic_bytes(case), algorithmic_flops(case)
+    ds = [di.linear_to_device(case, device) for _ in range(rotation(ab))]
     ws = torch.empty(ld.lora_workspace_size(case.n, len(case.widths), case.max_rank,
                                          case.max_loras), dtype=torch.uint8, device=device)
-    ms = timed(lambda: ld.lora_delta_fused(d.out0, d.x, d.seq_slot, d.pool, workspace=ws))
-    ab, fl = algorithmic_bytes(case), algorithmic_flops(case)
+    ms = timed([lambda d=d: ld.lora_delta_fused(d.out0, d.x, d.seq_slot, d.pool, workspace=ws)
+                for d in ds])
     gbs, tfs = ab / (ms / 1e3) / 1e9, fl / (ms / 1e3) / 1e12
     attain = min(bf16_peak, fl / ab * hbm_peak / 1e3)
     res["prefill_gate_up"] = {"rows_per_s": round(case.n / (ms / 1e3), 1), "ms": round(ms, 4),
@@ -490,8 +510,8 @@ def _prefill(ld, di, inputs, device, hbm_peak, bf16_peak, timed, res):
                               "tensor_frac": round(tfs / bf16_peak, 5),
                               "attainable_TFLOP_per_s": round(attain, 1),
                               "roofline_frac": round(tfs / attain, 4),
-                              "launches_per_call": 5}
-    del d, ws
+                              "launches_per_call": 5, "copies": len(ds)}
+    del ds, ws
     torch.cuda.empty_cache()
 
 
@@ -499,17 +519,19 @@ def _skewed(ld, di, inputs, device, hbm_peak, timed, res):
     import torch
     # skewed many-adapter decode: both projections per step
     c1, c2 = inputs.skewed_case(0), inputs.skewed_case(1)
-    d1, d2 = di.linear_to_device(c1, device), di.linear_to_device(c2, device)
+    ab = algorithmic_bytes(c1) + algorithmic_bytes(c2)
+    ds = [(di.linear_to_device(c1, device), di.linear_to_device(c2, device))
+          for _ in range(rotation(ab))]
     ws = torch.empty(max(ld.lora_workspace_size(c.n, 1, c.max_rank, c.max_loras) for c in (c1, c2)),
                      dtype=torch.uint8, device=device)
-    ms = timed(lambda: (ld.lora_delta_fused(d1.out0, d1.x, d1.seq_slot, d1.pool, workspace=ws),
-                        ld.lora_delta_fused(d2.out0, d2.x, d2.seq_slot, d2.pool, workspace=ws)))
-    ab = algorithmic_bytes(c1) + algorithmic_bytes(c2)
+    ms = timed([lambda d1=d1, d2=d2: (
+        ld.lora_delta_fused(d1.out0, d1.x, d1.seq_slot, d1.pool, workspace=ws),
+        ld.lora_delta_fused(d2.out0, d2.x, d2.seq_slot, d2.pool, workspace=ws)) for d1, d2 in ds])
     res["skewed_decode"] = {"rows_per_s": round(c1.n / (ms / 1e3), 1), "ms": round(ms, 4),
                             "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
                             "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4),
-                            "launches_per_call": 10}
-    del d1, d2, ws
+                            "launches_per_call": 10, "copies": len(ds)}
+    del ds, ws
     torch.cuda.empty_cache()
 
 
@@ -518,51 +540,58 @@ def _fold(ld, di, inputs, device, hbm_peak, timed, res):
     # expert-sorted MoE fold (w13): 2048 tokens x top-8 of 64 experts, one
     # adapter per expert (10% unadapted), rows grouped by device offsets
     case, offsets = inputs.expert_sorted_case()
-    d = di.linear_to_device(case, device)
+    ab = algorithmic_bytes(case)
+    ds = [di.linear_to_device(case, device) for _ in range(rotation(ab))]
     off = torch.from_numpy(offsets).to(device)
     ws = torch.empty(ld.lora_workspace_size(case.n, 1, case.max_rank, case.max_loras),
                      dtype=torch.uint8, device=device)
-    ms = timed(lambda: ld.lora_delta_segmented(d.out0, d.x, off, d.pool, workspace=ws))
-    ab = algorithmic_bytes(case)
+    ms = timed([lambda d=d: ld.lora_delta_segmented(d.out0, d.x, off, d.pool, workspace=ws)
+                for d in ds])
     gbs = ab / (ms / 1e3) / 1e9
     res["moe_expert_fold_w13"] = {"rows_per_s": round(case.n / (ms / 1e3), 1), "ms": round(ms, 4),
                                   "GB_per_s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
-                                  "launches_per_call": 5}
-    del d, ws
+                                  "launches_per_call": 5, "copies": len(ds)}
+    del ds, ws
     torch.cuda.empty_cache()
 
 
-def _moe(ld, di, inputs, device, hbm_peak, timed, res):
+def _moe_keys(case):
     import numpy as np
+    valid = case.lora_ids >= 0
+    return valid, {(int(l), int(e)) for t in np.flatnonzero(valid)
+                   for l, e in zip([case.lora_ids[t]] * case.top_k, case.topk_ids[t])}
+
+
+def _moe(ld, di, inputs, device, hbm_peak, timed, res):
     import torch
     # MoE FC1 (regular and shared-A / fused-B)
     for shared in (False, True):
         mc = inputs.moe_case(shared_a=shared)
-        dm = di.moe_to_device(mc, device)
-        out = torch.empty(mc.T, mc.top_k, 2 * mc.I, dtype=torch.bfloat16, device=device)
-        ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L, mc.rank, shared),
-                         dtype=torch.uint8, device=device)
-        ms = timed(lambda: ld.lora_moe_fc1_delta(out, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b,
-                                                 dm.stride_b, shared, dm.topk_ids, dm.lora_ids,
-                                                 mc.E, mc.I, mc.rank, mc.L, mc.scale,
-                                                 workspace=ws))
-        valid = mc.lora_ids >= 0
+        valid, keys = _moe_keys(mc)
         pairs = int(valid.sum()) * mc.top_k
-        keys = {(int(l), int(e)) for t in np.flatnonzero(valid) for l, e in
-                zip([mc.lora_ids[t]] * mc.top_k, mc.topk_ids[t])}
         n_a = 1 if shared else 2
         bank = len(keys) * (n_a * mc.rank * mc.H * 2 + 2 * mc.I * mc.rank * 2)
         ab = bank + mc.T * mc.top_k * 2 * mc.I * 2 + int(valid.sum()) * mc.H * 2
+        sets = []
+        for _ in range(rotation(ab)):
+            dm = di.moe_to_device(mc, device)
+            out = torch.empty(mc.T, mc.top_k, 2 * mc.I, dtype=torch.bfloat16, device=device)
+            sets.append((dm, out))
+        ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L, mc.rank, shared),
+                         dtype=torch.uint8, device=device)
+        ms = timed([lambda dm=dm, out=out: ld.lora_moe_fc1_delta(
+            out, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b, shared, dm.topk_ids,
+            dm.lora_ids, mc.E, mc.I, mc.rank, mc.L, mc.scale, workspace=ws) for dm, out in sets])
         res["moe_fc1_" + ("shared" if shared else "regular")] = {
             "pairs_per_s": round(mc.T * mc.top_k / (ms / 1e3), 1), "ms": round(ms, 4),
             "routed_pairs": pairs, "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
-            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 3}
-        del dm, out, ws
+            "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4), "launches_per_call": 3,
+            "copies": len(sets)}
+        del sets, ws
         torch.cuda.empty_cache()
 
 
 def _moe_inplace(ld, di, inputs, device, hbm_peak, timed, res):
-    import numpy as np
     import torch
     # in-place MoE deltas on either side of the activation, FC1's routing:
     # w13 (gate/up, regular banks) into intermediate_cache1, w2 (down, with
@@ -570,39 +599,41 @@ def _moe_inplace(ld, di, inputs, device, hbm_peak, timed, res):
     mc = inputs.moe_case()
     c2 = inputs.moe_w2_case()
     for name, case in (("moe_w13_inplace", mc), ("moe_w2_inplace_weighted", c2)):
-        dm = di.moe_to_device(case, device)
-        valid = case.lora_ids >= 0
+        valid, keys = _moe_keys(case)
         pairs = int(valid.sum()) * case.top_k
-        keys = {(int(l), int(e)) for t in np.flatnonzero(valid) for l, e in
-                zip([case.lora_ids[t]] * case.top_k, case.topk_ids[t])}
         if name == "moe_w13_inplace":
-            y = di.bf16(inputs.moe_y0(mc.seed, (mc.T, mc.top_k, 2 * mc.I)), device)
-            ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L, mc.rank,
-                                                        False), dtype=torch.uint8, device=device)
-            fn = lambda: ld.lora_moe_w13_delta(y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b,
-                                               dm.stride_b, False, dm.topk_ids, dm.lora_ids,
-                                               mc.E, mc.I, mc.rank, mc.L, mc.scale, workspace=ws)
             bank = len(keys) * (2 * mc.rank * mc.H * 2 + 2 * mc.I * mc.rank * 2)
             ab = bank + pairs * 2 * mc.I * 2 * 2 + int(valid.sum()) * mc.H * 2
+            y0 = inputs.moe_y0(mc.seed, (mc.T, mc.top_k, 2 * mc.I))
+            ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, mc.E, mc.L, mc.rank,
+                                                        False), dtype=torch.uint8, device=device)
+            fns = []
+            for _ in range(rotation(ab)):
+                dm, y = di.moe_to_device(case, device), di.bf16(y0, device)
+                fns.append(lambda dm=dm, y=y: ld.lora_moe_w13_delta(
+                    y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b, False, dm.topk_ids,
+                    dm.lora_ids, mc.E, mc.I, mc.rank, mc.L, mc.scale, workspace=ws))
         else:
-            y = di.bf16(case.y0, device)
-            wts = torch.from_numpy(case.topk_weights).to(device)
+            bank = len(keys) * (case.rank * case.I * 2 + case.H * case.rank * 2)
+            ab = bank + pairs * case.H * 2 * 2 + pairs * case.I * 2
             ws = torch.empty(ld.lora_moe_workspace_size(case.T, case.top_k, case.E, case.L,
                                                         case.rank, True),
                              dtype=torch.uint8, device=device)
-            fn = lambda: ld.lora_moe_w2_delta(y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b,
-                                              dm.stride_b, dm.topk_ids, dm.lora_ids, case.E,
-                                              case.H, case.rank, case.L, case.scale,
-                                              topk_weights=wts, workspace=ws)
-            bank = len(keys) * (case.rank * case.I * 2 + case.H * case.rank * 2)
-            ab = bank + pairs * case.H * 2 * 2 + pairs * case.I * 2
-        ms = timed(fn)
+            fns = []
+            for _ in range(rotation(ab)):
+                dm, y = di.moe_to_device(case, device), di.bf16(case.y0, device)
+                wts = torch.from_numpy(case.topk_weights).to(device)
+                fns.append(lambda dm=dm, y=y, wts=wts: ld.lora_moe_w2_delta(
+                    y, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b, dm.topk_ids,
+                    dm.lora_ids, case.E, case.H, case.rank, case.L, case.scale,
+                    topk_weights=wts, workspace=ws))
+        ms = timed(fns)
         res[name] = {"pairs_per_s": round(case.T * case.top_k / (ms / 1e3), 1),
                      "ms": round(ms, 4), "routed_pairs": pairs,
                      "GB_per_s": round(ab / (ms / 1e3) / 1e9, 1),
                      "hbm_frac": round(ab / (ms / 1e3) / 1e9 / hbm_peak, 4),
-                     "launches_per_call": 3}
-        del dm, y, ws
+                     "launches_per_call": 3, "copies": len(fns)}
+        del fns, ws
         torch.cuda.empty_cache()
 
 
@@ -639,10 +670,11 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(dt / K * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; random-init adapters)",
-            "config": {"workload": case.name, "rows_per_step": rows},
+            "config": decode_config(case, world),
             "cpu_baseline": {"value": round(value, 1), "unit": "rows/s", "cores": cores,
                              "kind": "oracle",
-                             "sample": f"first {rows} rows of the decode batch per step"},
+                             "sample": f"first {rows} rows of the {case.n}-row decode batch "
+                                       f"per step ({K} steps after {W} warm-up steps)"},
             "e2e": {"value": round(value, 1), "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
