@@ -313,6 +313,29 @@ int lora_moe_w2_delta(void *y, const void *x, const int64_t *w_ptr_a, int64_t st
                       lora_stream_t stream);
 
 /*
+ * lora_moe_w2_delta_routed -- [punica] add_lora_w2 with the routing that the
+ * preceding add_lora_w13 of the same layer handed over ("Reuses routing
+ * tensors returned by add_lora_w13"): the same delta as lora_moe_w2_delta,
+ * without sorting the pairs again.  `workspace` must be the workspace that a
+ * preceding lora_moe_w13_delta call was given, on the same stream, with the
+ * same T, top_k, E, num_loras and routing arrays (topk_ids, lora_ids,
+ * expert_map, adapter_enabled), and left untouched since: that call wrote the
+ * pairs' clustering by (adapter, local expert) at the front of it, and this
+ * call reads it.  Every routing decision (no adapter, a switched-off adapter,
+ * a non-local expert, a bad id) is taken from there, and its errors were
+ * already reported by the w13 call.  x, the banks, topk_weights, y and the
+ * arithmetic are as in lora_moe_w2_delta; ws_bytes must be at least
+ * lora_moe_workspace_size(T, top_k, E, num_loras, rank, 1).  The workspace is
+ * not written before the kernels read the routing, so a following call may
+ * reuse it again.
+ */
+int lora_moe_w2_delta_routed(void *y, const void *x, const int64_t *w_ptr_a, int64_t stride_a,
+                             const int64_t *w_ptr_b, int64_t stride_b, const float *topk_weights,
+                             int T, int top_k, int E, int H, int I, int rank, int num_loras,
+                             float scale, int add_inputs, void *workspace, size_t ws_bytes,
+                             uint32_t *err_word, lora_stream_t stream);
+
+/*
  * lora_delta_fused_noalloc -- lora_delta_fused for callers that cannot
  * allocate device memory.  The pages have no counterpart to this call: it
  * exists for callers whose memory is fixed up front (a budget set at start

@@ -26,7 +26,7 @@ __all__ = [
     "lora_route_with_scratch", "lora_shrink", "lora_expand", "lora_delta_fused",
     "lora_delta_segmented",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_moe_w13_delta",
-    "lora_moe_w2_delta", "lora_get_error", "new_error_word",
+    "lora_moe_w2_delta", "lora_moe_w2_delta_routed", "lora_get_error", "new_error_word",
     "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes", "lora_set_wait_limit_ns",
     "WAIT_LIMIT_DEFAULT_NS",
 ]
@@ -411,6 +411,30 @@ def lora_moe_w2_delta(y, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, topk
         0 if expert_map is None else expert_map.numel(), _ptr(adapter_enabled),
         _ptr(topk_weights), T, top_k, int(E), int(H), I, int(rank), int(num_loras),
         float(scale), int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_moe_w2_delta_routed(y, x, w_ptr_a, stride_a: int, w_ptr_b, stride_b: int, T: int,
+                             top_k: int, E: int, H: int, rank: int, num_loras: int,
+                             scale: float, workspace, topk_weights=None, add_inputs: bool = True,
+                             err=None, stream=None):
+    """add_lora_w2 on the routing that the preceding ``lora_moe_w13_delta`` left in
+    ``workspace`` (the same T, top_k, E, num_loras and routing arrays; the
+    workspace untouched since): no second sort of the pairs."""
+    _dev(y, "y", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(w_ptr_a, "w_ptr_a", torch.int64)
+    _dev(w_ptr_b, "w_ptr_b", torch.int64)
+    _opt_dev(topk_weights, "topk_weights", torch.float32)
+    if workspace is None:
+        raise ValueError("lora_moe_w2_delta_routed needs the w13 call's workspace")
+    I = x.shape[1]
+    if x.shape[0] != T * top_k:
+        raise ValueError("x must hold one row per (token, slot) pair")
+    _check("lora_moe_w2_delta_routed", lib().lora_moe_w2_delta_routed(
+        _ptr(y), _ptr(x), _ptr(w_ptr_a), int(stride_a), _ptr(w_ptr_b), int(stride_b),
+        _ptr(topk_weights), int(T), int(top_k), int(E), int(H), I, int(rank), int(num_loras),
+        float(scale), int(bool(add_inputs)), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
 
 
 def lora_get_error(err: torch.Tensor, clear: bool = True, stream=None) -> int:

@@ -43,6 +43,8 @@ SIGNATURES = {
                                 _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp, _vp]),
     "lora_moe_w2_delta": (_i, [_vp, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i, _vp, _vp,
                                _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp, _vp]),
+    "lora_moe_w2_delta_routed": (_i, [_vp, _vp, _vp, _i64, _vp, _i64, _vp, _i, _i, _i, _i, _i,
+                                      _i, _i, _f, _i, _vp, _sz, _vp, _vp]),
     "lora_get_error": (_i, [_vp, _vp, _i, _vp]),
     "lora_noalloc_scratch_bytes": (_sz, []),
     "lora_delta_fused_noalloc": (_i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i,

@@ -867,6 +867,7 @@ struct MoeCall {
   float scale;
   int add_inputs;
   int zero_skipped;  // write zeros on the pairs with no delta (fresh output)
+  int routed;        // the workspace already holds this call's routing (w2 after w13)
 };
 
 int moe_delta(const MoeCall& c, void* workspace, size_t ws_bytes, uint32_t* err_word,
@@ -875,7 +876,7 @@ int moe_delta(const MoeCall& c, void* workspace, size_t ws_bytes, uint32_t* err_
   const int n_cols = c.widths[0] + (c.n_slices > 1 ? c.widths[1] : 0);
   if (n64 == 0 || n_cols == 0) return LORA_OK;
   if (n64 > (1 << 30)) return LORA_ERR_UNSUPPORTED;
-  if (!c.out || !c.x || !c.w_ptr_a || !c.w_ptr_b || !c.topk_ids || !c.lora_ids)
+  if (!c.out || !c.x || !c.w_ptr_a || !c.w_ptr_b || (!c.routed && (!c.topk_ids || !c.lora_ids)))
     return LORA_ERR_ARG;
   if (c.expert_map && c.n_global < 1) return LORA_ERR_ARG;
   if ((int64_t)c.E * c.num_loras > kMaxKeys) return LORA_ERR_UNSUPPORTED;
@@ -891,10 +892,12 @@ int moe_delta(const MoeCall& c, void* workspace, size_t ws_bytes, uint32_t* err_
   const Workspace w = carve(workspace, n, n_keys);
   int32_t* perm = w.perm;
   int32_t* seg = w.seg;
-  rc = launch_route_scratch(MoeKey{c.topk_ids, c.lora_ids, c.expert_map, c.adapter_enabled,
-                                   c.top_k, c.E, c.num_loras, c.n_global},
-                            n, n_keys, perm, seg, w.rcounts, err_word, s);
-  if (rc) return rc;
+  if (!c.routed) {
+    rc = launch_route_scratch(MoeKey{c.topk_ids, c.lora_ids, c.expert_map, c.adapter_enabled,
+                                     c.top_k, c.E, c.num_loras, c.n_global},
+                              n, n_keys, perm, seg, w.rcounts, err_word, s);
+    if (rc) return rc;
+  }
 
   DeltaArgs a = {};
   if ((rc = make_slices(c.widths, c.n_slices, 0, a.sl, a.rel))) return rc;
@@ -1063,6 +1066,41 @@ int lora_moe_w2_delta(void* y, const void* x, const int64_t* w_ptr_a, int64_t st
   c.num_loras = num_loras;
   c.scale = scale;
   c.add_inputs = add_inputs ? 1 : 0;
+  return moe_delta(c, workspace, ws_bytes, err_word, (cudaStream_t)stream);
+}
+
+int lora_moe_w2_delta_routed(void* y, const void* x, const int64_t* w_ptr_a, int64_t stride_a,
+                             const int64_t* w_ptr_b, int64_t stride_b, const float* topk_weights,
+                             int T, int top_k, int E, int H, int I, int rank, int num_loras,
+                             float scale, int add_inputs, void* workspace, size_t ws_bytes,
+                             uint32_t* err_word, lora_stream_t stream) {
+  if (T < 0 || top_k < 0 || E < 1 || H < 0 || I < 0 || num_loras < 1 || stride_a < 0 ||
+      stride_b < 0)
+    return LORA_ERR_ARG;
+  MoeCall c = {};
+  c.out = y;
+  c.ld_out = H;
+  c.x = x;
+  c.ld_x = I;
+  c.k_in = I;
+  c.x_div = 1;
+  c.n_slices = 1;
+  c.widths[0] = H;
+  c.w_ptr_a = w_ptr_a;
+  c.w_ptr_b = w_ptr_b;
+  c.stride_a = stride_a;
+  c.stride_b = stride_b;
+  c.pair_weight = topk_weights;
+  c.T = T;
+  c.top_k = top_k;
+  c.E = E;
+  c.H = H;
+  c.I = I;
+  c.rank = rank;
+  c.num_loras = num_loras;
+  c.scale = scale;
+  c.add_inputs = add_inputs ? 1 : 0;
+  c.routed = 1;
   return moe_delta(c, workspace, ws_bytes, err_word, (cudaStream_t)stream);
 }
 

@@ -80,6 +80,10 @@ def lib() -> ctypes.CDLL:
                                 _vpp, _vpp, _vpp, ctypes.c_int, _vpp, _vpp] + [
                                     ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int,
                                                          ctypes.c_int, _u32p]
+    L.oracle_gather_rank_blocks.restype = ctypes.c_int
+    L.oracle_gather_rank_blocks.argtypes = [_vpp, _vpp] + [ctypes.c_int] * 4
+    L.oracle_rank_sum.restype = ctypes.c_int
+    L.oracle_rank_sum.argtypes = [_vpp, _vpp, ctypes.c_int, ctypes.c_int64]
     _LIB = L
     return L
 
@@ -355,3 +359,78 @@ def moe_w2(y: np.ndarray, x: np.ndarray, banks_a: list, banks_b: list, topk_ids:
                                E, H, I, rank, num_loras, float(scale), int(bool(add_inputs)),
                                int(acc64), ctypes.byref(err)), "moe_w2")
     return out, int(err.value)
+
+
+# ------------------------------------------- tensor-parallel sharded forms ----
+# "vllm.lora.fully_sharded_layers": the shrink and the expand run per rank on
+# sharded adapters, with one collective on the fp32 h buffer in between.
+
+def gather_rank_blocks(shards) -> np.ndarray:
+    """Column parallel (_mcp_apply): the all-gather of the rank shards of h,
+    ``shards`` [tp, S, n, Rs] -> h [S, n, tp * Rs] (rank p's block at p * Rs)."""
+    sh = np.ascontiguousarray(shards, dtype=np.float32)
+    tp, S, n, Rs = sh.shape
+    h = np.empty((S, n, tp * Rs), dtype=np.float32)
+    _check(lib().oracle_gather_rank_blocks(_p(h), _p(sh), tp, S, n, Rs), "gather_rank_blocks")
+    return h
+
+
+def rank_sum(parts) -> np.ndarray:
+    """Row parallel (RowParallelLinearWithShardedLoRA apply): the all-reduce of
+    the rank partials of h, ``parts`` [tp, ...] -> fp32 sum in rank order."""
+    pa = np.ascontiguousarray(parts, dtype=np.float32)
+    tp = pa.shape[0]
+    h = np.empty(pa.shape[1:], dtype=np.float32)
+    _check(lib().oracle_rank_sum(_p(h), _p(pa), tp, h.size), "rank_sum")
+    return h
+
+
+def shard_pool_a_rows(pool: OraclePool, tp: int, p: int) -> OraclePool:
+    """Rank p's pool of the column-parallel form: rows p*R/tp .. (p+1)*R/tp - 1
+    of every slot's padded A (the rank slice), B left whole (unused)."""
+    Rs = pool.R // tp
+    sp = OraclePool(k_in=pool.k_in, widths=pool.widths, max_loras=pool.max_loras, R=Rs)
+    sp.A = [np.ascontiguousarray(a[:, p * Rs:(p + 1) * Rs, :]) for a in pool.A]
+    sp.B = pool.B
+    sp.scale_table = pool.scale_table
+    sp.a_table = _table_like(pool.a_table, pool.A, sp.A)
+    sp.b_table = pool.b_table
+    return sp
+
+
+def shard_pool_a_cols(pool: OraclePool, tp: int, p: int) -> OraclePool:
+    """Rank p's pool of the row-parallel form: columns p*k_in/tp .. of every
+    slot's A (the input slice, as x is sliced), B left whole (unused)."""
+    ks = pool.k_in // tp
+    sp = OraclePool(k_in=ks, widths=pool.widths, max_loras=pool.max_loras, R=pool.R)
+    sp.A = [np.ascontiguousarray(a[:, :, p * ks:(p + 1) * ks]) for a in pool.A]
+    sp.B = pool.B
+    sp.scale_table = pool.scale_table
+    sp.a_table = _table_like(pool.a_table, pool.A, sp.A)
+    sp.b_table = pool.b_table
+    return sp
+
+
+def shard_pool_b_rows(pool: OraclePool, tp: int, p: int) -> OraclePool:
+    """Rank p's pool for the expand of either form: output columns p*w_j/tp ..
+    of every slice (rows of B), A left whole (unused)."""
+    ws = tuple(w // tp for w in pool.widths)
+    sp = OraclePool(k_in=pool.k_in, widths=ws, max_loras=pool.max_loras, R=pool.R)
+    sp.A = pool.A
+    sp.B = [np.ascontiguousarray(b[:, p * w:(p + 1) * w, :]) for b, w in zip(pool.B, ws)]
+    sp.scale_table = pool.scale_table
+    sp.a_table = pool.a_table
+    sp.b_table = _table_like(pool.b_table, pool.B, sp.B)
+    return sp
+
+
+def _table_like(table, old, new):
+    """Pointer table of ``new`` with the entries that are 0 in ``table`` kept 0."""
+    S = len(old)
+    L = old[0].shape[0]
+    t = np.zeros_like(table)
+    for j in range(S):
+        for s in range(L):
+            if table[j * L + s]:
+                t[j * L + s] = new[j][s].ctypes.data
+    return t

@@ -590,3 +590,44 @@ int oracle_moe_w2(uint16_t *y, const uint16_t *x, const uint16_t *const *w_ptr_a
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Tensor-parallel sharded LoRA [sharded].  Between the per-rank shrink */
+/* (scale 1, fp32 buffer) and the per-rank expand sits one collective:  */
+/*  - column parallel (_mcp_apply, ColumnParallelLinearWithShardedLoRA: */
+/*    A sliced along the rank): rank p's shard of h, [S, n, Rs] from    */
+/*    its Rs rows of A, is all-gathered along the last dimension,       */
+/*    h[j][i][p*Rs + q] = shard_p[j][i][q]; a pure copy, so every rank  */
+/*    holds the unsharded h exactly;                                    */
+/*  - row parallel (RowParallelLinearWithShardedLoRA apply: A sliced    */
+/*    along the input, like x): rank p's partial h, [S, n, R] over its  */
+/*    k columns, is all-reduced, h = ((part_0 + part_1) + ...) +        */
+/*    part_{tp-1} in fp32, rank order (reading: the page leaves the     */
+/*    order to the collective).                                         */
+/* ------------------------------------------------------------------ */
+int oracle_gather_rank_blocks(float *h, const float *shards, int tp, int S, int n, int Rs)
+{
+    if (tp <= 0 || S < 0 || n < 0 || Rs < 0)
+        return 1;
+    const int R = tp * Rs;
+    for (int p = 0; p < tp; ++p)
+        for (int j = 0; j < S; ++j)
+            for (int i = 0; i < n; ++i)
+                for (int q = 0; q < Rs; ++q)
+                    h[((size_t)j * n + i) * R + (size_t)p * Rs + q] =
+                        shards[(((size_t)p * S + j) * n + i) * Rs + q];
+    return 0;
+}
+
+int oracle_rank_sum(float *h, const float *parts, int tp, int64_t len)
+{
+    if (tp <= 0 || len < 0)
+        return 1;
+    for (int64_t e = 0; e < len; ++e) {
+        float s = parts[e];
+        for (int p = 1; p < tp; ++p)
+            s = s + parts[(size_t)p * len + e];
+        h[e] = s;
+    }
+    return 0;
+}

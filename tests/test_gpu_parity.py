@@ -837,3 +837,69 @@ def test_wait_time_out_sets_the_error_bit_and_the_next_call_is_correct(ld, di, o
         ld.lora_delta_fused(out2, d.x, d.seq_slot, d.pool, workspace=ws, err=err2)
         e2 = ld.lora_get_error(err2)
         check_linear(oracle, case, di.bits(out2), e2)
+
+
+# ------------------------------------------- w13 -> w2 routing hand-over --
+
+@pytest.mark.parametrize("full", [True, False])
+def test_moe_w2_on_the_routing_of_w13(ld, di, oracle, full):
+    """"punica_base.py", add_lora_w2: "Reuses routing tensors returned by
+    add_lora_w13".  lora_moe_w2_delta_routed reads the clustering that the
+    preceding lora_moe_w13_delta left in its workspace.  Its result equals
+    lora_moe_w2_delta's (which sorts again) bit for bit, and the oracle's within
+    the tolerance; pairs with no delta keep y.  Full size: the FC1 workload's
+    routing with routing weights.  Small: an expert map (5 of 12 experts local),
+    a switched-off adapter and repeated experts."""
+    if full:
+        mc = inputs.moe_case(seed=1240)
+        c = inputs.moe_w2_case()
+        mc.topk_ids, mc.lora_ids = c.topk_ids, c.lora_ids
+        emap = en = None
+        E_loc = c.E
+    else:
+        mc = inputs.moe_case(seed=73, T=90, top_k=4, E=12, H=136, I=48, rank=16, L=3,
+                             p_none=0.1, dup_frac=0.3)
+        c = inputs.moe_w2_case(seed=75, T=90, top_k=4, E=12, H=136, I=48, rank=16, L=3)
+        c.topk_ids, c.lora_ids = mc.topk_ids, mc.lora_ids
+        local = {2: 3, 5: 0, 7: 4, 8: 1, 11: 2}
+        emap = np.full(12, -1, np.int32)
+        for g, loc in local.items():
+            emap[g] = loc
+        inv = {loc: g for g, loc in local.items()}
+        pick = lambda b: np.ascontiguousarray(b[[inv[i] for i in range(5)]])
+        mc = inputs.MoeCase(**{**mc.__dict__, "E": 5, "A_banks": [pick(b) for b in mc.A_banks],
+                               "B_banks": [pick(b) for b in mc.B_banks]})
+        c = inputs.MoeDownCase(**{**c.__dict__, "E": 5, "A_banks": [pick(c.A_banks[0])],
+                                  "B_banks": [pick(c.B_banks[0])]})
+        en = np.array([1, 0, 1], np.int32)
+        E_loc = 5
+    dm = di.moe_to_device(mc)
+    d2 = di.moe_to_device(c)
+    topk, lora = dm.topk_ids, dm.lora_ids
+    y13 = di.bf16(inputs.moe_y0(mc.seed, (mc.T, mc.top_k, 2 * mc.I)), "cuda")
+    ws = torch.empty(ld.lora_moe_workspace_size(mc.T, mc.top_k, E_loc, mc.L, mc.rank, False),
+                     dtype=torch.uint8, device="cuda")
+    wts = torch.from_numpy(c.topk_weights).cuda()
+    err = ld.new_error_word()
+    ld.lora_moe_w13_delta(y13, dm.x, dm.w_ptr_a, dm.stride_a, dm.w_ptr_b, dm.stride_b, False,
+                          topk, lora, E_loc, mc.I, mc.rank, mc.L, mc.scale,
+                          expert_map=_opt_cuda(emap), adapter_enabled=_opt_cuda(en),
+                          workspace=ws, err=err)
+    y_routed = di.bf16(c.y0, "cuda")
+    ld.lora_moe_w2_delta_routed(y_routed, d2.x, d2.w_ptr_a, d2.stride_a, d2.w_ptr_b, d2.stride_b,
+                                c.T, c.top_k, E_loc, c.H, c.rank, c.L, c.scale, ws,
+                                topk_weights=wts, err=err)
+    e = ld.lora_get_error(err)
+    y_own = di.bf16(c.y0, "cuda")
+    ld.lora_moe_w2_delta(y_own, d2.x, d2.w_ptr_a, d2.stride_a, d2.w_ptr_b, d2.stride_b, topk,
+                         lora, E_loc, c.H, c.rank, c.L, c.scale, expert_map=_opt_cuda(emap),
+                         adapter_enabled=_opt_cuda(en), topk_weights=wts)
+    got = di.bits(y_routed)
+    assert np.array_equal(got, di.bits(y_own))
+    ref, ref_err = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids,
+                                 c.rank, c.scale, c.L, expert_map=emap, adapter_enabled=en,
+                                 topk_weights=c.topk_weights)
+    assert e == ref_err
+    assert_close(got, ref, "w2 on the routing of w13")
+    keep = np.all(ref == c.y0, axis=2)
+    assert keep.any() and np.array_equal(got[keep], c.y0[keep])

@@ -4,7 +4,8 @@ Each case copies ``oracle/lora_oracle.c``, plants one plausible mistake (a
 dropped term, a transposed operand, a wrong index or offset, a missing scale, a
 wrong tie rule, an unstable sort, an overwrite that still adds or drops the scale, non-zero padding, swapped MoE slices, a wrong
 adapter stride, a per-token input row for the down projection, a dropped routing
-weight, a non-local expert treated as local, a disabled adapter applied), compiles the copy into a temporary library and runs the pin
+weight, a non-local expert treated as local, a disabled adapter applied, a reversed rank gather, a dropped rank
+partial), compiles the copy into a temporary library and runs the pin
 suite against it in a subprocess.  The pins must fail for every mutant.
 """
 import os
@@ -63,6 +64,12 @@ MUTANTS = {
     "moe_nonlocal_expert_as_zero": (
         "        else if (expert_map[e] < 0)\n            return 0;",
         "        else if (expert_map[e] < 0)\n            e = 0;"),
+    "gather_rank_blocks_reversed": (
+        "                    h[((size_t)j * n + i) * R + (size_t)p * Rs + q] =",
+        "                    h[((size_t)j * n + i) * R + (size_t)(tp - 1 - p) * Rs + q] ="),
+    "rank_sum_drops_last_rank": (
+        "        for (int p = 1; p < tp; ++p)\n            s = s + parts[(size_t)p * len + e];",
+        "        for (int p = 1; p < tp - 1; ++p)\n            s = s + parts[(size_t)p * len + e];"),
     "moe_disabled_adapter_applied": (
         "adapter_enabled && adapter_enabled[l] == 0)",
         "adapter_enabled && adapter_enabled[l] == 2)"),

@@ -662,3 +662,115 @@ def test_moe_w2_weight_two_is_double_scale(oracle):
     plain, _ = oracle.moe_w2(c.y0, c.x, c.A_banks, c.B_banks, c.topk_ids, c.lora_ids, c.rank,
                              c.scale, c.L)
     assert not np.array_equal(a, plain)
+
+
+# ------------------------------------------- tensor-parallel sharded forms --
+
+def test_gather_rank_blocks_is_numpy_concatenation_along_the_rank(oracle):
+    """'vllm.lora.fully_sharded_layers', _mcp_apply: the all-gather of the h shards
+    along the last dimension is numpy's concatenation of the rank blocks."""
+    rng = np.random.default_rng(3)
+    for tp, S, n, Rs in [(1, 2, 5, 8), (2, 3, 7, 8), (4, 1, 9, 4)]:
+        shards = rng.standard_normal((tp, S, n, Rs)).astype(np.float32)
+        want = np.concatenate(list(shards), axis=2)
+        assert np.array_equal(oracle.gather_rank_blocks(shards), want)
+
+
+def test_rank_sum_is_the_rank_order_fp32_sum(oracle):
+    """RowParallelLinearWithShardedLoRA apply: the all-reduce of the h partials.
+    Integer-valued partials sum exactly; random partials stay within tp - 1 fp32
+    roundings of the exact sum; one rank is the identity."""
+    rng = np.random.default_rng(4)
+    ints = rng.integers(-1000, 1000, size=(4, 6, 5)).astype(np.float32)
+    assert np.array_equal(oracle.rank_sum(ints), ints.astype(np.int64).sum(0).astype(np.float32))
+    for tp in (2, 3, 4):
+        parts = rng.standard_normal((tp, 3, 7, 16)).astype(np.float32)
+        exact = parts.astype(np.float64).sum(0)
+        bound = (tp - 1) * 2.0 ** -24 * np.abs(parts.astype(np.float64)).sum(0) + 1e-30
+        assert np.all(np.abs(oracle.rank_sum(parts) - exact) <= bound)
+    one = rng.standard_normal((1, 4, 4)).astype(np.float32)
+    assert np.array_equal(oracle.rank_sum(one), one[0])
+
+
+def _tp_case():
+    return inputs.linear_case(131, n=37, k_in=96, widths=(64, 32), max_loras=3, max_rank=16,
+                              ranks=[16, 8, 12], alpha=16.0, p_none=0.2)
+
+
+def _rank_columns(case, tp, p, offset_start=0):
+    """Columns of out that rank p's shard of the expand covers (per slice j:
+    off_j + p * w_j / tp ...)."""
+    cols, off = [], offset_start
+    for w in case.widths:
+        ws = w // tp
+        cols.extend(range(off + p * ws, off + (p + 1) * ws))
+        off += w
+    return np.array(cols)
+
+
+@pytest.mark.parametrize("tp", [2, 4])
+def test_column_sharded_form_equals_the_unsharded_delta_bit_for_bit(oracle, tp):
+    """'vllm.lora.fully_sharded_layers', _mcp_apply (ColumnParallelLinearWithShardedLoRA,
+    MergedColumnParallelLinearWithShardedLoRA): A sliced along the rank, each rank's
+    shrink (scale 1) into an fp32 buffer, all-gather, then each rank expands with the
+    B rows of its output columns.  Every rank then holds the unsharded h exactly, so
+    its output columns equal the unsharded delta's bit for bit (over two slices)."""
+    case = _tp_case()
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, 3, 16)
+    full = case.out0.copy()
+    oracle.delta(full, case.x, case.seq_slot, pool)
+    shards = np.stack([oracle.shrink(case.x, case.seq_slot,
+                                     oracle.shard_pool_a_rows(pool, tp, p), None)[0]
+                       for p in range(tp)])
+    h = oracle.gather_rank_blocks(shards)
+    for p in range(tp):
+        cols = _rank_columns(case, tp, p)
+        out_p = np.ascontiguousarray(case.out0[:, cols])
+        oracle.expand(out_p, h, case.seq_slot, oracle.shard_pool_b_rows(pool, tp, p),
+                      pool.scale_table)
+        assert np.array_equal(out_p, full[:, cols])
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4])
+def test_row_sharded_form_matches_the_dense_composition(oracle, tp):
+    """RowParallelLinearWithShardedLoRA apply: x and A sliced along the input; each
+    rank's shrink gives a partial h over its k columns; the all-reduce sums them;
+    rank p expands with its B rows into its slice of the (partial-sum) output at
+    offset_start = p * shard.  Within the slice the result is RN(out + scale * h.B)
+    with h the reduced sum: within the parity tolerance of the fp64 dense
+    composition (one rank: the unsharded delta bit for bit); outside the slice
+    nothing changes; over all ranks every column gets its delta from one rank."""
+    case = inputs.linear_case(133, n=29, k_in=128, widths=(64,), max_loras=3, max_rank=16,
+                              ranks=[16, 4, 12], alpha=16.0, p_none=0.2)
+    pool = oracle.build_pool(case.adapters, case.k_in, case.widths, 3, 16)
+    ks = case.k_in // tp
+    parts = np.stack([oracle.shrink(np.ascontiguousarray(case.x[:, p * ks:(p + 1) * ks]),
+                                    case.seq_slot, oracle.shard_pool_a_cols(pool, tp, p),
+                                    None)[0] for p in range(tp)])
+    h = oracle.rank_sum(parts)
+    xf = f32(case.x).astype(np.float64)
+    A = f32(pool.A[0]).astype(np.float64)
+    B = f32(pool.B[0]).astype(np.float64)
+    full = case.out0.copy()
+    oracle.delta(full, case.x, case.seq_slot, pool)
+    ws = case.widths[0] // tp
+    covered = np.zeros(case.out0.shape, dtype=bool)
+    for p in range(tp):
+        out_p = case.out0.copy()
+        oracle.expand(out_p, h, case.seq_slot, oracle.shard_pool_b_rows(pool, tp, p),
+                      pool.scale_table, offset_start=p * ws)
+        inside = np.zeros(case.ld_out, dtype=bool)
+        inside[p * ws:(p + 1) * ws] = True
+        assert np.array_equal(out_p[:, ~inside], case.out0[:, ~inside])
+        routed = case.seq_slot >= 0
+        assert np.array_equal(out_p[~routed], case.out0[~routed])
+        covered[:, inside] = True
+        for i in np.flatnonzero(routed):
+            s = case.seq_slot[i]
+            ref = f32(case.out0[i, inside]).astype(np.float64) + float(pool.scale_table[s]) * (
+                (A[s] @ xf[i]) @ B[s][p * ws:(p + 1) * ws].T)
+            got = f32(out_p[i, inside]).astype(np.float64)
+            assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+        if tp == 1:
+            assert np.array_equal(out_p, full)
+    assert covered.all()
