@@ -192,6 +192,24 @@ int lora_expand(void *out, int64_t ld_out, const float *h, const int32_t *seq_sl
                 size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
 
 /*
+ * lora_expand_gathered -- lora_expand on h as the all-gather of rank-sharded
+ * shrinks leaves it ([sharded] _mcp_apply, ColumnParallelLinearWithShardedLoRA
+ * and MergedColumnParallelLinearWithShardedLoRA: A sliced along the rank,
+ * each of `parts` tensor-parallel ranks shrinks its R / parts rows into an
+ * fp32 buffer [S, n, R / parts], and the buffers are all-gathered).  h is
+ * [parts][S][n][R / parts] fp32, rank-major: h[p][j][i][q] is rank
+ * p * R / parts + q of slice j, row i.  The rest is lora_expand with R the
+ * whole rank; each rank calls it with the B rows of its own output columns
+ * (b_table, widths) and gets them bit for bit as the unsharded delta does.
+ * parts = 1 is lora_expand.  Requires R % parts == 0 (else LORA_ERR_ARG).
+ */
+int lora_expand_gathered(void *out, int64_t ld_out, const float *h, int parts,
+                         const int32_t *seq_slot, const uint64_t *b_table,
+                         const float *scale_table, const int32_t *widths, int S, int R, int n,
+                         int max_loras, int offset_start, int add_inputs, void *workspace,
+                         size_t ws_bytes, uint32_t *err_word, lora_stream_t stream);
+
+/*
  * lora_delta_fused -- the routed delta in one pass ([punica] add_lora_linear,
  * [metrale] apply_lora_bgmv): for every routed row i (s = seq_slot[i]) and
  * slice j whose A and B table entries are both nonzero,

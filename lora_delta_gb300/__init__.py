@@ -23,7 +23,8 @@ from ._lib import LibraryMissing, lib, status_string
 __all__ = [
     "LoraError", "LibraryMissing", "LoraPool", "lora_scale", "lora_pool_pack",
     "lora_workspace_size", "lora_workspace_min_size", "lora_route", "lora_route_scratch_size",
-    "lora_route_with_scratch", "lora_shrink", "lora_expand", "lora_delta_fused",
+    "lora_route_with_scratch", "lora_shrink", "lora_expand", "lora_expand_gathered",
+    "lora_delta_fused",
     "lora_delta_segmented",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_moe_w13_delta",
     "lora_moe_w2_delta", "lora_moe_w2_delta_routed", "lora_get_error", "new_error_word",
@@ -260,6 +261,29 @@ def lora_expand(out, h, seq_slot, pool: LoraPool, scale_table=None, offset_start
         _ptr(out), ld_out, _ptr(h), _ptr(seq_slot), _ptr(pool.b_table), _ptr(scale_table), w,
         pool.S, pool.R, n, pool.max_loras, int(offset_start), int(bool(add_inputs)), _ptr(ws),
         wsb, _ptr(err), _stream(stream)))
+
+
+def lora_expand_gathered(out, h_parts, seq_slot, pool: LoraPool, scale_table=None,
+                         offset_start: int = 0, add_inputs: bool = True, workspace=None,
+                         err=None, stream=None):
+    """lora_expand on the all-gather of rank-sharded shrinks: ``h_parts``
+    [parts, S, n, R / parts] float32 (rank-major), ``pool`` the pool of this rank's
+    output columns with the whole rank R."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(h_parts, "h_parts", torch.float32)
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n, ld_out = out.shape
+    parts = h_parts.shape[0]
+    if h_parts.dim() != 4 or h_parts.shape[1:3] != (pool.S, n) or \
+            h_parts.shape[3] * parts != pool.R:
+        raise ValueError("h_parts must be [parts, S, n, R / parts]")
+    ws, wsb = _workspace(lora_workspace_size(n, pool.S, pool.R, pool.max_loras) if n > 1024
+                         else 0, workspace, out.device, stream)
+    w = _widths_arg(pool.widths)
+    _check("lora_expand_gathered", lib().lora_expand_gathered(
+        _ptr(out), ld_out, _ptr(h_parts), parts, _ptr(seq_slot), _ptr(pool.b_table),
+        _ptr(scale_table), w, pool.S, pool.R, n, pool.max_loras, int(offset_start),
+        int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
 
 
 def lora_delta_fused(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,

@@ -32,6 +32,8 @@ SIGNATURES = {
     "lora_shrink": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp, _vp]),
     "lora_expand": (_i, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz,
                          _vp, _vp]),
+    "lora_expand_gathered": (_i, [_vp, _i64, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                  _i, _vp, _sz, _vp, _vp]),
     "lora_delta_fused": (_i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                               _i, _vp, _sz, _vp, _vp]),
     "lora_delta_segmented": (_i, [_vp, _i64, _vp, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i,

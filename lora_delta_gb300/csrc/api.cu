@@ -10,6 +10,7 @@
 #include <unordered_map>
 
 #include "bgmv.cuh"
+#include "bgmv_fused.cuh"
 #include "common.cuh"
 #include "keyed.cuh"
 #include "lora_delta.h"
@@ -246,8 +247,46 @@ int launch_delta_r(const DeltaArgs& a, const Tables& tb, int n_keys, int smem,
   return cuda_status(e);
 }
 
+// The fused small-segment kernel for one k stage per CTA (bgmv_fused_kernel);
+// LORA_FUSED_KERNEL=0 keeps every fused call on the general cluster kernel.
+bool fused_kernel_on() {
+  static const bool on = env_int("LORA_FUSED_KERNEL", 1) != 0;
+  return on;
+}
+
+template <int RMAX, class Tables>
+int launch_fused_r(const DeltaArgs& a, const Tables& tb, int n_keys, int smem,
+                   cudaStream_t stream) {
+  auto kernel = bgmv_fused_kernel<RMAX, Tables>;
+  const int cs = a.cs;
+  if (prepare_kernel(kernel, smem, cs > 8) != cudaSuccess) return LORA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_keys * cs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 2 : 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, a, tb));
+}
+
 template <int MODE, class Tables>
 int launch_delta(const DeltaArgs& a, const Tables& tb, int n_keys, cudaStream_t s) {
+  if (MODE == kModeFused && fused_kernel_on() && fused_kernel_fits(a)) {
+    const int smem = fused_plan(a).total;
+    if (smem <= 226 * 1024) {
+      if (a.R <= 16) return launch_fused_r<16>(a, tb, n_keys, smem, s);
+      if (a.R <= 32) return launch_fused_r<32>(a, tb, n_keys, smem, s);
+      return launch_fused_r<64>(a, tb, n_keys, smem, s);
+    }
+  }
   const int smem = smem_plan(a, MODE).total;
   if (smem > 226 * 1024) return LORA_ERR_UNSUPPORTED;  // leaves room for static smem
   if (a.R <= 16) return launch_delta_r<16, MODE>(a, tb, n_keys, smem, s);
@@ -614,6 +653,41 @@ __global__ void segment_plan_kernel(const int32_t* __restrict__ offsets, int n_s
   }
 }
 
+namespace {
+
+// lora_expand and lora_expand_gathered: h as [parts][S][n][R / parts].
+int expand_parts(void* out, int64_t ld_out, const float* h, int parts, const int32_t* seq_slot,
+                 const uint64_t* b_table, const float* scale_table, const int32_t* widths, int S,
+                 int R, int n, int max_loras, int offset_start, int add_inputs, void* workspace,
+                 size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (n < 0) return LORA_ERR_ARG;
+  if (n == 0) return LORA_OK;
+  if (!out || !h || !seq_slot || !b_table) return LORA_ERR_ARG;
+  int rc = check_max_loras(max_loras);
+  if (rc) return rc;
+  DeltaArgs a = {};
+  if ((rc = make_slices(widths, S, offset_start, a.sl, a.rel))) return rc;
+  if ((rc = check_rank(S, R))) return rc;
+  if (ld_out < (int64_t)offset_start + a.sl.n_cols) return LORA_ERR_SHAPE;
+  if (ld_out % 8 || !aligned16(out) || !aligned16(h)) return LORA_ERR_ALIGN;
+  if (a.sl.n_cols == 0) return LORA_OK;
+  a.out = (__nv_bfloat16*)out;
+  a.ld_out = ld_out;
+  a.h = (float*)h;
+  a.R = R;
+  a.add_inputs = add_inputs ? 1 : 0;
+  a.sr_max = S * R;
+  rc = prepare_rows(a, seq_slot, n, max_loras, (S * R + 15) / 16 * 16, workspace, ws_bytes,
+                    err_word, (cudaStream_t)stream, nullptr);
+  if (rc) return rc;
+  a.h_parts = parts;
+  plan_tiles(a, 8, a.sl.n_cols, a.sr_max, kModeExpand);
+  LinearTables tb{nullptr, b_table, scale_table, max_loras};
+  return launch_delta<kModeExpand>(a, tb, max_loras, (cudaStream_t)stream);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* lora_status_string(int status) {
@@ -723,30 +797,20 @@ int lora_expand(void* out, int64_t ld_out, const float* h, const int32_t* seq_sl
                 const uint64_t* b_table, const float* scale_table, const int32_t* widths, int S,
                 int R, int n, int max_loras, int offset_start, int add_inputs, void* workspace,
                 size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
-  if (n < 0) return LORA_ERR_ARG;
-  if (n == 0) return LORA_OK;
-  if (!out || !h || !seq_slot || !b_table) return LORA_ERR_ARG;
-  int rc = check_max_loras(max_loras);
-  if (rc) return rc;
-  DeltaArgs a = {};
-  if ((rc = make_slices(widths, S, offset_start, a.sl, a.rel))) return rc;
-  if ((rc = check_rank(S, R))) return rc;
-  if (ld_out < (int64_t)offset_start + a.sl.n_cols) return LORA_ERR_SHAPE;
-  if (ld_out % 8 || !aligned16(out) || !aligned16(h)) return LORA_ERR_ALIGN;
-  if (a.sl.n_cols == 0) return LORA_OK;
-  a.out = (__nv_bfloat16*)out;
-  a.ld_out = ld_out;
-  a.h = (float*)h;
-  a.R = R;
-  a.add_inputs = add_inputs ? 1 : 0;
-  a.sr_max = S * R;
-  rc = prepare_rows(a, seq_slot, n, max_loras, (S * R + 15) / 16 * 16, workspace, ws_bytes,
-                    err_word, (cudaStream_t)stream, nullptr);
-  if (rc) return rc;
-  plan_tiles(a, 8, a.sl.n_cols, a.sr_max, kModeExpand);
-  LinearTables tb{nullptr, b_table, scale_table, max_loras};
-  return launch_delta<kModeExpand>(a, tb, max_loras, (cudaStream_t)stream);
+  return expand_parts(out, ld_out, h, 1, seq_slot, b_table, scale_table, widths, S, R, n,
+                      max_loras, offset_start, add_inputs, workspace, ws_bytes, err_word, stream);
 }
+
+int lora_expand_gathered(void* out, int64_t ld_out, const float* h, int parts,
+                         const int32_t* seq_slot, const uint64_t* b_table,
+                         const float* scale_table, const int32_t* widths, int S, int R, int n,
+                         int max_loras, int offset_start, int add_inputs, void* workspace,
+                         size_t ws_bytes, uint32_t* err_word, lora_stream_t stream) {
+  if (parts < 1 || R < 1 || R % parts) return LORA_ERR_ARG;
+  return expand_parts(out, ld_out, h, parts, seq_slot, b_table, scale_table, widths, S, R, n,
+                      max_loras, offset_start, add_inputs, workspace, ws_bytes, err_word, stream);
+}
+
 
 int lora_delta_segmented(void* out, int64_t ld_out, const void* x, int n, int k_in,
                          const int32_t* seg_start, int n_segs, const uint64_t* a_table,

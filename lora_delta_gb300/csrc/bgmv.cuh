@@ -128,6 +128,7 @@ struct DeltaArgs {
   int64_t ld_x;
   int k_in;
   float* h;  // [S, n, R] fp32 for the shrink / expand modes
+  int h_parts;  // expand: h as [h_parts][S][n][R / h_parts] (0 or 1: [S, n, R])
   int n;     // rows (items)
   const int32_t* seq_slot;  // own clustering by scan when perm == nullptr
   const int32_t* perm;
@@ -645,10 +646,15 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
       cluster_arrive_relaxed();  // done reading the peers' Rx (waited on later)
       __syncthreads();   // H complete
     } else {
+      // (h in rank parts, as the all-gather of rank-sharded shrinks leaves it:
+      // rank q of slice j, row i at [q / rp][j][i][q % rp])
+      const int rp = a.h_parts > 1 ? R / a.h_parts : R;
       for (int i = tid; i < nr * SRa; i += kThreads) {
         const int r = i / SRa, t = i - r * SRa;
         const int jj = t / R, q = t - jj * R;
-        H[r * SR16 + t] = a.h[((size_t)v.act_slice[jj] * a.n + prow[r]) * R + q];
+        const int part = q / rp, qq = q - part * rp;
+        H[r * SR16 + t] =
+            a.h[(((size_t)part * a.sl.S + v.act_slice[jj]) * a.n + prow[r]) * rp + qq];
       }
       __syncthreads();
     }

@@ -150,3 +150,118 @@ def test_two_rank_shards_reproduce_the_whole_batch(oracle):
     assert r0["moe_cover"] == [(0, 19), (19, 37)]
     assert r0["moe_equal"]
     assert r0["w2_equal"]
+
+
+# ------------------------------------------- tensor-parallel sharded forms --
+# "vllm.lora.fully_sharded_layers": the collective steps of lora_delta_gb300.tp
+# (the all-gather of the column-parallel h shards, the all-reduce of the
+# row-parallel h partials) between per-rank oracle shrinks and expands.
+
+def _tp_worker(rank: int, world: int, port: int, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    try:
+        import torch
+        import torch.distributed as dist
+
+        import oracle
+        from lora_delta_gb300 import dist as ldist
+        from lora_delta_gb300 import inputs, tp
+
+        r, w = ldist.init("gloo")
+        res = {}
+        # column parallel: two slices, ranks 16 split in two 8-row halves
+        case = inputs.linear_case(4401, 45, 256, (128, 64), 5, 16, [16, 8, 16, 12, 16], 32.0,
+                                  p_none=0.1)
+        pool = oracle.build_pool(case.adapters, case.k_in, case.widths, 5, 16)
+        h_shard, _ = oracle.shrink(case.x, case.seq_slot, oracle.shard_pool_a_rows(pool, w, r),
+                                   None)
+        h_all = tp.gather_rank_shards(torch.from_numpy(h_shard)).numpy()
+        mine = [None] * w
+        dist.all_gather_object(mine, h_shard)
+        res["gather_rank_major"] = bool(np.array_equal(h_all, np.stack(mine)))
+        h = oracle.gather_rank_blocks(h_all)
+        cols, off = [], 0
+        for wd in case.widths:
+            cols.extend(range(off + r * (wd // w), off + (r + 1) * (wd // w)))
+            off += wd
+        cols = np.array(cols)
+        out_c = np.ascontiguousarray(case.out0[:, cols])
+        oracle.expand(out_c, h, case.seq_slot, oracle.shard_pool_b_rows(pool, w, r),
+                      pool.scale_table)
+        col_shards = [None] * w
+        dist.all_gather_object(col_shards, (cols, out_c))
+
+        # row parallel: one slice, k_in split in two
+        rc = inputs.linear_case(4403, 39, 256, (96,), 4, 16, [16, 4, 16, 8], 32.0, p_none=0.1)
+        rpool = oracle.build_pool(rc.adapters, rc.k_in, rc.widths, 4, 16)
+        ks = rc.k_in // w
+        part, _ = oracle.shrink(np.ascontiguousarray(rc.x[:, r * ks:(r + 1) * ks]), rc.seq_slot,
+                                oracle.shard_pool_a_cols(rpool, w, r), None)
+        parts = [None] * w
+        dist.all_gather_object(parts, part)
+        hr = tp.reduce_rank_partials(torch.from_numpy(part.copy())).numpy()
+        res["reduce_is_rank_sum"] = bool(np.array_equal(hr, oracle.rank_sum(np.stack(parts))))
+        wsl = rc.widths[0] // w
+        out_r = rc.out0.copy()
+        oracle.expand(out_r, hr, rc.seq_slot, oracle.shard_pool_b_rows(rpool, w, r),
+                      rpool.scale_table, offset_start=r * wsl)
+        row_shards = [None] * w
+        dist.all_gather_object(row_shards, out_r)
+
+        if rank == 0:
+            whole = case.out0.copy()
+            oracle.delta(whole, case.x, case.seq_slot, pool)
+            res["column_equal"] = all(bool(np.array_equal(o, whole[:, c])) for c, o in col_shards)
+            res["column_cover"] = sorted(np.concatenate([c for c, _ in col_shards]).tolist()) == \
+                list(range(case.ld_out))
+            rwhole = rc.out0.copy()
+            oracle.delta(rwhole, rc.x, rc.seq_slot, rpool)
+            ok_in, ok_out = True, True
+            for p, o in enumerate(row_shards):
+                inside = np.zeros(rc.ld_out, dtype=bool)
+                inside[p * wsl:(p + 1) * wsl] = True
+                ok_out &= bool(np.array_equal(o[:, ~inside], rc.out0[:, ~inside]))
+                g = (o[:, inside].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+                f = (rwhole[:, inside].astype(np.uint32) << 16).view(np.float32).astype(
+                    np.float64)
+                ok_in &= bool(np.all(np.abs(g - f) <= 1e-2 + 1e-2 * np.abs(f)))
+            res["row_slices_close"] = ok_in
+            res["row_outside_untouched"] = ok_out
+        dist.destroy_process_group()
+        q.put((rank, res, None))
+    except Exception as e:  # reported to the parent, which fails the test
+        q.put((rank, None, repr(e)))
+
+
+def test_two_rank_tensor_parallel_forms(oracle):
+    """Column parallel: every rank's output columns equal the unsharded delta's bit
+    for bit, the gather is rank-major, the columns cover the output once.  Row
+    parallel: the all-reduce of the partials is their rank-order sum, each rank's
+    slice is within the parity tolerance of the unsharded delta, and the rest of
+    its partial-sum output is untouched."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_tp_worker, args=(r, WORLD, port, q)) for r in range(WORLD)]
+    for p in procs:
+        p.start()
+    results = {}
+    try:
+        for _ in range(WORLD):
+            rank, res, err = q.get(timeout=240)
+            assert err is None, f"rank {rank}: {err}"
+            results[rank] = res
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    for rank in range(WORLD):
+        assert results[rank]["gather_rank_major"]
+        assert results[rank]["reduce_is_rank_sum"]
+    r0 = results[0]
+    assert r0["column_equal"] and r0["column_cover"]
+    assert r0["row_slices_close"] and r0["row_outside_untouched"]

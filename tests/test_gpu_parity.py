@@ -903,3 +903,71 @@ def test_moe_w2_on_the_routing_of_w13(ld, di, oracle, full):
     assert_close(got, ref, "w2 on the routing of w13")
     keep = np.all(ref == c.y0, axis=2)
     assert keep.any() and np.array_equal(got[keep], c.y0[keep])
+
+
+# ------------------------------------------- tensor-parallel sharded forms --
+
+@pytest.mark.parametrize("tp_n", [2, 4])
+def test_tensor_parallel_forms_with_the_ranks_in_turn_on_one_gpu(ld, di, oracle, tp_n):
+    """"vllm.lora.fully_sharded_layers": the kernels of both sharded forms, each
+    rank's step run in turn on this GPU, the collective between them done by a
+    stack (the all-gather) or by adds in rank order (the all-reduce); no kernel
+    waits on another rank.  Column parallel (_mcp_apply): every rank's output
+    columns within the tolerance of the oracle's column form, which equals the
+    unsharded delta bit for bit.  Row parallel (RowParallelLinearWithShardedLoRA
+    apply): every rank's slice within the tolerance of the oracle's row form, the
+    rest of its partial-sum output untouched."""
+    from lora_delta_gb300 import tp
+    case = inputs.linear_case(141, n=300, k_in=512, widths=(256, 128), max_loras=5,
+                              max_rank=32, ranks=[32, 16, 8, 32, 24], alpha=32.0, p_none=0.1)
+    d = di.linear_to_device(case)
+    opool = oracle.build_pool(case.adapters, case.k_in, case.widths, 5, 32)
+    want, _ = oracle_delta(oracle, case)
+    shards = []
+    for p in range(tp_n):
+        h_p = torch.zeros(2, case.n, 32 // tp_n, dtype=torch.float32, device="cuda")
+        ld.lora_shrink(h_p, d.x, d.seq_slot, tp.shard_pool_a_rows(d.pool, tp_n, p))
+        shards.append(h_p)
+    h_all = torch.stack(shards)
+    routed = case.seq_slot >= 0
+    for p in range(tp_n):
+        cols = np.concatenate([np.arange(off + p * (w // tp_n), off + (p + 1) * (w // tp_n))
+                               for off, w in ((0, 256), (256, 128))])
+        out_p = d.out0[:, torch.from_numpy(cols).cuda()].contiguous()
+        pb = tp.shard_pool_b_rows(d.pool, tp_n, p)
+        ld.lora_expand_gathered(out_p, h_all, d.seq_slot, pb, scale_table=pb.scale_table)
+        got = di.bits(out_p)
+        assert_close(got, want[:, cols], f"column parallel rank {p}")
+        assert np.array_equal(got[~routed], case.out0[~routed][:, cols])
+
+    rc = inputs.linear_case(143, n=200, k_in=1024, widths=(512,), max_loras=4, max_rank=16,
+                            ranks=[16, 8, 16, 4], alpha=32.0, p_none=0.1)
+    rd = di.linear_to_device(rc)
+    rpool = oracle.build_pool(rc.adapters, rc.k_in, rc.widths, 4, 16)
+    ks, wsl = rc.k_in // tp_n, rc.widths[0] // tp_n
+    parts, oparts = [], []
+    for p in range(tp_n):
+        h_p = torch.zeros(1, rc.n, 16, dtype=torch.float32, device="cuda")
+        ld.lora_shrink(h_p, rd.x[:, p * ks:(p + 1) * ks].contiguous(), rd.seq_slot,
+                       tp.shard_pool_a_cols(rd.pool, tp_n, p))
+        parts.append(h_p)
+        oparts.append(oracle.shrink(np.ascontiguousarray(rc.x[:, p * ks:(p + 1) * ks]),
+                                    rc.seq_slot, oracle.shard_pool_a_cols(rpool, tp_n, p),
+                                    None)[0])
+    h = parts[0]
+    for h_p in parts[1:]:
+        h = h + h_p
+    oh = oracle.rank_sum(np.stack(oparts))
+    for p in range(tp_n):
+        out_p = rd.out0.clone()
+        pb = tp.shard_pool_b_rows(rd.pool, tp_n, p)
+        ld.lora_expand(out_p, h, rd.seq_slot, pb, scale_table=pb.scale_table,
+                       offset_start=p * wsl)
+        ref = rc.out0.copy()
+        oracle.expand(ref, oh, rc.seq_slot, oracle.shard_pool_b_rows(rpool, tp_n, p),
+                      rpool.scale_table, offset_start=p * wsl)
+        got = di.bits(out_p)
+        assert_close(got, ref, f"row parallel rank {p}")
+        inside = np.zeros(rc.ld_out, dtype=bool)
+        inside[p * wsl:(p + 1) * wsl] = True
+        assert np.array_equal(got[:, ~inside], rc.out0[:, ~inside])
