@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t aaddr0 = smem_addr(As + (size_t)(m0 * 16 + arow) * stride + acol);
       const uint32_t aaddr1 = smem_addr(As + (size_t)(m1 * 16 + arow) * stride + acol);
       if (has0) {
+#pragma unroll 2
         for (int ks = my_g; ks < ksteps; ks += G) {
           uint32_t b0, b1, b2, b3, a0, a1, a2, a3;
           ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
@@ -364,36 +365,45 @@ __global__ void __launch_bounds__(kThreads, 2)
               }
             }
           }
-          // fold: d[t] = C[col gq / gq + 8][rows t * 8 + 2tq, + 1]
+          // fold: d[t] = C[col gq / gq + 8][rows t * 8 + 2tq, + 1]; every staged
+          // value is read before any is written (the accesses could alias as far
+          // as the compiler knows, which would serialize each read behind the
+          // previous write)
           const int wtile = min(16, c1 - col0);
+          __nv_bfloat16* ob = Os + (col0 - cb + gq);
+          float ov[2][4];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (t >= NT) continue;
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int r = t * 8 + 2 * tq + (e & 1);
-              const int cc = gq + (e >> 1) * 8;
-              if (r < nr && cc < wtile) {
-                __nv_bfloat16* o = Os + (size_t)r * pl.o_stride + (col0 - cb + cc);
-                const float val = sc[t][e & 1] * d[t][e];
-                *o = __float2bfloat16_rn(a.add_inputs ? __bfloat162float(*o) + val : val);
-              }
+              const int r = t * 8 + 2 * tq + (e & 1), cc = (e >> 1) * 8;
+              const bool ok = t < NT && r < nr && gq + cc < wtile && a.add_inputs;
+              ov[t][e] = ok ? __bfloat162float(ob[(size_t)r * pl.o_stride + cc]) : 0.0f;
             }
-          }
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = t * 8 + 2 * tq + (e & 1), cc = (e >> 1) * 8;
+              if (t < NT && r < nr && gq + cc < wtile)
+                ob[(size_t)r * pl.o_stride + cc] =
+                    __float2bfloat16_rn(ov[t][e] + sc[t][e & 1] * d[t][e]);
+            }
         }
       }
     }
     __syncthreads();
-    // ---- the pass's out segments back to global memory (16-byte stores) ---
-    for (int j = 0; j < a.sl.S; ++j) {
-      const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
-      if (c1 <= c0 || v.ja[j] < 0) continue;
-      const int vpr = (c1 - c0) >> 3;
-      const int64_t col = a.sl.off[j] + (c0 - a.rel[j]);
-      for (int i = tid; i < nr * vpr; i += kThreads) {
-        const int r = i / vpr, c = i - r * vpr;
-        *reinterpret_cast<uint4*>(a.out + tb.out_row(prow[r]) * a.ld_out + col + c * 8) =
-            *reinterpret_cast<const uint4*>(Os + (size_t)r * pl.o_stride + (c0 - cb) + c * 8);
+    // ---- the pass's out segments back to global memory: a warp per row,
+    // 16-byte stores ------------------------------------------------------
+    for (int r = warp; r < nr; r += kWarps) {
+      __nv_bfloat16* orow = a.out + tb.out_row(prow[r]) * a.ld_out;
+      const __nv_bfloat16* srow = Os + (size_t)r * pl.o_stride - cb;
+      for (int j = 0; j < a.sl.S; ++j) {
+        const int c0 = max(cb, a.rel[j]), c1 = min(ce, a.rel[j + 1]);
+        if (c1 <= c0 || v.ja[j] < 0) continue;
+        __nv_bfloat16* dst = orow + a.sl.off[j] - a.rel[j];
+        for (int c = c0 + lane * 8; c < c1; c += 256)
+          *reinterpret_cast<uint4*>(dst + c) = *reinterpret_cast<const uint4*>(srow + c);
       }
     }
   }
