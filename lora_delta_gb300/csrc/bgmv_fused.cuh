@@ -11,10 +11,10 @@
 //   * the key's rows (own ballot scan, or the routing kernel's clusters), in
 //     passes of 16: x rows of the CTA's k share and out segments of its columns
 //     by cp.async, in separate groups, so the shrink waits for x only;
-//   * shrink on mma.sync m16n8k16 (pairs x rows x k): the warps split into G
-//     k-groups of W warps, each warp at most two 16-pair tiles, so every warp
-//     runs short independent chains; the k-group partials meet in shared
-//     memory in group order;
+//   * shrink on mma.sync m16n8k16 (pairs x rows x k): warp w owns the 16-pair
+//     tiles w and w + 8 over the CTA's whole k share, in two accumulator
+//     chains on alternate k-steps, and writes its sums straight to the
+//     buffer the cluster reads (nothing to combine inside the CTA);
 //   * the CS partials meet through distributed shared memory: each CTA reads
 //     the CS partials of its entries from its peers (all loads in flight
 //     together), sums them in rank order, and holds the whole fp32 h;
@@ -32,20 +32,14 @@ namespace lora {
 
 // Shared-memory plan (bytes) of bgmv_fused_kernel, identical on host and device.
 struct FusedPlan {
-  int rows_off, As_off, Xs_off, Bs_off, Os_off, P_off, Rx_off, H_off, total;
+  int rows_off, As_off, Xs_off, Bs_off, Os_off, Rx_off, H_off, total;
   int stride;    // elements per staged A / x row: the k share + 8 (ldmatrix conflict-free)
   int o_stride;  // elements per staged out row: the CTA's columns + 8
   int sr16;      // S * R rounded up to 16
-  int wm, G;     // warps per k-group (each takes <= 2 pair tiles) and k-groups
 };
 __host__ __device__ inline FusedPlan fused_plan(const DeltaArgs& a) {
   FusedPlan p;
   p.sr16 = (a.sr_max + 15) / 16 * 16;
-  const int mt = p.sr16 / 16;
-  int wm = 1;
-  while (wm < kWarps && wm * 2 < mt) wm *= 2;
-  p.wm = wm;
-  p.G = kWarps / wm;
   p.stride = a.kc + 8;
   p.o_stride = a.cpc + 8;
   int o = 128;  // the pass's row ids (16 ints) at offset 64
@@ -62,8 +56,6 @@ __host__ __device__ inline FusedPlan fused_plan(const DeltaArgs& a) {
   p.Os_off = o;
   o += kRowsPerPass * p.o_stride * 2;
   o = (o + 127) / 128 * 128;
-  p.P_off = o;  // k-group partials [G][sr16][16 rows]
-  o += p.G * p.sr16 * kRowsPerPass * 4;
   p.Rx_off = o;  // this CTA's partial h, read by the cluster: [16 rows][sr16]
   o += kRowsPerPass * p.sr16 * 4;
   p.H_off = o;   // the pass's h [16 rows][sr16]
@@ -73,7 +65,7 @@ __host__ __device__ inline FusedPlan fused_plan(const DeltaArgs& a) {
 }
 
 // Shapes the kernel takes: one k stage per CTA (kst == kc), R a multiple of
-// 16 up to 64, S * R up to 256.
+// 16 up to 64, S * R up to 256 (at most two 16-pair tiles per warp).
 inline bool fused_kernel_fits(const DeltaArgs& a) {
   return a.nbuf == 1 && a.kst == a.kc && a.R % 16 == 0 && a.R <= 64 && a.sr_max <= 256;
 }
@@ -97,7 +89,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   __nv_bfloat16* Xs = reinterpret_cast<__nv_bfloat16*>(smem + pl.Xs_off);
   __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(smem + pl.Bs_off);
   __nv_bfloat16* Os = reinterpret_cast<__nv_bfloat16*>(smem + pl.Os_off);
-  float* P = reinterpret_cast<float*>(smem + pl.P_off);
   float* Rx = reinterpret_cast<float*>(smem + pl.Rx_off);
   float* H = reinterpret_cast<float*>(smem + pl.H_off);
   const int stride = pl.stride, SR16 = pl.sr16;
@@ -176,11 +167,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int i = tid; i < SR16; i += kThreads)
       *reinterpret_cast<uint4*>(As + (size_t)i * stride + kw) = make_uint4(0, 0, 0, 0);
 
-  // shrink split: G k-groups of wm warps; warp (g, sub) takes pair tiles
-  // sub, sub + wm (at most two) and the k-steps g, g + G, ...
-  const int mt = (SRa + 15) / 16;
-  const int G = pl.G, wm = pl.wm;
-  const int my_g = warp / wm, my_sub = warp - my_g * wm;
+  const int mt = (SRa + 15) / 16;  // 16-pair tiles of the shrink (<= 16: two per warp)
   const int ksteps = (kw + 15) / 16;
   const int ng = (SRa >> 2);  // 4-pair groups per row (SRa is a multiple of 16)
 
@@ -199,70 +186,62 @@ __global__ void __launch_bounds__(kThreads, 2)
     cp_async_wait<1>();  // weights and x rows landed (the out segments may still fly)
     __syncthreads();
 
-    // ---- shrink: partial P[g][pair][row] over this CTA's k share ----------
+    // ---- shrink: warp w owns pair tiles w and w + 8 over the whole k share,
+    // each in two accumulator chains on alternate k-steps (no partials to
+    // combine inside the CTA); the sums are this CTA's partial of h, written
+    // straight to Rx[row][pair] for the cluster ------------------------------
+    if (p0 > 0) cluster_wait();  // the previous pass's readers are done with Rx
     {
-      float acc[2][2][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[i][t][e] = 0.0f;
       const bool two_n = nr > 8;  // (uniform) rows 8..15 exist
-      const int m0 = my_sub, m1 = my_sub + wm;
-      const bool has0 = m0 < mt, has1 = m1 < mt;
       const uint32_t xaddr = smem_addr(Xs + (size_t)(((lane >> 4) << 3) + (lane & 7)) * stride +
                                        ((lane >> 3) & 1) * 8);
       const uint32_t arow = (uint32_t)((((lane >> 3) & 1) << 3) + (lane & 7));
       const uint32_t acol = (uint32_t)((lane >> 4) << 3);
-      const uint32_t aaddr0 = smem_addr(As + (size_t)(m0 * 16 + arow) * stride + acol);
-      const uint32_t aaddr1 = smem_addr(As + (size_t)(m1 * 16 + arow) * stride + acol);
-      if (has0) {
-#pragma unroll 2
-        for (int ks = my_g; ks < ksteps; ks += G) {
-          uint32_t b0, b1, b2, b3, a0, a1, a2, a3;
-          ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
-          ldsm_x4(aaddr0 + ks * 32, a0, a1, a2, a3);
-          mma_16816(acc[0][0], a0, a1, a2, a3, b0, b1);
-          if (two_n) mma_16816(acc[0][1], a0, a1, a2, a3, b2, b3);
-          if (has1) {
-            ldsm_x4(aaddr1 + ks * 32, a0, a1, a2, a3);
-            mma_16816(acc[1][0], a0, a1, a2, a3, b0, b1);
-            if (two_n) mma_16816(acc[1][1], a0, a1, a2, a3, b2, b3);
-          }
-        }
-      }
-      // (every warp stores, zeros where it has no tile or no k-step, so the
-      // group sum below never reads an unwritten entry)
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int m = i == 0 ? m0 : m1;
-        if (m * 16 >= SR16) continue;
+        const int m = warp + i * kWarps;
+        if (m >= mt) break;  // (uniform)
+        const uint32_t aaddr = smem_addr(As + (size_t)(m * 16 + arow) * stride + acol);
+        float acc[2][2][4];  // [chain][row tile][fragment]
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[c][t][e] = 0.0f;
+        int ks = 0;
+        for (; ks + 1 < ksteps; ks += 2) {
+          uint32_t b0, b1, b2, b3, a0, a1, a2, a3, c0, c1, c2, c3, d0, d1, d2, d3;
+          ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+          ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
+          ldsm_x4(xaddr + (ks + 1) * 32, c0, c1, c2, c3);
+          ldsm_x4(aaddr + (ks + 1) * 32, d0, d1, d2, d3);
+          mma_16816(acc[0][0], a0, a1, a2, a3, b0, b1);
+          mma_16816(acc[1][0], d0, d1, d2, d3, c0, c1);
+          if (two_n) {
+            mma_16816(acc[0][1], a0, a1, a2, a3, b2, b3);
+            mma_16816(acc[1][1], d0, d1, d2, d3, c2, c3);
+          }
+        }
+        if (ks < ksteps) {
+          uint32_t b0, b1, b2, b3, a0, a1, a2, a3;
+          ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+          ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
+          mma_16816(acc[0][0], a0, a1, a2, a3, b0, b1);
+          if (two_n) mma_16816(acc[0][1], a0, a1, a2, a3, b2, b3);
+        }
+        // C[pair m*16 + gq (+8)][row t*8 + 2tq (+1)] -> Rx[row][pair]
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          float* base = P + ((size_t)my_g * SR16 + m * 16 + gq) * kRowsPerPass + t * 8 + 2 * tq;
-          base[0] = acc[i][t][0];
-          base[1] = acc[i][t][1];
-          base[8 * kRowsPerPass] = acc[i][t][2];
-          base[8 * kRowsPerPass + 1] = acc[i][t][3];
+          float* rx = Rx + (t * 8 + 2 * tq) * SR16 + m * 16 + gq;
+          rx[0] = acc[0][t][0] + acc[1][t][0];
+          rx[SR16] = acc[0][t][1] + acc[1][t][1];
+          rx[8] = acc[0][t][2] + acc[1][t][2];
+          rx[SR16 + 8] = acc[0][t][3] + acc[1][t][3];
         }
       }
     }
-    __syncthreads();
-    // ---- the k-group partials summed in group order -> Rx[row][pair] --------
-    if (p0 > 0) cluster_wait();  // the previous pass's readers are done with Rx
-    for (int e = tid; e < nr * ng; e += kThreads) {
-      const int r = e / ng, p = (e - r * ng) * 4;
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int g = 0; g < G; ++g) {
-        const float* src = P + ((size_t)g * SR16 + p) * kRowsPerPass + r;
-        s.x += src[0];
-        s.y += src[kRowsPerPass];
-        s.z += src[2 * kRowsPerPass];
-        s.w += src[3 * kRowsPerPass];
-      }
-      *reinterpret_cast<float4*>(Rx + r * SR16 + p) = s;
-    }
+    __syncthreads();  // (the whole CTA's partial is in Rx before the release)
     cluster_arrive_release_smem();  // partials in place
     cluster_wait();
     // ---- the cluster's partials: 4 lanes per 4-entry group; lane qq reads
