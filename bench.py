@@ -288,6 +288,10 @@ def run_ours(args, rank, world):
                 "algorithmic_bytes_per_launch": abytes,
                 "kernel": "delta_cluster_kernel<16,fused,LinearTables>"}
 
+    # the data-movement floor of this launch shape: the same bytes, grid,
+    # cluster size and programmatic dependent launch, no arithmetic
+    floor = decode_floor(ld, bufs, copies, K, stream, device, abytes, hbm_peak, ms_step)
+
     # eager (no graph) timing of the same K steps, for context
     ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -310,6 +314,7 @@ def run_ours(args, rank, world):
               f"({copies * per_copy / 2**20:.0f} MiB > 2x L2)",
         "timing": "one CUDA graph of K steps, CUDA events on the launching stream",
         "roofline": roofline,
+        "decode_floor": floor,
         "eager_ms_per_step": round(eager_ms, 6),
         "e2e": e2e,
         "gpu_launches": K,
@@ -322,6 +327,41 @@ def run_ours(args, rank, world):
                                                       bf16_peak, peak_src)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def decode_floor(ld, bufs, copies, K, stream, device, abytes, hbm_peak, ms_step):
+    """K steps of lora_delta_fused_floor (the fused call's bytes and launch plan,
+    no arithmetic) as one CUDA graph on the same rotating buffers."""
+    import torch
+    step = lambda k: ld.lora_delta_fused_floor(bufs[k % copies]["out"], bufs[k % copies]["x"],
+                                               bufs[k % copies]["seq"], bufs[k % copies]["pool"])
+    with torch.cuda.stream(stream):
+        for k in range(copies):
+            step(k)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(K):
+            step(k)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / K
+    gbs = abytes / (ms / 1e3) / 1e9
+    return {"ms_per_step": round(ms, 6), "GB_per_s": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm_peak, 4),
+            "kernel_frac_of_floor": round(ms / ms_step, 4),
+            "what": "lora_delta_fused_floor: the decode step's bytes (A/B shares, x and out "
+                    "rows, out written back) with the same grid, cluster size, shared-memory "
+                    "plan and programmatic dependent launch, no arithmetic; K steps in one "
+                    "CUDA graph on the same rotating buffers"}
 
 
 def run_e2e(ld, di, case, bufs, copies, K, W, device):

@@ -354,6 +354,24 @@ int lora_moe_w2_delta_routed(void *y, const void *x, const int64_t *w_ptr_a, int
                              uint32_t *err_word, lora_stream_t stream);
 
 /*
+ * lora_delta_fused_floor -- a measurement aid, not part of the method (none of
+ * the pages has it): moves the bytes that lora_delta_fused moves for a small
+ * batch -- every routed slot's A and B (each CTA's share), the slot's x rows
+ * and out rows, out written back -- with the same launch plan (grid, thread-
+ * block cluster size, shared-memory plan, programmatic dependent launch), but
+ * computes nothing: out is written back unchanged.  Timed next to
+ * lora_delta_fused on the same inputs, it gives the data-movement floor of a
+ * decode step in this launch shape.  Arguments as lora_delta_fused without
+ * scale table, add_inputs, workspace and error word; LORA_ERR_UNSUPPORTED
+ * unless n <= 1024 and the shape takes the fused small-segment kernel (one k
+ * stage per CTA, R a multiple of 16 up to 64, S * R <= 256).
+ */
+int lora_delta_fused_floor(void *out, int64_t ld_out, const void *x, int n, int k_in,
+                           const int32_t *seq_slot, const uint64_t *a_table,
+                           const uint64_t *b_table, const int32_t *widths, int S, int R,
+                           int max_loras, int offset_start, lora_stream_t stream);
+
+/*
  * lora_delta_fused_noalloc -- lora_delta_fused for callers that cannot
  * allocate device memory.  The pages have no counterpart to this call: it
  * exists for callers whose memory is fixed up front (a budget set at start

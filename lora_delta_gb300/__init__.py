@@ -25,7 +25,7 @@ __all__ = [
     "lora_workspace_size", "lora_workspace_min_size", "lora_route", "lora_route_scratch_size",
     "lora_route_with_scratch", "lora_shrink", "lora_expand", "lora_expand_gathered",
     "lora_delta_fused",
-    "lora_delta_segmented",
+    "lora_delta_segmented", "lora_delta_fused_floor",
     "lora_moe_workspace_size", "lora_moe_fc1_delta", "lora_moe_w13_delta",
     "lora_moe_w2_delta", "lora_moe_w2_delta_routed", "lora_get_error", "new_error_word",
     "lora_delta_fused_noalloc", "lora_noalloc_scratch_bytes", "lora_set_wait_limit_ns",
@@ -306,6 +306,20 @@ def lora_delta_fused(out, x, seq_slot, pool: LoraPool, offset_start: int = 0,
         _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
         _ptr(pool.b_table), _ptr(st), w, pool.S, pool.R, pool.max_loras, int(offset_start),
         int(bool(add_inputs)), _ptr(ws), wsb, _ptr(err), _stream(stream)))
+
+
+def lora_delta_fused_floor(out, x, seq_slot, pool: LoraPool, offset_start: int = 0, stream=None):
+    """Measurement aid: the bytes and launch plan of ``lora_delta_fused`` on a small
+    batch with no arithmetic (``out`` is written back unchanged)."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(x, "x", torch.bfloat16)
+    _dev(seq_slot, "seq_slot", torch.int32)
+    n, k_in = x.shape
+    w = _widths_arg(pool.widths)
+    _check("lora_delta_fused_floor", lib().lora_delta_fused_floor(
+        _ptr(out), out.shape[1], _ptr(x), n, k_in, _ptr(seq_slot), _ptr(pool.a_table),
+        _ptr(pool.b_table), w, pool.S, pool.R, pool.max_loras, int(offset_start),
+        _stream(stream)))
 
 
 def lora_delta_segmented(out, x, seg_start, pool: LoraPool, offset_start: int = 0,

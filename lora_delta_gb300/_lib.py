@@ -38,6 +38,8 @@ SIGNATURES = {
                               _i, _vp, _sz, _vp, _vp]),
     "lora_delta_segmented": (_i, [_vp, _i64, _vp, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i,
                                   _i, _i, _vp, _sz, _vp, _vp]),
+    "lora_delta_fused_floor": (_i, [_vp, _i64, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                                    _vp]),
     "lora_moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "lora_moe_fc1_delta": (_i, [_vp, _vp, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i, _i, _i, _i, _i,
                                 _i, _i, _f, _vp, _sz, _vp, _vp]),

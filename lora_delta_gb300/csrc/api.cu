@@ -11,6 +11,7 @@
 
 #include "bgmv.cuh"
 #include "bgmv_fused.cuh"
+#include "floor.cuh"
 #include "common.cuh"
 #include "keyed.cuh"
 #include "lora_delta.h"
@@ -902,6 +903,57 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
   rc = launch_delta<kModeFused>(a, tb, max_loras, (cudaStream_t)stream);
   if (rc || !sgmv) return rc;
   return launch_sgmv(a, tb, w, max_loras, thr, (cudaStream_t)stream);
+}
+
+int lora_delta_fused_floor(void* out, int64_t ld_out, const void* x, int n, int k_in,
+                           const int32_t* seq_slot, const uint64_t* a_table,
+                           const uint64_t* b_table, const int32_t* widths, int S, int R,
+                           int max_loras, int offset_start, lora_stream_t stream) {
+  if (n < 0 || k_in < 0) return LORA_ERR_ARG;
+  if (n == 0) return LORA_OK;
+  if (!out || !x || !seq_slot || !a_table || !b_table) return LORA_ERR_ARG;
+  int rc = check_max_loras(max_loras);
+  if (rc) return rc;
+  DeltaArgs a = {};
+  if ((rc = make_slices(widths, S, offset_start, a.sl, a.rel))) return rc;
+  if ((rc = check_rank(S, R))) return rc;
+  if (ld_out < (int64_t)offset_start + a.sl.n_cols) return LORA_ERR_SHAPE;
+  if (k_in % 8 || ld_out % 8 || !aligned16(out) || !aligned16(x)) return LORA_ERR_ALIGN;
+  if (a.sl.n_cols == 0) return LORA_OK;
+  if (n > kInlineRowsMax) return LORA_ERR_UNSUPPORTED;  // (rows found by the kernel's own scan)
+  a.out = (__nv_bfloat16*)out;
+  a.ld_out = ld_out;
+  a.x = (const __nv_bfloat16*)x;
+  a.ld_x = k_in;
+  a.k_in = k_in;
+  a.R = R;
+  a.add_inputs = 1;
+  a.sr_max = S * R;
+  rc = prepare_rows(a, seq_slot, n, max_loras, (S * R + 15) / 16 * 16, nullptr, 0, nullptr,
+                    (cudaStream_t)stream, nullptr);
+  if (rc) return rc;
+  plan_tiles(a, k_in, a.sl.n_cols, a.sr_max, kModeFused);
+  if (!fused_kernel_fits(a)) return LORA_ERR_UNSUPPORTED;
+  const int smem = fused_plan(a).total;
+  if (smem > 226 * 1024) return LORA_ERR_UNSUPPORTED;
+  LinearTables tb{a_table, b_table, nullptr, max_loras};
+  auto kernel = bgmv_floor_kernel;
+  if (prepare_kernel(kernel, smem, a.cs > 8) != cudaSuccess) return LORA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(max_loras * a.cs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl() ? 2 : 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, a, tb));
 }
 
 size_t lora_moe_workspace_size(int T, int top_k, int E, int num_loras, int rank, int shared_a) {

@@ -9,7 +9,7 @@
 //     B rows of its 1/CS of the output columns start streaming into shared
 //     memory (adapter weights are never written by the preceding kernel);
 //   * the key's rows (own ballot scan, or the routing kernel's clusters), in
-//     passes of 16: x rows of the CTA's k share and out segments of its columns
+//     passes of 8: x rows of the CTA's k share and out segments of its columns
 //     by cp.async, in separate groups, so the shrink waits for x only;
 //   * shrink on mma.sync m16n8k16 (pairs x rows x k): warp w owns the 16-pair
 //     tiles w and w + 8 over the CTA's whole k share, in two accumulator
@@ -30,6 +30,8 @@
 
 namespace lora {
 
+constexpr int kFusedRows = 8;  // rows of one pass: one 8-row MMA tile
+
 // Shared-memory plan (bytes) of bgmv_fused_kernel, identical on host and device.
 struct FusedPlan {
   int rows_off, As_off, Xs_off, Bs_off, Os_off, Rx_off, H_off, total;
@@ -42,24 +44,24 @@ __host__ __device__ inline FusedPlan fused_plan(const DeltaArgs& a) {
   p.sr16 = (a.sr_max + 15) / 16 * 16;
   p.stride = a.kc + 8;
   p.o_stride = a.cpc + 8;
-  int o = 128;  // the pass's row ids (16 ints) at offset 64
+  int o = 128;  // the pass's row ids (8 ints) at offset 64
   p.rows_off = o;
   o += ((a.row_cap * 4 + 127) / 128) * 128;
   p.As_off = o;
   o += p.sr16 * p.stride * 2;
   p.Xs_off = o;
-  o += kRowsPerPass * p.stride * 2;
+  o += kFusedRows * p.stride * 2;
   o = (o + 127) / 128 * 128;
   p.Bs_off = o;  // the CTA's B rows [cpc][R], + 16 rows of slack (read by a half tile)
   o += (a.cpc + 16) * a.R * 2;
   o = (o + 127) / 128 * 128;
   p.Os_off = o;
-  o += kRowsPerPass * p.o_stride * 2;
+  o += kFusedRows * p.o_stride * 2;
   o = (o + 127) / 128 * 128;
-  p.Rx_off = o;  // this CTA's partial h, read by the cluster: [16 rows][sr16]
-  o += kRowsPerPass * p.sr16 * 4;
-  p.H_off = o;   // the pass's h [16 rows][sr16]
-  o += kRowsPerPass * p.sr16 * 4;
+  p.Rx_off = o;  // this CTA's partial h, read by the cluster: [8 rows][sr16]
+  o += kFusedRows * p.sr16 * 4;
+  p.H_off = o;   // the pass's h [8 rows][sr16]
+  o += kFusedRows * p.sr16 * 4;
   p.total = o;
   return p;
 }
@@ -171,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int ksteps = (kw + 15) / 16;
   const int ng = (SRa >> 2);  // 4-pair groups per row (SRa is a multiple of 16)
 
-  for (int p0 = 0; p0 < nrows; p0 += kRowsPerPass) {
-    const int nr = min(kRowsPerPass, nrows - p0);
+  for (int p0 = 0; p0 < nrows; p0 += kFusedRows) {
+    const int nr = min(kFusedRows, nrows - p0);
     if (p0 > 0) __syncthreads();  // the previous pass is done with prow, Xs and Os
     if (tid < nr) prow[tid] = rows[p0 + tid];
     __syncthreads();
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (a.add_inputs) copy_out_rows(a, tb, v, prow, nr, cb, ce, Os, pl.o_stride, tid);
     cp_async_commit();  // group: out segments (waited for before the expand)
     if (kw & 15)
-      for (int i = tid; i < kRowsPerPass; i += kThreads)
+      for (int i = tid; i < kFusedRows; i += kThreads)
         *reinterpret_cast<uint4*>(Xs + (size_t)i * stride + kw) = make_uint4(0, 0, 0, 0);
     cp_async_wait<1>();  // weights and x rows landed (the out segments may still fly)
     __syncthreads();
@@ -192,9 +194,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     // straight to Rx[row][pair] for the cluster ------------------------------
     if (p0 > 0) cluster_wait();  // the previous pass's readers are done with Rx
     {
-      const bool two_n = nr > 8;  // (uniform) rows 8..15 exist
-      const uint32_t xaddr = smem_addr(Xs + (size_t)(((lane >> 4) << 3) + (lane & 7)) * stride +
-                                       ((lane >> 3) & 1) * 8);
+      // x fragments (rows 0..7 of the pass, k halves) by ldmatrix.x2 (lanes
+      // 0-15); A fragments (16 pairs) by ldmatrix.x4
+      const uint32_t xaddr = smem_addr(Xs + (size_t)(lane & 7) * stride + ((lane >> 3) & 1) * 8);
       const uint32_t arow = (uint32_t)((((lane >> 3) & 1) << 3) + (lane & 7));
       const uint32_t acol = (uint32_t)((lane >> 4) << 3);
 #pragma unroll
@@ -202,43 +204,33 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int m = warp + i * kWarps;
         if (m >= mt) break;  // (uniform)
         const uint32_t aaddr = smem_addr(As + (size_t)(m * 16 + arow) * stride + acol);
-        float acc[2][2][4];  // [chain][row tile][fragment]
+        float acc[2][4];  // [chain][fragment]
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[c][t][e] = 0.0f;
+          for (int e = 0; e < 4; ++e) acc[c][e] = 0.0f;
         int ks = 0;
         for (; ks + 1 < ksteps; ks += 2) {
-          uint32_t b0, b1, b2, b3, a0, a1, a2, a3, c0, c1, c2, c3, d0, d1, d2, d3;
-          ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+          uint32_t b0, b1, c0, c1, a0, a1, a2, a3, d0, d1, d2, d3;
+          ldsm_x2(xaddr + ks * 32, b0, b1);
           ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
-          ldsm_x4(xaddr + (ks + 1) * 32, c0, c1, c2, c3);
+          ldsm_x2(xaddr + (ks + 1) * 32, c0, c1);
           ldsm_x4(aaddr + (ks + 1) * 32, d0, d1, d2, d3);
-          mma_16816(acc[0][0], a0, a1, a2, a3, b0, b1);
-          mma_16816(acc[1][0], d0, d1, d2, d3, c0, c1);
-          if (two_n) {
-            mma_16816(acc[0][1], a0, a1, a2, a3, b2, b3);
-            mma_16816(acc[1][1], d0, d1, d2, d3, c2, c3);
-          }
+          mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
+          mma_16816(acc[1], d0, d1, d2, d3, c0, c1);
         }
         if (ks < ksteps) {
-          uint32_t b0, b1, b2, b3, a0, a1, a2, a3;
-          ldsm_x4(xaddr + ks * 32, b0, b1, b2, b3);
+          uint32_t b0, b1, a0, a1, a2, a3;
+          ldsm_x2(xaddr + ks * 32, b0, b1);
           ldsm_x4(aaddr + ks * 32, a0, a1, a2, a3);
-          mma_16816(acc[0][0], a0, a1, a2, a3, b0, b1);
-          if (two_n) mma_16816(acc[0][1], a0, a1, a2, a3, b2, b3);
+          mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
         }
-        // C[pair m*16 + gq (+8)][row t*8 + 2tq (+1)] -> Rx[row][pair]
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          float* rx = Rx + (t * 8 + 2 * tq) * SR16 + m * 16 + gq;
-          rx[0] = acc[0][t][0] + acc[1][t][0];
-          rx[SR16] = acc[0][t][1] + acc[1][t][1];
-          rx[8] = acc[0][t][2] + acc[1][t][2];
-          rx[SR16 + 8] = acc[0][t][3] + acc[1][t][3];
-        }
+        // C[pair m*16 + gq (+8)][row 2tq (+1)] -> Rx[row][pair]
+        float* rx = Rx + (2 * tq) * SR16 + m * 16 + gq;
+        rx[0] = acc[0][0] + acc[1][0];
+        rx[SR16] = acc[0][1] + acc[1][1];
+        rx[8] = acc[0][2] + acc[1][2];
+        rx[SR16 + 8] = acc[0][3] + acc[1][3];
       }
     }
     __syncthreads();  // (the whole CTA's partial is in Rx before the release)
@@ -288,16 +280,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     {
       constexpr int KS = RMAX / 16;
       const int ks_n = R / 16;
-      const int NT = nr > 8 ? 2 : 1;
-      // this thread's rows (2tq, 2tq + 1 of each 8-row tile) and their scales
-      float sc[2][2];
+      // this thread's rows (2tq, 2tq + 1) and their scales
+      float sc[2];
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int r = t * 8 + 2 * tq + e;
-          sc[t][e] = r < nr ? v.scale * tb.row_weight(prow[r]) : 0.0f;
-        }
+      for (int e = 0; e < 2; ++e) {
+        const int r = 2 * tq + e;
+        sc[e] = r < nr ? v.scale * tb.row_weight(prow[r]) : 0.0f;
+      }
       // tiles of every active slice's part of [cb, ce), 16 columns each (the
       // last of a slice may be 8 wide), dealt to the warps in turn
       int tile_base = 0;
@@ -309,65 +298,49 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int t_first = ((warp - tile_base) % kWarps + kWarps) % kWarps;
         tile_base += ntl;
         if (t_first >= ntl) continue;
-        // B operand: h of this slice, rows gq (+8) of the tile, as bf16 (hi, lo)
-        uint32_t bhi[KS][2][2], blo[KS][2][2];
+        // B operand: h of this slice, row gq of the pass, as bf16 (hi, lo)
+        uint32_t bhi[KS][2], blo[KS][2];
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk)
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int r = t * 8 + gq;
-            const bool ok = kk < ks_n && r < nr;
-            const float* hp = H + r * SR16 + ja * R + kk * 16 + 2 * tq;
-            split_bf16x2(ok ? hp[0] : 0.f, ok ? hp[1] : 0.f, bhi[kk][t][0], blo[kk][t][0]);
-            split_bf16x2(ok ? hp[8] : 0.f, ok ? hp[9] : 0.f, bhi[kk][t][1], blo[kk][t][1]);
-          }
+        for (int kk = 0; kk < KS; ++kk) {
+          const bool ok = kk < ks_n && gq < nr;
+          const float* hp = H + gq * SR16 + ja * R + kk * 16 + 2 * tq;
+          split_bf16x2(ok ? hp[0] : 0.f, ok ? hp[1] : 0.f, bhi[kk][0], blo[kk][0]);
+          split_bf16x2(ok ? hp[8] : 0.f, ok ? hp[9] : 0.f, bhi[kk][1], blo[kk][1]);
+        }
         const uint32_t brow = (uint32_t)((((lane >> 3) & 1) << 3) + (lane & 7));
         const uint32_t bcol = (uint32_t)((lane >> 4) << 3);
         for (int t = t_first; t < ntl; t += kWarps) {
           const int col0 = c0 + t * 16;  // first column of the tile (CTA-relative: - cb)
           const uint32_t baddr = smem_addr(Bs + (size_t)(col0 - cb + brow) * R + bcol);
-          float d[2][4];
-#pragma unroll
-          for (int u = 0; u < 2; ++u)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) d[u][e] = 0.0f;
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < KS; ++kk) {
             if (kk < ks_n) {
               uint32_t a0, a1, a2, a3;
               ldsm_x4(baddr + kk * 32, a0, a1, a2, a3);
-              mma_16816(d[0], a0, a1, a2, a3, bhi[kk][0][0], bhi[kk][0][1]);
-              mma_16816(d[0], a0, a1, a2, a3, blo[kk][0][0], blo[kk][0][1]);
-              if (NT > 1) {
-                mma_16816(d[1], a0, a1, a2, a3, bhi[kk][1][0], bhi[kk][1][1]);
-                mma_16816(d[1], a0, a1, a2, a3, blo[kk][1][0], blo[kk][1][1]);
-              }
+              mma_16816(d, a0, a1, a2, a3, bhi[kk][0], bhi[kk][1]);
+              mma_16816(d, a0, a1, a2, a3, blo[kk][0], blo[kk][1]);
             }
           }
-          // fold: d[t] = C[col gq / gq + 8][rows t * 8 + 2tq, + 1]; every staged
-          // value is read before any is written (the accesses could alias as far
-          // as the compiler knows, which would serialize each read behind the
+          // fold: d = C[col gq / gq + 8][rows 2tq, 2tq + 1]; every staged value
+          // is read before any is written (the accesses could alias as far as
+          // the compiler knows, which would serialize each read behind the
           // previous write)
           const int wtile = min(16, c1 - col0);
           __nv_bfloat16* ob = Os + (col0 - cb + gq);
-          float ov[2][4];
+          float ov[4];
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
+          for (int e = 0; e < 4; ++e) {
+            const int r = 2 * tq + (e & 1), cc = (e >> 1) * 8;
+            const bool ok = r < nr && gq + cc < wtile && a.add_inputs;
+            ov[e] = ok ? __bfloat162float(ob[(size_t)r * pl.o_stride + cc]) : 0.0f;
+          }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int r = t * 8 + 2 * tq + (e & 1), cc = (e >> 1) * 8;
-              const bool ok = t < NT && r < nr && gq + cc < wtile && a.add_inputs;
-              ov[t][e] = ok ? __bfloat162float(ob[(size_t)r * pl.o_stride + cc]) : 0.0f;
-            }
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int r = t * 8 + 2 * tq + (e & 1), cc = (e >> 1) * 8;
-              if (t < NT && r < nr && gq + cc < wtile)
-                ob[(size_t)r * pl.o_stride + cc] =
-                    __float2bfloat16_rn(ov[t][e] + sc[t][e & 1] * d[t][e]);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int r = 2 * tq + (e & 1), cc = (e >> 1) * 8;
+            if (r < nr && gq + cc < wtile)
+              ob[(size_t)r * pl.o_stride + cc] = __float2bfloat16_rn(ov[e] + sc[e & 1] * d[e]);
+          }
         }
       }
     }

@@ -38,13 +38,6 @@ constexpr int kKeyStages = 5;             // ring depth
 constexpr int kKeyStride = kKeyKC + 8;    // padded row (elements): ldmatrix conflict-free
 constexpr int kKeyMaxSR = 64;             // largest S * R (rounded to 16) this kernel takes
 
-// ldmatrix of two 8x8 b16 matrices (lanes 0-15 give the row addresses).
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-
 // 16-byte asynchronous global -> shared copy to a shared-window address.
 __device__ __forceinline__ void cp_async16_s(uint32_t saddr, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gsrc) : "memory");
