@@ -50,8 +50,8 @@ def load_peaks():
 # with the hash of the sources it was taken on: reported only while they are
 # unchanged, null otherwise.
 DECODE_TRAFFIC = {"bytes": 10652160, "sources_sha256_16": "ac08fb373e1f02b3"}
-DECODE_SOURCES = ("lora_delta_gb300/csrc/bgmv.cuh", "lora_delta_gb300/csrc/common.cuh",
-                  "lora_delta_gb300/csrc/api.cu")
+DECODE_SOURCES = ("lora_delta_gb300/csrc/bgmv.cuh", "lora_delta_gb300/csrc/bgmv_fused.cuh",
+                  "lora_delta_gb300/csrc/common.cuh", "lora_delta_gb300/csrc/api.cu")
 
 
 def decode_traffic():
@@ -286,7 +286,7 @@ def run_ours(args, rank, world):
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "traffic": decode_traffic(), "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": abytes,
-                "kernel": "delta_cluster_kernel<16,fused,LinearTables>"}
+                "kernel": "bgmv_fused_kernel<16,LinearTables>"}
 
     # the data-movement floor of this launch shape: the same bytes, grid,
     # cluster size and programmatic dependent launch, no arithmetic

@@ -73,7 +73,7 @@ inline bool fused_kernel_fits(const DeltaArgs& a) {
 }
 
 template <int RMAX, class Tables>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     bgmv_fused_kernel(const DeltaArgs a, const Tables tb) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ SlotView v;

@@ -13,7 +13,7 @@
 
 namespace lora {
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     bgmv_floor_kernel(const DeltaArgs a, const LinearTables tb) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ SlotView v;
