@@ -16,8 +16,9 @@
 //     chains on alternate k-steps, and writes its sums straight to the
 //     buffer the cluster reads (nothing to combine inside the CTA);
 //   * the CS partials meet through distributed shared memory: each CTA reads
-//     the CS partials of its entries from its peers (all loads in flight
-//     together), sums them in rank order, and holds the whole fp32 h;
+//     the CS partials of every entry of the pass from its peers in one round
+//     (all loads in flight together), sums them in a fixed order, and holds
+//     the whole fp32 h;
 //   * expand + fold on mma.sync with M = 16 output columns (B rows by
 //     ldmatrix) and N = 8 rows (h as a bf16 (hi, lo) pair, so the rank
 //     contraction keeps ~fp32 accuracy); each product is folded into the
@@ -236,34 +237,37 @@ __global__ void __launch_bounds__(kThreads, 3)
     __syncthreads();  // (the whole CTA's partial is in Rx before the release)
     cluster_arrive_release_smem();  // partials in place
     cluster_wait();
-    // ---- the cluster's partials: 4 lanes per 4-entry group; lane qq reads
-    // peers qq, qq + 4, qq + 8, qq + 12 (all in flight together), then two
-    // xor-shuffles add the lanes in the same order in every CTA ------------
+    // ---- the cluster's partials: lg lanes per 4-entry group (4, or 2 when
+    // the pass's groups would not fit one round of 4), lane qq reading peers
+    // qq, qq + lg, ... (all in flight together), then xor-shuffles add the
+    // lanes: the same summation order in every CTA ------------------------
     {
       const uint32_t rx_addr = smem_addr(Rx);
-      const int ngrp = nr * ng, qq = lane & 3;
-      for (int gb = (tid >> 2); gb - (lane >> 2) < ngrp; gb += kThreads / 4) {
+      const int ngrp = nr * ng;
+      const int lg = ngrp * 4 <= kThreads ? 4 : 2;  // (uniform)
+      const int gpr = kThreads / lg, qq = lane & (lg - 1);
+      for (int gb0 = 0; gb0 < ngrp; gb0 += gpr) {  // (uniform rounds)
+        const int gb = gb0 + tid / lg;
         const bool valid = gb < ngrp;  // (the warp's lanes stay together)
         const int e = valid ? gb : 0;
         const int r = e / ng, p = (e - r * ng) * 4;
         const uint32_t addr = rx_addr + 4u * (uint32_t)(r * SR16 + p);
-        float4 part[4];
+        float4 part[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = qq + 4 * u;
+        for (int u = 0; u < 8; ++u) {
+          const int c = qq + lg * u;
           part[u] = (valid && c < ncta) ? dsmem_ld_f32x4(dsmem_map(addr, (uint32_t)c))
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float4 hv = part[0];
 #pragma unroll
-        for (int u = 1; u < 4; ++u) {
+        for (int u = 1; u < 8; ++u) {
           hv.x += part[u].x;
           hv.y += part[u].y;
           hv.z += part[u].z;
           hv.w += part[u].w;
         }
-#pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
+        for (int off = 1; off < lg; off <<= 1) {
           hv.x += __shfl_xor_sync(0xffffffffu, hv.x, off);
           hv.y += __shfl_xor_sync(0xffffffffu, hv.y, off);
           hv.z += __shfl_xor_sync(0xffffffffu, hv.z, off);
