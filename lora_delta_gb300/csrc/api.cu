@@ -307,7 +307,11 @@ int launch_key(const DeltaArgs& a, const Tables& tb, int n_keys, int zero_ctas,
   auto kernel = a.R <= 16 ? delta_key_kernel<16, Tables> : delta_key_kernel<32, Tables>;
   if (prepare_kernel(kernel, smem, false) != cudaSuccess) return LORA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n_keys + zero_ctas), 1, 1);
+  // two CTAs per key (the second takes the odd 32-row passes): keys with more
+  // than one pass no longer set the length of the launch; LORA_MOE_HALVES=1
+  // keeps one CTA per key
+  static const int halves = env_int("LORA_MOE_HALVES", 2) == 1 ? 1 : 2;
+  cfg.gridDim = dim3((unsigned)(n_keys * halves + zero_ctas), 1, 1);
   cfg.blockDim = dim3(kKeyThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
@@ -316,7 +320,7 @@ int launch_key(const DeltaArgs& a, const Tables& tb, int n_keys, int zero_ctas,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = use_pdl() ? 1 : 0;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, a, tb, zero_ctas));
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, a, tb, zero_ctas, halves));
 }
 
 // The one-CTA-per-key kernel for the routed-MoE deltas (LORA_MOE_KEYED=0

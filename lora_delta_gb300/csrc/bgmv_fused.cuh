@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
         const uint32_t brow = (uint32_t)((((lane >> 3) & 1) << 3) + (lane & 7));
         const uint32_t bcol = (uint32_t)((lane >> 4) << 3);
+#pragma unroll 4
         for (int t = t_first; t < ntl; t += kWarps) {
           const int col0 = c0 + t * 16;  // first column of the tile (CTA-relative: - cb)
           const uint32_t baddr = smem_addr(Bs + (size_t)(col0 - cb + brow) * R + bcol);

@@ -71,13 +71,19 @@ __host__ __device__ inline KeySmem key_smem(int sr16) {
 
 template <int RMAX, class Tables>
 __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
-    delta_key_kernel(const DeltaArgs a, const Tables tb, int zero_ctas) {
+    delta_key_kernel(const DeltaArgs a, const Tables tb, int zero_ctas, int halves) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ SlotView v;
   __shared__ int prow[kKeyRows];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, tq = lane & 3;
-  const int key = blockIdx.x;
+  // CTA (key, half): with halves == 2, CTAs n_keys .. 2 n_keys - 1 take the
+  // odd passes of their key (keys of more than one pass share the work; for
+  // the others the second CTA ends at once), the rest the even passes.
+  const int nk_ctas = a.n_keys * halves;
+  const int half = (int)blockIdx.x >= a.n_keys && (int)blockIdx.x < nk_ctas ? 1 : 0;
+  const int key = (int)blockIdx.x < nk_ctas ? (int)blockIdx.x - half * a.n_keys
+                                            : a.n_keys + ((int)blockIdx.x - nk_ctas);
 
   if (key >= a.n_keys) {
     // The last zero_ctas CTAs write zeros on the rows of the no-key bucket
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
     }
   };
 
-  const bool early = a.early && v.nact > 0;
+  const bool early = a.early && v.nact > 0 && half == 0;
   if (early) {  // A rows of the first stages, before the dependency wait
     uint32_t sb = ring_s;
     for (int c = 0; c < kKeyStages - 1 && c < nchunks; ++c, sb += sbytes) copy_a(c, sb);
@@ -156,7 +162,7 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
   cudaGridDependencySynchronize();
   const int s0 = a.seg_start[key];
   const int nrows = v.nact > 0 ? a.seg_start[key + 1] - s0 : 0;
-  if (nrows <= 0 || nrows < a.min_rows || nrows >= a.max_rows) {
+  if (nrows <= half * kKeyRows || nrows < a.min_rows || nrows >= a.max_rows) {
     if (early) cp_async_wait<0>();  // no copy may land in a CTA that has exited
     return;
   }
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
   constexpr int KS = RMAX / 16;
   bool first_pass = true;
 
-  for (int p0 = 0; p0 < nrows; p0 += kKeyRows) {
+  for (int p0 = half * kKeyRows; p0 < nrows; p0 += halves * kKeyRows) {
     const int nr = min(kKeyRows, nrows - p0);
     if (!first_pass) __syncthreads();  // the previous pass is done with prow, H and the ring
     if (tid < nr) prow[tid] = rows[p0 + tid];
