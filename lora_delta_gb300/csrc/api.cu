@@ -5,6 +5,9 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <mutex>
 #include <unordered_map>
@@ -490,10 +493,48 @@ int prepare_rows(DeltaArgs& a, const int32_t* seq_slot, int n, int max_loras, in
   return LORA_OK;
 }
 
-// Launch of the tensor-core path for the keys with >= min_rows rows.
+// 2-D tensor maps for TMA loads of row blocks (128 rows x 64 columns, bf16,
+// 128-byte swizzle) of a row-major [rows, cols] matrix with leading dimension
+// ld; the encoder comes from the driver through the runtime, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+bool encode_row_blocks(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || rows < 1 || cols < 1) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTileRows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// TMA loads of the activation tiles on the tensor-core path when the rows of
+// each key are already contiguous; LORA_SGMV_TMA=0 keeps the cp.async copies.
+bool sgmv_tma_on() {
+  static const bool on = env_int("LORA_SGMV_TMA", 1) != 0;
+  return on;
+}
+
+// Launch of the tensor-core path for the keys with >= min_rows rows.  With
+// tmx and tmo (tensor maps of x and out), the tiles' rows are contiguous.
 template <class Tables>
 int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_keys,
-                int min_rows, cudaStream_t stream) {
+                int min_rows, cudaStream_t stream, const CUtensorMap* tmx = nullptr,
+                const CUtensorMap* tmo = nullptr) {
+  static const CUtensorMap no_map = {};
   SgmvArgs s = {};
   s.out = d.out;
   s.ld_out = d.ld_out;
@@ -543,6 +584,9 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
   s.add_inputs = d.add_inputs;
   s.err = d.err;
   s.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  s.contig = (tmx && tmo) ? 1 : 0;
+  const CUtensorMap& map_x = s.contig ? *tmx : no_map;
+  const CUtensorMap& map_out = s.contig ? *tmo : no_map;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -564,7 +608,7 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
     cfg.gridDim = dim3((unsigned)(most < slots ? most : slots));
     cfg.blockDim = dim3(kShrinkThreads);
     cfg.dynamicSmemBytes = (size_t)shrink_smem;
-    if ((e = cudaLaunchKernelEx(&cfg, kernel, s, tb)) != cudaSuccess) return LORA_ERR_CUDA;
+    if ((e = cudaLaunchKernelEx(&cfg, kernel, s, tb, map_x)) != cudaSuccess) return LORA_ERR_CUDA;
   }
   // expand: persistent, one CTA per SM
   {
@@ -582,11 +626,11 @@ int launch_sgmv(const DeltaArgs& d, const Tables& tb, const Workspace& w, int n_
     if (d.R <= 64) {
       auto kernel = sgmv_expand_kernel<64, Tables>;
       if ((e = prepare_kernel(kernel, smem, false)) != cudaSuccess) return LORA_ERR_CUDA;
-      e = cudaLaunchKernelEx(&cfg, kernel, s, tb, nch);
+      e = cudaLaunchKernelEx(&cfg, kernel, s, tb, nch, map_out);
     } else {
       auto kernel = sgmv_expand_kernel<128, Tables>;
       if ((e = prepare_kernel(kernel, smem, false)) != cudaSuccess) return LORA_ERR_CUDA;
-      e = cudaLaunchKernelEx(&cfg, kernel, s, tb, nch);
+      e = cudaLaunchKernelEx(&cfg, kernel, s, tb, nch, map_out);
     }
     if (e != cudaSuccess) return LORA_ERR_CUDA;
   }
@@ -864,7 +908,13 @@ int lora_delta_segmented(void* out, int64_t ld_out, const void* x, int n, int k_
   if (sgmv) a.max_rows = thr;
   rc = launch_delta<kModeFused>(a, tb, n_segs, st);
   if (rc || !sgmv) return rc;
-  return launch_sgmv(a, tb, w, n_segs, thr, st);
+  // the rows of a segment are consecutive rows of x and out: the tensor-core
+  // tiles take them by TMA
+  CUtensorMap tmx, tmo;
+  const bool tma = sgmv_tma_on() && encode_row_blocks(&tmx, x, n, k_in, k_in) &&
+                   encode_row_blocks(&tmo, out, n, ld_out, ld_out);
+  return tma ? launch_sgmv(a, tb, w, n_segs, thr, st, &tmx, &tmo)
+             : launch_sgmv(a, tb, w, n_segs, thr, st);
 }
 
 int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,

@@ -158,6 +158,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Add `bytes` to the transaction count the current phase of `bar` waits for
+// (no arrival): a TMA load that completes on `bar` brings them.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 2-D tiled TMA load: the box of the tensor map `map` (a kernel parameter or
+// global memory) at element coordinates (c0 innermost, c1) into shared memory
+// at `dst`, completing `bar`'s transaction count with the box's bytes.  The
+// innermost coordinate times the element size must be a multiple of 16 bytes;
+// with 128-byte swizzle `dst` must be 1024-byte aligned.  Elements outside the
+// tensor arrive as zeros.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed (the
 // arrival counts toward the barrier's expected count).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {

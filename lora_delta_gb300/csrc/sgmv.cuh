@@ -23,6 +23,8 @@
 // MMA thread's issued MMAs finish and still releases its TMEM.
 #pragma once
 
+#include <cuda.h>
+
 #include "bgmv.cuh"
 #include "common.cuh"
 #include "tc.cuh"
@@ -106,6 +108,11 @@ struct SgmvArgs {
   int add_inputs;
   uint32_t* err;
   uint64_t wait_ns;  // limit of every bounded wait (kWaitLimitNs unless a test lowers it)
+  // The rows of every tile are consecutive items that are also consecutive
+  // rows of x and out (rows already grouped by adapter: perm is the
+  // identity), and the kernels' tensor-map arguments describe x and out: the
+  // tile's x k-blocks and out segments then arrive by 2-D TMA loads.
+  int contig;
 };
 
 __device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gsrc, bool valid) {
@@ -129,7 +136,7 @@ constexpr int kShrinkThreads = kShrinkProducers + 32;
 
 template <class Tables>
 __global__ void __launch_bounds__(kShrinkThreads)
-    sgmv_shrink_kernel(const SgmvArgs a, const Tables tb) {
+    sgmv_shrink_kernel(const SgmvArgs a, const Tables tb, const __grid_constant__ CUtensorMap tm_x) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ SlotView v;
   __shared__ uint32_t taddr_s;
@@ -196,8 +203,12 @@ __global__ void __launch_bounds__(kShrinkThreads)
     if (warp < kShrinkMmaWarp) {
       // -------------------------------------------------------- producer --
       // piece (row, 16-byte chunk c) of a block: rows of x then of A,
-      // zero-filled past the tile's rows, the key's pairs and k_in
+      // zero-filled past the tile's rows, the key's pairs and k_in; with
+      // contiguous tile rows the x block is one TMA load (rows past the
+      // tile feed accumulator rows nobody writes; columns past k_in arrive
+      // as zeros)
       const int c = tid & 7;
+      const int r_first = (a.contig ? kTileRows : 0) + (tid >> 3);
       for (int kb = 0; kb < nkb; ++kb) {
         const int g = kbg + kb, s = g % kShrinkStages, k = g / kShrinkStages;
         if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1, a.wait_ns)) {
@@ -206,9 +217,13 @@ __global__ void __launch_bounds__(kShrinkThreads)
         }
         uint8_t* xs = smem + (size_t)s * stage_bytes;
         uint8_t* as = xs + xbytes;
+        if (a.contig && tid == 0) {
+          mbar_expect_tx(&full_bar[s], (uint32_t)xbytes);
+          tma_load_2d(xs, &tm_x, (kb_begin + kb) * 64, tile.pos0, &full_bar[s]);
+        }
         const int kk = (kb_begin + kb) * 64 + c * 8;
         const bool kin = kk < a.k_in;
-        for (int r = tid >> 3; r < kTileRows + N; r += kShrinkProducers / 8) {
+        for (int r = r_first; r < kTileRows + N; r += kShrinkProducers / 8) {
           const __nv_bfloat16* row = r < kTileRows ? xrow_s[r] : arow_s[r - kTileRows];
           const bool v_ok = kin && row != nullptr;
           uint8_t* dst = r < kTileRows ? xs + tc::sw128_offset(r, c * 8)
@@ -319,7 +334,8 @@ struct ExpandSmem {
 
 template <int RMAX, class Tables>
 __global__ void __launch_bounds__(kExpandThreads, 1)
-    sgmv_expand_kernel(const SgmvArgs a, const Tables tb, int n_chunks) {
+    sgmv_expand_kernel(const SgmvArgs a, const Tables tb, int n_chunks,
+                       const __grid_constant__ CUtensorMap tm_out) {
   using SM = ExpandSmem<RMAX>;
   constexpr int KB = SM::KB, NS = SM::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -422,7 +438,20 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
           cp_async16_zfill(bb + (size_t)(kk >> 6) * kExpandCols * 128 + tc::sw128_offset(c, kk & 63),
                            v ? bsrc + (size_t)c * R + kk : bsrc, v);
         }
-        if (a.add_inputs) {
+        if (a.add_inputs && a.contig) {
+          // out rows: each 64-column half one TMA load of the tile's 128 rows
+          // in the 128-byte swizzle (the epilogue's layout); rows past the
+          // tile and columns past the slice are not written back
+          if (tid == 0) {
+            const SgmvTile& t = tiles_s[it.lt];
+            const int halves = it.nc > 64 ? 2 : 1;
+            fence_proxy_async_smem();  // the epilogue's writes to this stage come first
+            mbar_expect_tx(&full_bar[s], (uint32_t)(halves * SM::kHalf));
+            for (int h = 0; h < halves; ++h)
+              tma_load_2d(stage_o(s) + h * SM::kHalf, &tm_out, a.sl.off[it.j] + it.c0 + 64 * h,
+                          t.pos0, &full_bar[s]);
+          }
+        } else if (a.add_inputs) {
           // out rows: piece p (8 columns) of row r at half p / 8, chunk (p mod 8) ^ (r mod 8)
           const SgmvTile& t = tiles_s[it.lt];
           const int* om = orow_map[it.lt];
