@@ -207,8 +207,12 @@ __global__ void __launch_bounds__(kShrinkThreads)
       // contiguous tile rows the x block is one TMA load (rows past the
       // tile feed accumulator rows nobody writes; columns past k_in arrive
       // as zeros)
+      // Rows past the tile's and pairs past the key's feed accumulator rows
+      // and columns that nobody writes: they are not copied at all (a small
+      // tile moves its own rows only); columns past k_in are zeros.
       const int c = tid & 7;
-      const int r_first = (a.contig ? kTileRows : 0) + (tid >> 3);
+      const int x_rows = a.contig ? 0 : tile.rows;  // (contiguous rows: one TMA load)
+      const int n_rows = x_rows + SRa;
       for (int kb = 0; kb < nkb; ++kb) {
         const int g = kbg + kb, s = g % kShrinkStages, k = g / kShrinkStages;
         if (k > 0 && !mbar_wait_bounded(&empty_bar[s], (k - 1) & 1, a.wait_ns)) {
@@ -223,12 +227,12 @@ __global__ void __launch_bounds__(kShrinkThreads)
         }
         const int kk = (kb_begin + kb) * 64 + c * 8;
         const bool kin = kk < a.k_in;
-        for (int r = r_first; r < kTileRows + N; r += kShrinkProducers / 8) {
-          const __nv_bfloat16* row = r < kTileRows ? xrow_s[r] : arow_s[r - kTileRows];
-          const bool v_ok = kin && row != nullptr;
-          uint8_t* dst = r < kTileRows ? xs + tc::sw128_offset(r, c * 8)
-                                       : as + tc::sw128_offset(r - kTileRows, c * 8);
-          cp_async16_zfill(dst, v_ok ? row + kk : a.x, v_ok);
+        for (int i = tid >> 3; i < n_rows; i += kShrinkProducers / 8) {
+          const bool is_x = i < x_rows;
+          const __nv_bfloat16* row = is_x ? xrow_s[i] : arow_s[i - x_rows];
+          uint8_t* dst = is_x ? xs + tc::sw128_offset(i, c * 8)
+                              : as + tc::sw128_offset(i - x_rows, c * 8);
+          cp_async16_zfill(dst, kin ? row + kk : a.x, kin);
         }
         cp_async_arrive(&full_bar[s]);
       }
