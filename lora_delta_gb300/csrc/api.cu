@@ -643,6 +643,86 @@ int check_max_loras(int max_loras) {
   return LORA_OK;
 }
 
+// A call whose keys split between the small-segment kernel and the
+// tensor-core path runs the two on disjoint rows and separate weights, so the
+// small-segment launch goes to a second stream of the device (forked from the
+// caller's stream by an event and joined back by another) and the two share
+// the GPU: each leaves DRAM idle in phases the other fills (the skewed decode
+// workload: 0.284 -> 0.245 ms).  One side stream and event pair per device,
+// created outside stream capture on first use; a call made while the caller's
+// stream is being captured before that runs both parts on the caller's stream.
+// Fork and join are recorded under a lock, so calls from several host threads
+// keep their pairs apart (their small-segment launches then queue on the one
+// side stream).  LORA_FORK=0 keeps everything on the caller's stream.
+struct ForkStreams {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_fork_mu;
+ForkStreams g_fork[kMaxDevices];
+
+bool fork_on() {
+  static const bool on = env_int("LORA_FORK", 1) != 0;
+  return on;
+}
+
+// The device's side stream and events, or nullptr (fork off, not creatable
+// now, or an unknown device); called with g_fork_mu held.
+ForkStreams* fork_streams(cudaStream_t caller) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  ForkStreams& f = g_fork[dev];
+  if (f.side) return &f;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  ForkStreams g;
+  if (cudaStreamCreateWithFlags(&g.side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&g.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&g.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (g.join) cudaEventDestroy(g.join);
+    if (g.fork) cudaEventDestroy(g.fork);
+    if (g.side) cudaStreamDestroy(g.side);
+    return nullptr;
+  }
+  f = g;
+  return &f;
+}
+
+// launch_delta<kModeFused> for the small keys and launch_sgmv for the others,
+// forked as above when possible.
+template <class Tables>
+int launch_split(const DeltaArgs& a, const Tables& tb, const Workspace& w, int n_keys, int thr,
+                 cudaStream_t s, const CUtensorMap* tmx = nullptr,
+                 const CUtensorMap* tmo = nullptr) {
+  if (fork_on()) {
+    std::lock_guard<std::mutex> lock(g_fork_mu);
+    ForkStreams* f = fork_streams(s);
+    if (f) {
+      if (cudaEventRecord(f->fork, s) != cudaSuccess ||
+          cudaStreamWaitEvent(f->side, f->fork, 0) != cudaSuccess)
+        return LORA_ERR_CUDA;
+      const int rc1 = launch_delta<kModeFused>(a, tb, n_keys, f->side);
+      const int rc2 = launch_sgmv(a, tb, w, n_keys, thr, s, tmx, tmo);
+      // joined whatever the launches returned (a capture must not be left forked)
+      const bool joined = cudaEventRecord(f->join, f->side) == cudaSuccess &&
+                          cudaStreamWaitEvent(s, f->join, 0) == cudaSuccess;
+      if (rc1) return rc1;
+      if (rc2) return rc2;
+      return joined ? LORA_OK : LORA_ERR_CUDA;
+    }
+  }
+  const int rc = launch_delta<kModeFused>(a, tb, n_keys, s);
+  return rc ? rc : launch_sgmv(a, tb, w, n_keys, thr, s, tmx, tmo);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ pack --
@@ -906,15 +986,14 @@ int lora_delta_segmented(void* out, int64_t ld_out, const void* x, int n, int k_
   const bool sgmv = a.sr_max <= kSgmvMaxSR;
   const int thr = sgmv_min_rows(S, R, k_in);
   if (sgmv) a.max_rows = thr;
-  rc = launch_delta<kModeFused>(a, tb, n_segs, st);
-  if (rc || !sgmv) return rc;
+  if (!sgmv) return launch_delta<kModeFused>(a, tb, n_segs, st);
   // the rows of a segment are consecutive rows of x and out: the tensor-core
   // tiles take them by TMA
   CUtensorMap tmx, tmo;
   const bool tma = sgmv_tma_on() && encode_row_blocks(&tmx, x, n, k_in, k_in) &&
                    encode_row_blocks(&tmo, out, n, ld_out, ld_out);
-  return tma ? launch_sgmv(a, tb, w, n_segs, thr, st, &tmx, &tmo)
-             : launch_sgmv(a, tb, w, n_segs, thr, st);
+  return tma ? launch_split(a, tb, w, n_segs, thr, st, &tmx, &tmo)
+             : launch_split(a, tb, w, n_segs, thr, st);
 }
 
 int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
@@ -954,9 +1033,8 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
   // when the average slot has enough rows for the tensor-core path, most
   // slots will leave the cluster kernel at once: no early weight copies
   if (sgmv && n >= (int64_t)thr * max_loras) a.early = 0;
-  rc = launch_delta<kModeFused>(a, tb, max_loras, (cudaStream_t)stream);
-  if (rc || !sgmv) return rc;
-  return launch_sgmv(a, tb, w, max_loras, thr, (cudaStream_t)stream);
+  if (!sgmv) return launch_delta<kModeFused>(a, tb, max_loras, (cudaStream_t)stream);
+  return launch_split(a, tb, w, max_loras, thr, (cudaStream_t)stream);
 }
 
 int lora_delta_fused_floor(void* out, int64_t ld_out, const void* x, int n, int k_in,

@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, (RMAX <= 32 ? 3 : 2))
         __syncthreads();
       }
       constexpr int KS = RMAX / 16;
-      constexpr int NB = (4 / KS) > 0 ? (4 / KS) : 1;  // column tiles per load batch
+      constexpr int NB = KS == 4 ? 4 : (KS > 4 ? 1 : 4 / KS);  // column tiles per load batch
       const int row0 = gq, row1 = gq + 8;
       const bool ok0 = row0 < nr, ok1 = row1 < nr;
       const int64_t orow0 = ok0 ? tb.out_row(prow[row0]) : 0;

@@ -221,6 +221,36 @@ def test_add_inputs_false(ld, di, oracle):
     check_linear(oracle, case, got, err, add_inputs=False)
 
 
+def _stream_case(which):
+    rng = np.random.default_rng(91 + which)
+    if which == 0:  # two slices, one stage per CTA, keys of 1 to 40 rows
+        seq = np.concatenate([np.zeros(40), np.ones(17), np.full(5, 2), [3], np.full(6, -1)])
+        rng.shuffle(seq)
+        return inputs.linear_case(91, n=len(seq), k_in=1024, widths=(6144, 2056), max_loras=4,
+                                  max_rank=64, ranks=[64, 32, 48, 8], alpha=32.0,
+                                  seq_slot=seq.astype(np.int32),
+                                  adapted=[[True, True], [True, False], [False, True],
+                                           [True, True]])
+    # 56 keys (clusters of 8), so each CTA's k share takes two stages; one key of
+    # 40 rows, the others 1 to 3
+    seq = np.concatenate([np.zeros(40)] + [np.full(1 + s % 3, s) for s in range(1, 56)])
+    rng.shuffle(seq)
+    return inputs.linear_case(92, n=len(seq), k_in=3072, widths=(4096,), max_loras=56,
+                              max_rank=64, ranks=rng.choice([8, 16, 32, 64], 56).tolist(),
+                              alpha=32.0, seq_slot=seq.astype(np.int32))
+
+
+@pytest.mark.parametrize("which", [0, 1])
+@pytest.mark.parametrize("add_inputs", [True, False])
+def test_rank_64_wide_outputs_stream_b_rows_in_chunks(ld, di, oracle, which, add_inputs):
+    """Rank 64 where a CTA's B rows exceed the staged slab: the expand streams B rows
+    and out segments in chunks through the shrink's stage buffers; keys span several
+    16-row passes (the A rows are copied again each pass)."""
+    case = _stream_case(which)
+    got, err, _ = run_fused(ld, di, case, add_inputs=add_inputs)
+    check_linear(oracle, case, got, err, add_inputs=add_inputs)
+
+
 def test_bad_slot_sets_error_and_skips(ld, di, oracle):
     seq = np.array([0, 9, -1, 1, 2, 7, 0, 1], dtype=np.int32)
     case = inputs.linear_case(9, n=8, k_in=64, widths=(32,), max_loras=3, max_rank=8,
@@ -805,6 +835,39 @@ def test_sgmv_and_small_path_agree_on_a_hot_slot(ld, di, oracle):
     assert_close(di.bits(a), di.bits(b), "tensor-core vs small-segment path")
     ref, _ = oracle_delta(oracle, case)
     assert_close(di.bits(a), ref, "tensor-core path vs oracle")
+
+
+def test_split_call_replays_from_a_cuda_graph(ld, di, oracle):
+    """A call whose keys split between the tensor-core path and the small-segment
+    kernel runs the latter on a second stream, forked and joined by events.
+    Captured in a CUDA graph on a side stream and replayed, it gives the eager
+    call's bits, and those match the oracle."""
+    # two hot slots of ~600 rows, ten others of ~25 (below the threshold of 64)
+    case = _hot_slots_case(41, 1500, 512, (384, 128), 16,
+                           [16, 8, 16, 4, 16, 12, 16, 8, 2, 16, 1, 16], hot=(0, 3))
+    counts = np.bincount(case.seq_slot[case.seq_slot >= 0], minlength=12)
+    assert counts[[0, 3]].min() >= 64 and 0 < np.delete(counts, [0, 3]).max() < 64
+    d = di.linear_to_device(case)
+    ws = torch.empty(ld.lora_workspace_size(case.n, 2, 16, 12), dtype=torch.uint8, device="cuda")
+    eager = d.out0.clone()
+    ld.lora_delta_fused(eager, d.x, d.seq_slot, d.pool, workspace=ws)
+    torch.cuda.synchronize()
+    got = d.out0.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            ld.lora_delta_fused(got, d.x, d.seq_slot, d.pool, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    for _ in range(2):  # replays start from the same out
+        got.copy_(d.out0)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(di.bits(got), di.bits(eager))
+    ref, _ = oracle_delta(oracle, case)
+    assert_close(di.bits(eager), ref, case.name)
 
 
 # ------------------------------------------------------ bounded waits --
