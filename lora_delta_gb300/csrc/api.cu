@@ -723,6 +723,44 @@ int launch_split(const DeltaArgs& a, const Tables& tb, const Workspace& w, int n
   return rc ? rc : launch_sgmv(a, tb, w, n_keys, thr, s, tmx, tmo);
 }
 
+// A batch small enough for the kernels' own row scan that still goes through
+// the routing sort for the tensor-core path: forked before the sort, the
+// small-segment kernel finds its keys' rows by that scan on the side stream
+// (skipping keys with thr rows or more), so it does not wait for the sort.
+// Returns kNoFork, having launched nothing, when there is no side stream.
+constexpr int kNoFork = -1;
+int launch_split_scan(DeltaArgs& a, const LinearTables& tb, const int32_t* seq_slot, int n,
+                      int n_keys, int hs, int thr, void* workspace, size_t ws_bytes,
+                      uint32_t* err, cudaStream_t s) {
+  if (!fork_on()) return kNoFork;
+  // (the checks of the routing pass, before anything is launched)
+  if (ws_bytes < ws_bytes_for(n, n_keys, hs)) return LORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGN;
+  DeltaArgs c = a;
+  prepare_rows(c, seq_slot, n, n_keys, hs, nullptr, 0, err, s, nullptr);  // (own scan)
+  plan_tiles(c, a.k_in, a.sl.n_cols, a.sr_max, kModeFused);
+  c.max_rows = thr;
+  if (n >= (int64_t)thr * n_keys) c.early = 0;
+  std::lock_guard<std::mutex> lock(g_fork_mu);
+  ForkStreams* f = fork_streams(s);
+  if (!f) return kNoFork;
+  if (cudaEventRecord(f->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(f->side, f->fork, 0) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  const int rc1 = launch_delta<kModeFused>(c, tb, n_keys, f->side);
+  Workspace w = {};
+  int rc2 = prepare_rows(a, seq_slot, n, n_keys, hs, workspace, ws_bytes, err, s, &w);
+  if (!rc2) {
+    plan_tiles(a, a.k_in, a.sl.n_cols, a.sr_max, kModeFused);
+    rc2 = launch_sgmv(a, tb, w, n_keys, thr, s);
+  }
+  const bool joined = cudaEventRecord(f->join, f->side) == cudaSuccess &&
+                      cudaStreamWaitEvent(s, f->join, 0) == cudaSuccess;
+  if (rc1) return rc1;
+  if (rc2) return rc2;
+  return joined ? LORA_OK : LORA_ERR_CUDA;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ pack --
@@ -1020,15 +1058,21 @@ int lora_delta_fused(void* out, int64_t ld_out, const void* x, int n, int k_in,
   a.R = R;
   a.add_inputs = add_inputs ? 1 : 0;
   a.sr_max = S * R;
+  const int hs = (S * R + 15) / 16 * 16;
+  const int thr = sgmv_min_rows(S, R, k_in);
+  LinearTables tb{a_table, b_table, scale_table, max_loras};
+  if (n <= kInlineRowsMax && workspace && n >= kRouteMinRows && a.sr_max <= kSgmvMaxSR) {
+    rc = launch_split_scan(a, tb, seq_slot, n, max_loras, hs, thr, workspace, ws_bytes, err_word,
+                           (cudaStream_t)stream);
+    if (rc != kNoFork) return rc;
+  }
   Workspace w = {};
-  rc = prepare_rows(a, seq_slot, n, max_loras, (S * R + 15) / 16 * 16, workspace, ws_bytes,
-                    err_word, (cudaStream_t)stream, &w);
+  rc = prepare_rows(a, seq_slot, n, max_loras, hs, workspace, ws_bytes, err_word,
+                    (cudaStream_t)stream, &w);
   if (rc) return rc;
   plan_tiles(a, k_in, a.sl.n_cols, a.sr_max, kModeFused);
-  LinearTables tb{a_table, b_table, scale_table, max_loras};
   // keys with many rows go to the tensor-core path, the others stay here
   const bool sgmv = a.perm != nullptr && a.sr_max <= kSgmvMaxSR;
-  const int thr = sgmv_min_rows(S, R, k_in);
   if (sgmv) a.max_rows = thr;
   // when the average slot has enough rows for the tensor-core path, most
   // slots will leave the cluster kernel at once: no early weight copies

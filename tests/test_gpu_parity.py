@@ -837,13 +837,15 @@ def test_sgmv_and_small_path_agree_on_a_hot_slot(ld, di, oracle):
     assert_close(di.bits(a), ref, "tensor-core path vs oracle")
 
 
-def test_split_call_replays_from_a_cuda_graph(ld, di, oracle):
+@pytest.mark.parametrize("n", [1000, 1500])
+def test_split_call_replays_from_a_cuda_graph(ld, di, oracle, n):
     """A call whose keys split between the tensor-core path and the small-segment
-    kernel runs the latter on a second stream, forked and joined by events.
-    Captured in a CUDA graph on a side stream and replayed, it gives the eager
-    call's bits, and those match the oracle."""
-    # two hot slots of ~600 rows, ten others of ~25 (below the threshold of 64)
-    case = _hot_slots_case(41, 1500, 512, (384, 128), 16,
+    kernel runs the latter on a second stream, forked and joined by events (at
+    1000 rows before the routing sort, the kernel scanning its rows itself; at
+    1500 after it).  Captured in a CUDA graph on a side stream and replayed, it
+    gives the eager call's bits, and those match the oracle."""
+    # two hot slots of 400-600 rows, ten others of 15-30 (below the threshold of 64)
+    case = _hot_slots_case(41, n, 512, (384, 128), 16,
                            [16, 8, 16, 4, 16, 12, 16, 8, 2, 16, 1, 16], hot=(0, 3))
     counts = np.bincount(case.seq_slot[case.seq_slot >= 0], minlength=12)
     assert counts[[0, 3]].min() >= 64 and 0 < np.delete(counts, [0, 3]).max() < 64
