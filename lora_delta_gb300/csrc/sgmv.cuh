@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
       tc::fence_after_sync();
       const int r = warp * 32 + lane;
       float* dst = a.hbuf + (size_t)split * a.plane + (size_t)(tile.pos0 + r) * a.hs;
-      if (ok)
+      if (ok && warp * 32 < tile.rows)  // (a lane quarter past the tile's rows: nothing)
         for (int c0 = 0; c0 < N; c0 += 16) {
           float vals[16];
           tc::tmem_ld16(taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, vals);
@@ -584,7 +584,9 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       // (in place; 16-byte chunk c of row r sits at chunk c ^ (r mod 8))
       const float sc = vt[it.lt].scale;
       uint8_t* hb = stage_o(s) + hf * SM::kHalf;
-      const bool mine = hf * 64 < it.nc;  // uniform across the warp
+      // (uniform across the warp; a lane quarter past the tile's rows has
+      // nothing to read or write back)
+      const bool mine = hf * 64 < it.nc && q * 32 < t.rows;
       if (mine) {
         float d[64];
         tc::tmem_ld64(taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kExpandCols + hf * 64),
