@@ -358,6 +358,32 @@ int launch_route_scratch(const KeyFn& kf, int n, int n_keys, int32_t* perm, int3
                          uint32_t* counts, uint32_t* err, cudaStream_t stream) {
   if (n < kRouteChunkedMinItems) return launch_route(kf, n, n_keys, perm, seg_start, err, stream);
   const int nb = (n + kRouteChunk - 1) / kRouteChunk;
+  // up to kRouteClusterMax chunks: the one-launch cluster sort
+  // (LORA_ROUTE_CLUSTER=0 keeps the two kernels)
+  static const bool cluster_on = env_int("LORA_ROUTE_CLUSTER", 1) != 0;
+  const size_t smem_cl = route_cluster_smem_bytes(n_keys);
+  if (cluster_on && nb <= kRouteClusterMax && smem_cl <= 200 * 1024) {
+    auto kcl = route_cluster_kernel<KeyFn>;
+    if (prepare_kernel(kcl, (int)smem_cl, nb > 8) == cudaSuccess) {
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)nb;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)nb);
+      cfg.blockDim = dim3(kRouteThreads);
+      cfg.dynamicSmemBytes = smem_cl;
+      cfg.stream = stream;
+      cfg.attrs = attr;
+      cfg.numAttrs = use_pdl() ? 2 : 1;
+      if (cudaLaunchKernelEx(&cfg, kcl, kf, n, n_keys, perm, seg_start, err) == cudaSuccess)
+        return LORA_OK;
+    }
+    cudaGetLastError();  // (not launched: the two kernels below)
+  }
   const int smem_c = (int)route_smem_bytes(n_keys), smem_s = (int)route_chunk_smem_bytes(n_keys);
   auto kc = route_count_kernel<KeyFn>;
   auto ks = route_scatter_kernel<KeyFn>;

@@ -306,4 +306,83 @@ __global__ void __launch_bounds__(kRouteThreads)
   warp_scatter<kRoutePerWarp / 32>(key_of, b0, b1, nkb, my, perm);
 }
 
+// ------------------------------------------------------- cluster sort ---
+// Up to kRouteClusterMax chunks in one launch: one CTA per chunk, all in one
+// thread-block cluster.  Each CTA counts its chunk once (per warp, as above)
+// and leaves the chunk's per-key totals in its shared memory; after one
+// cluster barrier every CTA reads the totals of all chunks from its peers'
+// shared memory (distributed shared memory) into its start within each key
+// and the keys' totals, scans and scatters its chunk as route_scatter_kernel
+// does -- the same positions, so the same stable order -- with no counts in
+// global memory and one launch instead of two.
+constexpr int kRouteClusterMax = 16;
+
+inline size_t route_cluster_smem_bytes(int n_keys) {
+  return sizeof(uint32_t) * ((size_t)kRouteWarps + 3) * (size_t)(n_keys + 1);
+}
+
+template <class KeyFn>
+__global__ void __launch_bounds__(kRouteThreads)
+    route_cluster_kernel(KeyFn key_of, int n, int n_keys, int32_t* __restrict__ perm,
+                         int32_t* __restrict__ seg_start, uint32_t* err_word) {
+  // [kRouteWarps][n_keys + 1] per-warp counts, then this chunk's totals
+  // mine[n_keys + 1] (read by the peers), before[] and total[]
+  extern __shared__ uint32_t cnt[];
+  __shared__ uint32_t warp_sums[kRouteWarps];
+  cudaGridDependencySynchronize();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nkb = n_keys + 1, nblk = (int)gridDim.x, blk = (int)blockIdx.x;
+  uint32_t* mine = cnt + kRouteWarps * nkb;
+  uint32_t* before = mine + nkb;
+  uint32_t* total = before + nkb;
+  for (int i = tid; i < kRouteWarps * nkb; i += kRouteThreads) cnt[i] = 0;
+  __syncthreads();
+  const int b0 = min(n, blk * kRouteChunk + warp * kRoutePerWarp);
+  const int b1 = min(n, b0 + kRoutePerWarp);
+  uint32_t errbits = 0;
+  uint32_t* my = cnt + warp * nkb;
+  warp_count<kRoutePerWarp / 32>(key_of, b0, b1, nkb, my, errbits);
+  errbits = __reduce_or_sync(0xffffffffu, errbits);
+  if (lane == 0 && errbits) set_error(err_word, errbits);
+  __syncthreads();
+  for (int k = tid; k < nkb; k += kRouteThreads) {
+    uint32_t t = 0;
+    for (int w = 0; w < kRouteWarps; ++w) t += cnt[w * nkb + k];
+    mine[k] = t;
+  }
+  cluster_arrive_release_smem();  // this chunk's totals in place
+  cluster_wait();
+  const uint32_t mine_addr = smem_addr(mine);
+  for (int k = tid; k < nkb; k += kRouteThreads) {
+    uint32_t b = 0, t = 0;
+#pragma unroll 8
+    for (int c = 0; c < nblk; ++c) {  // (loads in flight together)
+      const uint32_t v = __float_as_uint(dsmem_ld_f32(dsmem_map(mine_addr + 4u * (uint32_t)k,
+                                                                  (uint32_t)c)));
+      t += v;
+      b += c < blk ? v : 0u;
+    }
+    before[k] = b;
+    total[k] = t;
+  }
+  cluster_arrive_relaxed();  // done reading the peers (waited on before exit)
+  __syncthreads();
+  int k0, k1;
+  uint32_t run = block_scan_keys(nkb, [&](int k) { return total[k]; }, k0, k1, warp_sums);
+  for (int k = k0; k < k1; ++k) {
+    if (blk == 0) seg_start[k] = (int32_t)run;
+    uint32_t at = run + before[k];
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const uint32_t c = cnt[w * nkb + k];
+      cnt[w * nkb + k] = at;
+      at += c;
+    }
+    run += total[k];
+  }
+  if (blk == 0 && tid == 0) seg_start[nkb] = n;
+  __syncthreads();
+  warp_scatter<kRoutePerWarp / 32>(key_of, b0, b1, nkb, my, perm);
+  cluster_wait();  // the peers have read this CTA's totals
+}
+
 }  // namespace lora
