@@ -186,6 +186,9 @@ __global__ void __launch_bounds__(kRouteThreads)
                  int32_t* __restrict__ seg_start, uint32_t* err_word) {
   extern __shared__ uint32_t cnt[];  // [kRouteWarps][n_keys + 1]
   __shared__ uint32_t warp_sums[kRouteWarps];
+  // The next launch may start its prologue (adapter weight copies) now: it
+  // reads this sort's output only after its own dependency wait.
+  cudaTriggerProgrammaticLaunchCompletion();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nkb = n_keys + 1;
   for (int i = tid; i < kRouteWarps * nkb; i += kRouteThreads) cnt[i] = 0;
@@ -266,6 +269,7 @@ __global__ void __launch_bounds__(kRouteThreads)
   extern __shared__ uint32_t cnt[];
   __shared__ uint32_t warp_sums[kRouteWarps];
   cudaGridDependencySynchronize();
+  cudaTriggerProgrammaticLaunchCompletion();  // (as in route_kernel)
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nkb = n_keys + 1, nblk = (int)gridDim.x, blk = (int)blockIdx.x;
   uint32_t* before = cnt + kRouteWarps * nkb;
@@ -330,6 +334,7 @@ __global__ void __launch_bounds__(kRouteThreads)
   extern __shared__ uint32_t cnt[];
   __shared__ uint32_t warp_sums[kRouteWarps];
   cudaGridDependencySynchronize();
+  cudaTriggerProgrammaticLaunchCompletion();  // (as in route_kernel)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nkb = n_keys + 1, nblk = (int)gridDim.x, blk = (int)blockIdx.x;
   uint32_t* mine = cnt + kRouteWarps * nkb;
