@@ -92,7 +92,10 @@ def test_route_bit_exact(ld, oracle, n, L):
                                  (100, 8)])
 def test_chunked_route_bit_exact(ld, oracle, n, L):
     """The many-CTA routing sort gives the one-CTA sort's output bit for bit
-    (the same stable order) and the oracle's segments."""
+    (the same stable order) and the oracle's segments: the one-launch cluster
+    sort (2 to 16 chunks of 1024 items, the last one ragged at 5003) and the
+    two-kernel sort (20000 items: 20 chunks; 3072 keys: more than the cluster
+    sort's shared memory holds)."""
     rng = np.random.default_rng(7 * n + L)
     seq = rng.integers(-2, L + 2, size=n).astype(np.int32)
     seq_d = torch.from_numpy(seq).cuda()
