@@ -5,10 +5,20 @@
  * ---------------------------------------
  *  - All tensors are caller-owned DEVICE memory unless an argument says
  *    "host".  bf16 tensors are row-major with the stated leading dimension.
- *  - Launchers only enqueue work on `stream` (a cudaStream_t; NULL is the
- *    legacy default stream): they allocate nothing and never synchronize
+ *  - Launchers enqueue work on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream): they allocate no device memory and never synchronize
  *    ("Module lora_delta", module invariants).  The one exception is
  *    lora_get_error, which waits on `stream` to read the error word back.
+ *    A call whose slots split between the small-segment kernel and the
+ *    tensor-core path (lora_delta_fused, lora_delta_segmented) runs the former
+ *    on a second stream of the library's, forked from `stream` by an event
+ *    and joined back by another: all of the call's work still comes before
+ *    anything enqueued on `stream` after it, and inside a stream capture the
+ *    fork and the join become part of the captured graph.  That stream and
+ *    its two events are created once per device, on the first such call made
+ *    outside a capture (a call made during a capture before then runs both
+ *    parts on `stream`); calls from several host threads share them, under a
+ *    lock.  LORA_FORK=0 in the environment keeps every call on `stream`.
  *  - Return value: LORA_OK (0) or a host-detected LORA_ERR_* status; an error
  *    status means nothing was enqueued.  Nothing is ever thrown.
  *  - Device-detected problems never trap: the offending row / pair is handled
