@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
     const int ostride = cc + (cc % 16 == 0 ? 8 : 16);  // elements, 8 mod 16: <= cc + 16
     const uint32_t o_off = (uint32_t)(cc * bstride * 2);
     const int vpc = R / 8;  // 16-byte pieces per B column
+    // (a power of two for R = 8, 16, 32, 64: shifts instead of divisions)
+    const int vpc_shift = (vpc & (vpc - 1)) == 0 ? __ffs(vpc) - 1 : -1;
     auto first_slice = [&](int j) {
       while (j < a.sl.S && v.ja[j] < 0) ++j;
       return j;
@@ -312,15 +314,15 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
       const int cw = min(cc, a.sl.width[j] - c0);
       const __nv_bfloat16* src = v.B[j] + (size_t)c0 * R;
       for (int i = tid; i < cw * vpc; i += kKeyThreads) {
-        const int col = i / vpc, part = i - col * vpc;
+        const int col = vpc_shift >= 0 ? i >> vpc_shift : i / vpc, part = i - col * vpc;
         cp_async16_s(hb + (uint32_t)(col * bstride + part * 8) * 2u, src + (size_t)col * R + part * 8);
       }
-      if (a.add_inputs) {
+      if (a.add_inputs) {  // a warp per out row, its lanes over the row's pieces
         const int ppr = cw / 8;  // pieces per out row
-        for (int i = tid; i < nr * ppr; i += kKeyThreads) {
-          const int r = i / ppr, q = i - r * ppr;
-          cp_async16_s(hb + o_off + (uint32_t)(r * ostride + q * 8) * 2u,
-                       a.out + tb.out_row(prow[r]) * a.ld_out + a.sl.off[j] + c0 + q * 8);
+        for (int r = warp; r < nr; r += kKeyWarps) {
+          const __nv_bfloat16* orow = a.out + tb.out_row(prow[r]) * a.ld_out + a.sl.off[j] + c0;
+          const uint32_t dst = hb + o_off + (uint32_t)(r * ostride) * 2u;
+          for (int q = lane; q < ppr; q += 32) cp_async16_s(dst + (uint32_t)q * 16u, orow + q * 8);
         }
       }
     };
