@@ -425,6 +425,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   if (warp < kMmaWarp) {
     // ---------------------------------------------------------- producer --
     const int cpr = (R + 15) >> 4 << 1;  // 16-byte pieces per B row that the K-steps read
+    // (a power of two unless R is 48, 80, ...: a shift instead of a division)
+    const int cpr_shift = (cpr & (cpr - 1)) == 0 ? __ffs(cpr) - 1 : -1;
     for (int w = w0; w < w1 && ok; ++w) {
       const int i = w - w0, s = i % NS, k = i / NS;
       const Item it = item_of(w);
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         const __nv_bfloat16* bsrc = vt[it.lt].B[it.j] + (size_t)it.c0 * R;
         uint8_t* bb = stage_b(s);
         for (int idx = tid; idx < kExpandCols * cpr; idx += kExpandProducers) {
-          const int c = idx / cpr, kk = (idx - c * cpr) * 8;
+          const int c = cpr_shift >= 0 ? idx >> cpr_shift : idx / cpr, kk = (idx - c * cpr) * 8;
           const bool v = c < it.nc && kk < R;  // zeros past the slice's end and past R
           cp_async16_zfill(bb + (size_t)(kk >> 6) * kExpandCols * 128 + tc::sw128_offset(c, kk & 63),
                            v ? bsrc + (size_t)c * R + kk : bsrc, v);
