@@ -254,6 +254,26 @@ def test_rank_64_wide_outputs_stream_b_rows_in_chunks(ld, di, oracle, which, add
     check_linear(oracle, case, got, err, add_inputs=add_inputs)
 
 
+@pytest.mark.parametrize("R,add_inputs", [(32, True), (32, False), (16, True), (64, True)])
+def test_small_slots_with_large_adapters(ld, di, oracle, R, add_inputs):
+    """Adapters of at least 512 KiB (the tensor-core threshold drops to 16 rows):
+    slots with 1 to 15 rows go to the small-segment kernel on the second stream,
+    slots with 16 or more to the tensor-core path.  Two ragged slices, ranks
+    under R, slots with an inactive slice, 40 slots."""
+    rng = np.random.default_rng(101 + R)
+    k_in = 524288 // (2 * 2 * R) + 8 * (R // 16)  # S * R * k_in * 2 just over 512 KiB
+    counts = rng.choice([1, 2, 3, 5, 9, 15, 16, 23], size=40)
+    seq = np.concatenate([np.full(c, s) for s, c in enumerate(counts)] + [np.full(7, -1)])
+    rng.shuffle(seq)
+    adapted = [[bool(rng.random() > 0.15), bool(rng.random() > 0.15)] for _ in range(40)]
+    ranks = rng.choice([R // 2, R], size=40).tolist()
+    case = inputs.linear_case(102 + R, n=len(seq), k_in=k_in, widths=(2048, 1032), max_loras=40,
+                              max_rank=R, ranks=ranks, alpha=float(R), seq_slot=seq.astype(np.int32),
+                              adapted=adapted)
+    got, err, _ = run_fused(ld, di, case, add_inputs=add_inputs)
+    check_linear(oracle, case, got, err, add_inputs=add_inputs)
+
+
 def test_bad_slot_sets_error_and_skips(ld, di, oracle):
     seq = np.array([0, 9, -1, 1, 2, 7, 0, 1], dtype=np.int32)
     case = inputs.linear_case(9, n=8, k_in=64, widths=(32,), max_loras=3, max_rank=8,
