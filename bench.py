@@ -49,7 +49,7 @@ def load_peaks():
 # ncu capture of that launch (dram__bytes_read.sum + dram__bytes_write.sum),
 # with the hash of the sources it was taken on: reported only while they are
 # unchanged, null otherwise.
-DECODE_TRAFFIC = {"bytes": 10622976, "sources_sha256_16": "c6f3c3575620f3f6"}
+DECODE_TRAFFIC = {"bytes": 10623232, "sources_sha256_16": "b9fab7ad425dee04"}
 DECODE_SOURCES = ("lora_delta_gb300/csrc/bgmv.cuh", "lora_delta_gb300/csrc/bgmv_fused.cuh",
                   "lora_delta_gb300/csrc/common.cuh", "lora_delta_gb300/csrc/api.cu")
 
