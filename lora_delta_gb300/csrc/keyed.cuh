@@ -368,6 +368,16 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
       const int64_t cbase = a.sl.off[j] + c0 + 2 * tq;
       const __nv_bfloat16* os = reinterpret_cast<const __nv_bfloat16*>(
           ring + (size_t)hsel * half_bytes + o_off) + 2 * tq;
+      // this lane's four output row pointers for the item, so that the tile
+      // loop only adds the tile's column (rank <= 16: the larger instance
+      // has no registers to spare for them)
+      constexpr bool kHoist = RMAX <= 16;
+      __nv_bfloat16* op[2][2];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          op[mi][h] = kHoist ? a.out + (int64_t)orow[mi][h] * a.ld_out + cbase : nullptr;
       for (int t = warp; t < cw / 8; t += kKeyWarps) {
         uint32_t bf[KS][2];
         const uint32_t ba = hbase + (uint32_t)(t * 8 * bstride) * 2u;
@@ -400,8 +410,8 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
                   a.add_inputs ? *reinterpret_cast<const uint32_t*>(
                                      os + (mi * 16 + gq + 8 * h) * ostride + t * 8)
                                : 0u;
-              *reinterpret_cast<uint32_t*>(a.out + (int64_t)orow[mi][h] * a.ld_out + cbase +
-                                           t * 8) =
+              *reinterpret_cast<uint32_t*>(
+                  (kHoist ? op[mi][h] : a.out + (int64_t)orow[mi][h] * a.ld_out + cbase) + t * 8) =
                   pack_bf16x2(bf16lo(o) + sc[mi][h] * d[2 * h], bf16hi(o) + sc[mi][h] * d[2 * h + 1]);
             }
         }
