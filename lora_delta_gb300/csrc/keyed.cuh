@@ -157,6 +157,12 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
     uint32_t sb = ring_s;
     for (int c = 0; c < kKeyStages - 1 && c < nchunks; ++c, sb += sbytes) copy_a(c, sb);
     cp_async_commit();
+    // ... and the whole of the key's A and B on their way to L2: the routing
+    // sort this launch waits for leaves DRAM nearly idle
+    if (warp == kKeyWarps - 1 && lane < a.sl.S && v.ja[lane] >= 0) {
+      bulk_prefetch_l2(v.A[lane], (uint32_t)(R * a.k_in * 2));
+      bulk_prefetch_l2(v.B[lane], (uint32_t)(a.sl.width[lane] * R * 2));
+    }
   }
   cudaTriggerProgrammaticLaunchCompletion();
   cudaGridDependencySynchronize();
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(kKeyThreads, RMAX <= 16 ? 4 : 3)
     __syncthreads();
     // L2 prefetch of the pass's expand operands (B of the key; out rows)
     if (warp == kKeyWarps - 1) {
-      if (first_pass)
+      if (first_pass && !early)  // (prefetched before the dependency wait otherwise)
         for (int j = lane; j < a.sl.S; j += 32)
           if (v.ja[j] >= 0)
             bulk_prefetch_l2(v.B[j], (uint32_t)(a.sl.width[j] * R * 2));
