@@ -346,7 +346,18 @@ __global__ void __launch_bounds__(kRouteThreads)
   const int b1 = min(n, b0 + kRoutePerWarp);
   uint32_t errbits = 0;
   uint32_t* my = cnt + warp * nkb;
-  warp_count<kRoutePerWarp / 32>(key_of, b0, b1, nkb, my, errbits);
+  // A warp's items are one round of kRoutePerWarp / 32 keys per lane: they are
+  // read once and kept in registers for both the count and the scatter.
+  static_assert(kRoutePerWarp == 64, "two keys per lane");
+  int kr[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = b0 + u * 32 + lane;
+    kr[u] = i < b1 ? key_of(i, errbits) : -1;
+  }
+  // (item i of the warp's block is round (i - b0) / 32 of this lane)
+  auto kept = [&](int i, uint32_t&) { return ((i - b0) >> 5) == 0 ? kr[0] : kr[1]; };
+  warp_count<kRoutePerWarp / 32>(kept, b0, b1, nkb, my, errbits);
   errbits = __reduce_or_sync(0xffffffffu, errbits);
   if (lane == 0 && errbits) set_error(err_word, errbits);
   __syncthreads();
@@ -386,7 +397,7 @@ __global__ void __launch_bounds__(kRouteThreads)
   }
   if (blk == 0 && tid == 0) seg_start[nkb] = n;
   __syncthreads();
-  warp_scatter<kRoutePerWarp / 32>(key_of, b0, b1, nkb, my, perm);
+  warp_scatter<kRoutePerWarp / 32>(kept, b0, b1, nkb, my, perm);
   cluster_wait();  // the peers have read this CTA's totals
 }
 
