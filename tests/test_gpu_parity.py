@@ -895,6 +895,35 @@ def test_split_call_replays_from_a_cuda_graph(ld, di, oracle, n):
     assert_close(di.bits(eager), ref, case.name)
 
 
+def test_split_call_on_the_legacy_default_stream(ld, di, oracle):
+    """The C ABI with stream NULL (the legacy default stream) on a call whose keys
+    split between the two paths: the second stream is forked from and joined to
+    it like any other; the result equals the same call on a created stream."""
+    import ctypes
+    case = _hot_slots_case(43, 1500, 512, (384, 128), 16,
+                           [16, 8, 16, 4, 16, 12, 16, 8, 2, 16, 1, 16], hot=(0, 3))
+    d = di.linear_to_device(case)
+    ws = torch.empty(ld.lora_workspace_size(case.n, 2, 16, 12), dtype=torch.uint8, device="cuda")
+    ref = d.out0.clone()
+    ld.lora_delta_fused(ref, d.x, d.seq_slot, d.pool, workspace=ws)
+    torch.cuda.synchronize()
+    got = d.out0.clone()
+    torch.cuda.synchronize()
+    L = ld.lib()
+    w = (ctypes.c_int32 * 2)(384, 128)
+    rc = L.lora_delta_fused(ctypes.c_void_p(got.data_ptr()), 512, ctypes.c_void_p(d.x.data_ptr()),
+                            case.n, 512, ctypes.c_void_p(d.seq_slot.data_ptr()),
+                            ctypes.c_void_p(d.pool.a_table.data_ptr()),
+                            ctypes.c_void_p(d.pool.b_table.data_ptr()),
+                            ctypes.c_void_p(d.pool.scale_table.data_ptr()), w, 2, 16, 12, 0, 1,
+                            ctypes.c_void_p(ws.data_ptr()), ws.numel(), None, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(di.bits(got), di.bits(ref))
+    ref_o, _ = oracle_delta(oracle, case)
+    assert_close(di.bits(got), ref_o, case.name)
+
+
 # ------------------------------------------------------ bounded waits --
 
 def test_wait_time_out_sets_the_error_bit_and_the_next_call_is_correct(ld, di, oracle):
