@@ -924,6 +924,52 @@ def test_split_call_on_the_legacy_default_stream(ld, di, oracle):
     assert_close(di.bits(got), ref_o, case.name)
 
 
+def test_split_calls_from_two_host_threads(ld, di):
+    """Two host threads making split calls on their own streams at once (the library
+    call releases the interpreter lock): the forks and joins of the shared second
+    stream are recorded under the library's lock, and every output equals the same
+    call made alone."""
+    import threading
+    cases = [_hot_slots_case(44 + t, 1500, 512, (384, 128), 16,
+                             [16, 8, 16, 4, 16, 12, 16, 8, 2, 16, 1, 16], hot=(0, 3))
+             for t in range(2)]
+    devs = [di.linear_to_device(c) for c in cases]
+    wss = [torch.empty(ld.lora_workspace_size(c.n, 2, 16, 12), dtype=torch.uint8, device="cuda")
+           for c in cases]
+    refs = []
+    for d, ws in zip(devs, wss):
+        o = d.out0.clone()
+        ld.lora_delta_fused(o, d.x, d.seq_slot, d.pool, workspace=ws)
+        refs.append(di.bits(o))
+    torch.cuda.synchronize()
+    reps = 12
+    outs = [[d.out0.clone() for _ in range(reps)] for d in devs]
+    streams = [torch.cuda.Stream() for _ in devs]
+    errors = []
+
+    def worker(t):
+        try:
+            with torch.cuda.stream(streams[t]):
+                for k in range(reps):
+                    ld.lora_delta_fused(outs[t][k], devs[t].x, devs[t].seq_slot, devs[t].pool,
+                                        workspace=wss[t], stream=streams[t])
+        except Exception as e:  # (reported below)
+            errors.append(e)
+
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for t in range(2):
+        for k in range(reps):
+            assert np.array_equal(di.bits(outs[t][k]), refs[t]), (t, k)
+
+
 # ------------------------------------------------------ bounded waits --
 
 def test_wait_time_out_sets_the_error_bit_and_the_next_call_is_correct(ld, di, oracle):
